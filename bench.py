@@ -1,0 +1,431 @@
+#!/usr/bin/env python3
+"""Benchmark: causal attention forward + backward on GB300 through the C ABI.
+
+One step = one pass of the whole path over one batch: rca_attn_fwd, then the
+three backward stages (preprocess, main, dQ convert). Workload: B=4, H=16,
+T=2048, Dh=64, bf16 operands with fp32 accumulation (override with --workload).
+
+Prints ONE JSON line (rank 0). FLOP convention (algorithmic, causal half):
+forward = 4*B*Hq*T^2*Dh/2, backward = 2.5 x forward (five GEMM-shaped products
+including the recompute of P); a step counts 3.5 x forward.
+
+Under torchrun each rank runs its own independent batch of (batch, head) units
+(no data exchange): weak scaling, value = all ranks' FLOPs / max rank time.
+`--impl reference` times the fp64 CPU oracle instead (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import os
+
+# The CPU oracle legs run one BLAS thread per worker thread; set before numpy loads.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import json
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from causal_head_attention_gb300.inputs import BY_NAME, HEADLINE, make_inputs  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+
+
+def fwd_flops(w) -> float:
+    return 4.0 * w.B * w.Hq * w.T * w.T * w.Dh / 2.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def src_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "causal_head_attention_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(kernel)
+    if not e or e.get("src_digest") != src_digest():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open(f"/tmp/rca_clocks_{os.getpid()}.csv", "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.out.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i] and "Not" not in r[5 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, budget_s: float, max_groups: int | None = None):
+    """Run the fp64 oracle (fwd + bwd) on whole (batch, KV-head) groups of the
+    workload, one worker thread per host core, until budget_s has elapsed.
+    Returns (causal FLOPs done, seconds, threads, groups)."""
+    import oracle
+
+    threads = len(os.sched_getaffinity(0))
+    q, k, v, do = make_inputs(w)
+    q64, k64, v64, do64 = (x.double().numpy() for x in (q, k, v, do))
+    groups = [(b, kv) for b in range(w.B) for kv in range(w.Hkv)]
+    if max_groups is not None:
+        groups = groups[:max_groups]
+    per_group = 3.5 * 4.0 * w.group * w.T * w.T * w.Dh / 2.0
+    done = 0
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        it = iter(groups)
+        futs = set()
+        for _ in range(threads):
+            g = next(it, None)
+            if g is not None:
+                futs.add(ex.submit(oracle.group_reference, q64, k64, v64, do64, g[0], g[1]))
+        while futs:
+            fin, futs = cf.wait(futs, return_when=cf.FIRST_COMPLETED)
+            done += len(fin)
+            if time.perf_counter() - t0 < budget_s:
+                for _ in fin:
+                    g = next(it, None)
+                    if g is not None:
+                        futs.add(ex.submit(oracle.group_reference, q64, k64, v64, do64, g[0], g[1]))
+    dt = time.perf_counter() - t0
+    return done * per_group, dt, threads, done
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return 0
+    steps = []
+    flops_step = None
+    threads = len(os.sched_getaffinity(0))
+    for s in range(args.warmup + args.steps):
+        fl, dt, threads, n = oracle_sample(w, 0.0, max_groups=threads)
+        if s >= args.warmup:
+            steps.append(dt)
+            flops_step = fl
+            n_groups = n
+    t = sum(steps)
+    value = flops_step * len(steps) / t / 1e12
+    line = {
+        "impl": "reference", "metric": args.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / len(steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.describe(), "name": w.name, "parallelism": "none (host cores)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n_groups} of {w.B * w.Hkv} (batch, KV-head) groups per step, fwd+bwd, fp64"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, w, world, rank, local):
+    import causal_head_attention_gb300 as rca
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    P = peaks()
+
+    q0, k0, v0, do0 = make_inputs(w)
+    set_bytes = sum(x.numel() * x.element_size() for x in (q0, k0, v0, do0))
+    nsets = max(2, -(-2 * L2_BYTES // set_bytes) + 1)
+    # Distinct copies of the same inputs, so each step reads memory the previous
+    # steps evicted from L2.
+    base = tuple(x.to(dev) for x in (q0, k0, v0, do0))
+    sets = [base] + [tuple(x.clone() for x in base) for _ in range(nsets - 1)]
+    out = torch.empty_like(sets[0][0])
+    lse = torch.empty((w.B, w.Hq, w.T), dtype=torch.float32, device=dev)
+    dq = torch.empty_like(sets[0][0])
+    dk = torch.empty_like(sets[0][1])
+    dv = torch.empty_like(sets[0][2])
+    ws = rca.workspace_for(sets[0][0])
+
+    def step(i, ev=None):
+        q, k, v, do = sets[i % nsets]
+        if ev is not None:
+            ev[0].record(stream)
+        rca.rca_attn_fwd(q, k, v, out, lse, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        rca.rca_attn_bwd_preprocess(out, lse, do, ws, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        rca.rca_attn_bwd_main(q, k, v, do, dk, dv, ws, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        rca.rca_attn_bwd_dq_convert(dq, ws, stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    rca.rca_stream_status(stream)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clk = ClockSampler(local)
+    clk.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i, evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = clk.stop()
+    rca.rca_stream_status(stream)
+    total_ms = t_start.elapsed_time(t_end)
+    per = {"fwd": [], "bwd_preprocess": [], "bwd_main": [], "bwd_dq_convert": []}
+    names = list(per)
+    for e in evs:
+        for j, n in enumerate(names):
+            per[n].append(e[j].elapsed_time(e[j + 1]))
+    avg = {n: sum(v) / len(v) for n, v in per.items()}
+
+    ms = max_over_ranks(total_ms, world) / args.steps
+    F = fwd_flops(w)
+    step_flops = 3.5 * F
+    value = step_flops * world / (ms * 1e-3) / 1e12
+
+    es = 2 if w.dtype == "bf16" else 4
+    n_q = w.B * w.T * w.Hq * w.Dh
+    n_kv = w.B * w.T * w.Hkv * w.Dh
+    Tpad = -(-w.T // 128) * 128
+    pre_bytes = 2 * n_q * es + 4 * w.B * w.Hq * w.T + 8 * w.B * w.Hq * Tpad + 4 * n_q
+    cvt_bytes = 4 * n_q + es * n_q
+    peak_tc = P["bf16_tflops"] if w.dtype == "bf16" else P["bf16_tflops"] / 2.0
+    kern = {
+        "fwd": {"bound": "tensor", "flops": F, "ms": avg["fwd"]},
+        "bwd_main": {"bound": "tensor", "flops": 2.5 * F, "ms": avg["bwd_main"]},
+        "bwd_preprocess": {"bound": "hbm", "bytes": pre_bytes, "ms": avg["bwd_preprocess"]},
+        "bwd_dq_convert": {"bound": "hbm", "bytes": cvt_bytes, "ms": avg["bwd_dq_convert"]},
+    }
+    for n, d in kern.items():
+        if d["bound"] == "tensor":
+            d["achieved"] = d["flops"] / (d["ms"] * 1e-3) / 1e12
+            d["unit"] = "TFLOP/s"
+            d["frac"] = d["achieved"] / peak_tc
+        else:
+            d["achieved"] = d["bytes"] / (d["ms"] * 1e-3) / 1e9
+            d["unit"] = "GB/s"
+            d["frac"] = d["achieved"] / P["hbm_gbs"]
+        d["share"] = d["ms"] / sum(avg.values())
+    dom = max(kern, key=lambda n: kern[n]["ms"])
+    dk_ = kern[dom]
+    roofline = {
+        "kernel": dom, "bound": dk_["bound"], "achieved": dk_["achieved"],
+        "peak": peak_tc if dk_["bound"] == "tensor" else P["hbm_gbs"], "unit": dk_["unit"],
+        "frac": dk_["frac"], "traffic": ncu_traffic(dom, w.name),
+        "peak_source": f"{P['source']} (bf16 burst{'; tf32 = bf16/2 nominal ratio' if w.dtype != 'bf16' else ''})",
+    }
+
+    # End to end: pinned host inputs -> device -> fwd+bwd -> outputs back to pinned host.
+    e2e = None
+    if not args.no_e2e:
+        hq_, hk_, hv_, hdo_ = (x.pin_memory() for x in (q0, k0, v0, do0))
+        ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        hdq = torch.empty(dq.shape, dtype=dq.dtype).pin_memory()
+        hdk = torch.empty(dk.shape, dtype=dk.dtype).pin_memory()
+        hdv = torch.empty(dv.shape, dtype=dv.dtype).pin_memory()
+        dq_, dk_d, dv_d, ddo = sets[0]
+
+        def e2e_step():
+            dq_.copy_(hq_, non_blocking=True)
+            dk_d.copy_(hk_, non_blocking=True)
+            dv_d.copy_(hv_, non_blocking=True)
+            ddo.copy_(hdo_, non_blocking=True)
+            rca.rca_attn_fwd(dq_, dk_d, dv_d, out, lse, stream)
+            rca.rca_attn_bwd(dq_, dk_d, dv_d, out, lse, ddo, dq, dk, dv, ws, stream)
+            ho.copy_(out, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+            hdq.copy_(dq, non_blocking=True)
+            hdk.copy_(dk, non_blocking=True)
+            hdv.copy_(dv, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        a = torch.cuda.Event(enable_timing=True)
+        bev = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        bev.record(stream)
+        torch.cuda.synchronize(dev)
+        rca.rca_stream_status(stream)
+        e_ms = max_over_ranks(a.elapsed_time(bev), world) / args.steps
+        h2d = sum(x.numel() * x.element_size() for x in (hq_, hk_, hv_, hdo_))
+        d2h = sum(x.numel() * x.element_size() for x in (ho, hl, hdq, hdk, hdv))
+        e2e = {"value": step_flops * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        fl, dt, threads, n = oracle_sample(w, args.cpu_budget)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} of {w.B * w.Hkv} (batch, KV-head) groups of the same workload, fwd+bwd, fp64, "
+                         f"{dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": args.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32 (tf32 MMA)", "data": "synthetic",
+            "config": {"workload": w.describe(), "name": w.name, "global_batch": w.B * world, "seq_len": w.T,
+                       "heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.Dh, "parallelism": f"independent units x{world}",
+                       "l2": f"{nsets} rotating input sets ({nsets * set_bytes / 2**20:.0f} MiB) > L2",
+                       "flop_convention": "fwd 4*B*H*T^2*Dh/2; bwd 2.5x fwd; step 3.5x fwd"},
+            "roofline": roofline,
+            "kernels": {n: {k2: (round(v2, 6) if isinstance(v2, float) else v2) for k2, v2 in d.items()}
+                        for n, d in kern.items()},
+            "fwd_frac_of_peak": kern["fwd"]["frac"],
+            "bwd_frac_of_peak": 2.5 * F / ((avg["bwd_preprocess"] + avg["bwd_main"] + avg["bwd_dq_convert"]) * 1e-3) / 1e12 / peak_tc,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "clocks": clocks,
+            "gpu_launches": 4 * args.steps,
+            "src_digest": src_digest(),
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(BY_NAME))
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    args.metric = "causal attn fwd+bwd TFLOP/s at B4 H16 T2048 Dh64 BF16; % of GB300 tensor peak"
+    w = BY_NAME[args.workload]
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        rc = run_reference(args, w, world, rank)
+    else:
+        rc = run_gpu(args, w, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

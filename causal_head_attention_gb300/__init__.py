@@ -1,0 +1,111 @@
+"""GB300 (sm_103a) causal multi-head attention: forward and its VJP.
+
+The computation lives in librca_attn.so (hand-written CUDA, C ABI in
+include/rca_attn.h). This package only allocates outputs with torch and
+marshals pointers; there is no CPU or library fallback.
+"""
+
+from __future__ import annotations
+
+from . import _native
+from ._native import (  # noqa: F401  (C-ABI names)
+    RcaError,
+    rca_abi_version,
+    rca_attn_bwd,
+    rca_attn_bwd_dq_convert,
+    rca_attn_bwd_main,
+    rca_attn_bwd_preprocess,
+    rca_attn_bwd_workspace_size,
+    rca_attn_fwd,
+    rca_last_error,
+    rca_set_wait_timeout_ns,
+    rca_stream_status,
+)
+
+__all__ = [
+    "attention_forward",
+    "attention_backward",
+    "CausalAttention",
+    "causal_attention",
+    "RcaError",
+    "rca_abi_version",
+    "rca_attn_fwd",
+    "rca_attn_bwd",
+    "rca_attn_bwd_workspace_size",
+    "rca_attn_bwd_preprocess",
+    "rca_attn_bwd_main",
+    "rca_attn_bwd_dq_convert",
+    "rca_stream_status",
+    "rca_last_error",
+    "rca_set_wait_timeout_ns",
+]
+
+
+def attention_forward(q, k, v, stream=None):
+    """Returns (out [B,T,Hq,Dh] in q's dtype, lse [B,Hq,T] float32)."""
+    import torch
+
+    B, T, Hq, Dh = q.shape
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    rca_attn_fwd(q, k, v, out, lse, stream)
+    return out, lse
+
+
+def workspace_for(q):
+    import torch
+
+    B, T, Hq, Dh = q.shape
+    n = rca_attn_bwd_workspace_size(B, Hq, T, Dh)
+    return torch.empty(n, dtype=torch.uint8, device=q.device)
+
+
+def attention_backward(q, k, v, out, lse, dout, workspace=None, stream=None):
+    """Returns (dq, dk, dv) in the storage dtype."""
+    import torch
+
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    ws = workspace if workspace is not None else workspace_for(q)
+    rca_attn_bwd(q, k, v, out, lse, dout.contiguous(), dq, dk, dv, ws, stream)
+    return dq, dk, dv
+
+
+def _autograd_cls():
+    import torch
+
+    class CausalAttention(torch.autograd.Function):
+        """torch.autograd wrapper: saves q, k, v, out and lse; backward recomputes P."""
+
+        @staticmethod
+        def forward(ctx, q, k, v):
+            out, lse = attention_forward(q, k, v)
+            ctx.save_for_backward(q, k, v, out, lse)
+            return out
+
+        @staticmethod
+        def backward(ctx, dout):
+            q, k, v, out, lse = ctx.saved_tensors
+            return attention_backward(q, k, v, out, lse, dout)
+
+    return CausalAttention
+
+
+class _Lazy:
+    cls = None
+
+
+def causal_attention(q, k, v):
+    """Differentiable causal attention over [B,T,H,Dh] tensors (GQA when Hkv < Hq)."""
+    if _Lazy.cls is None:
+        _Lazy.cls = _autograd_cls()
+    return _Lazy.cls.apply(q, k, v)
+
+
+def __getattr__(name):
+    if name == "CausalAttention":
+        if _Lazy.cls is None:
+            _Lazy.cls = _autograd_cls()
+        return _Lazy.cls
+    raise AttributeError(name)

@@ -1,0 +1,179 @@
+"""ctypes binding of librca_attn.so: the C ABI in include/rca_attn.h, same names.
+
+Argument marshalling only: tensors are turned into device pointers and sizes,
+and every step of the computation runs in the library's CUDA kernels. There is
+no CPU fallback: if the library is missing or fails to load, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "librca_attn.so")
+
+RCA_OK = 0
+RCA_ERR_INVALID_ARGUMENT = 1
+RCA_ERR_UNSUPPORTED = 2
+RCA_ERR_CUDA = 3
+RCA_ERR_DEVICE_TIMEOUT = 4
+RCA_F32_TF32 = 0
+RCA_BF16 = 1
+
+STATUS_NAMES = {
+    0: "RCA_OK",
+    1: "RCA_ERR_INVALID_ARGUMENT",
+    2: "RCA_ERR_UNSUPPORTED",
+    3: "RCA_ERR_CUDA",
+    4: "RCA_ERR_DEVICE_TIMEOUT",
+}
+
+# Every symbol include/rca_attn.h declares, with its ctypes signature.
+_P = ctypes.c_void_p
+_I = ctypes.c_int64
+_SIG = {
+    "rca_abi_version": (ctypes.c_uint32, []),
+    "rca_last_error": (ctypes.c_char_p, []),
+    "rca_attn_fwd": (ctypes.c_int, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_int, _P]),
+    "rca_attn_bwd_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "rca_attn_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                    ctypes.c_int, _P, ctypes.c_size_t, _P]),
+    "rca_attn_bwd_preprocess": (ctypes.c_int, [_P, _P, _P, _I, _I, _I, _I, ctypes.c_int, _P,
+                                               ctypes.c_size_t, _P]),
+    "rca_attn_bwd_main": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_int,
+                                         _P, ctypes.c_size_t, _P]),
+    "rca_attn_bwd_dq_convert": (ctypes.c_int, [_P, _I, _I, _I, _I, ctypes.c_int, _P,
+                                               ctypes.c_size_t, _P]),
+    "rca_stream_status": (ctypes.c_int, [_P]),
+    "rca_set_wait_timeout_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
+}
+
+_lib = None
+
+
+class RcaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+
+
+def lib() -> ctypes.CDLL:
+    """Load librca_attn.so (built in-tree by causal_head_attention_gb300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m causal_head_attention_gb300.build` "
+                "(the CUDA library is the only implementation; there is no fallback)"
+            )
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIG.items():
+            f = getattr(l, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = l
+    return _lib
+
+
+def _check(status: int):
+    if status != RCA_OK:
+        raise RcaError(status, lib().rca_last_error().decode(errors="replace"))
+
+
+# ---------------------------------------------------------------------------
+# torch-tensor marshalling
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return RCA_BF16
+    if t.dtype == torch.float32:
+        return RCA_F32_TF32
+    raise TypeError(f"unsupported dtype {t.dtype}: expected torch.bfloat16 or torch.float32")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("all tensors must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("all tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _shape(q, k):
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q must be [B,T,Hq,Dh] and k, v [B,T,Hkv,Dh]")
+    B, T, Hq, Dh = q.shape
+    return B, Hq, k.shape[2], T, Dh
+
+
+def rca_abi_version() -> int:
+    return lib().rca_abi_version()
+
+
+def rca_last_error() -> str:
+    return lib().rca_last_error().decode(errors="replace")
+
+
+def rca_set_wait_timeout_ns(ns: int) -> int:
+    return lib().rca_set_wait_timeout_ns(ns)
+
+
+def rca_attn_fwd(q, k, v, out, lse, stream=None):
+    B, Hq, Hkv, T, Dh = _shape(q, k)
+    _check(lib().rca_attn_fwd(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, T, Dh, _ptr(out), _ptr(lse),
+                              _dtype_code(q), _stream(stream)))
+
+
+def rca_attn_bwd_workspace_size(B, Hq, T, Dh) -> int:
+    return lib().rca_attn_bwd_workspace_size(B, Hq, T, Dh)
+
+
+def rca_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, workspace, stream=None):
+    B, Hq, Hkv, T, Dh = _shape(q, k)
+    _check(lib().rca_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
+                              _ptr(dk), _ptr(dv), B, Hq, Hkv, T, Dh, _dtype_code(q), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def rca_attn_bwd_preprocess(out, lse, dout, workspace, stream=None):
+    B, T, Hq, Dh = out.shape
+    _check(lib().rca_attn_bwd_preprocess(_ptr(out), _ptr(lse), _ptr(dout), B, Hq, T, Dh, _dtype_code(out),
+                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                         _stream(stream)))
+
+
+def rca_attn_bwd_main(q, k, v, dout, dk, dv, workspace, stream=None):
+    B, Hq, Hkv, T, Dh = _shape(q, k)
+    _check(lib().rca_attn_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dk), _ptr(dv), B, Hq, Hkv, T,
+                                   Dh, _dtype_code(q), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def rca_attn_bwd_dq_convert(dq, workspace, stream=None):
+    B, T, Hq, Dh = dq.shape
+    _check(lib().rca_attn_bwd_dq_convert(_ptr(dq), B, Hq, T, Dh, _dtype_code(dq), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def rca_stream_status(stream=None):
+    _check(lib().rca_stream_status(_stream(stream)))

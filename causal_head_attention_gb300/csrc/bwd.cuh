@@ -1,0 +1,469 @@
+// Causal attention backward (vector-Jacobian product) for sm_103a.
+//
+// The riftco-transformer page "Execution Backends and the Python ABI", section
+// "What the Metal slice does", specifies the memory-linear backward: scores and
+// probabilities are recomputed from Q, K and the saved per-row statistics
+// instead of reading a stored [T,T] probability tensor. With P = exp(S - LSE)
+// the softmax VJP is
+//   D = rowsum(dO * O),  dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),
+//   dQ = scale dS K,     dK = scale dS^T Q.
+// Grouped-query attention (algo-v1-codepoint "docs/ARCHITECTURE.md",
+// "config.py"): dK and dV sum over the query heads that share a KV head.
+//
+// Three kernels:
+//   attn_bwd_preprocess_kernel  D, LSE in base 2 (padded rows: D = 0, LSE = +inf),
+//                               zeroes the fp32 dQ accumulator. HBM-bound.
+//   attn_bwd_main_kernel        one CTA per (batch, KV head, 128-key tile j); loops
+//                               over every query head of the group and every query
+//                               tile i >= j; dK, dV accumulate in TMEM; dQ partials
+//                               are added into the fp32 accumulator.
+//   attn_bwd_dq_convert_kernel  dQ = scale * accumulator in the storage dtype.
+#pragma once
+
+#include "tc.cuh"
+
+namespace rca {
+
+// ----------------------------------------------------------------------------
+// preprocess
+// ----------------------------------------------------------------------------
+struct PreArgs {
+  const void* out;
+  const float* lse;
+  const void* dout;
+  float* dq_acc;  // [B, T, Hq, Dh]
+  float* lse2;    // [B, Hq, Tpad]
+  float* dvec;    // [B, Hq, Tpad]
+  int B, Hq, T, Dh, Tpad;
+};
+
+// A group of LPR consecutive lanes handles one (b, t, h) row of Dh elements,
+// each lane 16 bytes, so every load instruction is fully coalesced.
+template <bool F32>
+__global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const PreArgs a) {
+  constexpr int ES = F32 ? 4 : 2;
+  constexpr int EPL = 16 / ES;  // elements per lane
+  const int lpr = a.Dh / EPL;   // lanes per row: power of two in [2, 32]
+  const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long rows = static_cast<long long>(a.B) * a.Tpad * a.Hq;
+  const long long row = gid / lpr;
+  const int part = static_cast<int>(gid % lpr);
+  const bool in = row < rows;
+  int b = 0, t = 0, h = 0;
+  if (in) {
+    h = static_cast<int>(row % a.Hq);
+    const long long bt = row / a.Hq;
+    t = static_cast<int>(bt % a.Tpad);
+    b = static_cast<int>(bt / a.Tpad);
+  }
+  const bool live = in && t < a.T;
+  float acc = 0.f;
+  if (live) {
+    const size_t off = ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * a.Dh + part * EPL;
+    const uint4 o = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.out) + off * ES);
+    const uint4 g = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.dout) + off * ES);
+    const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if constexpr (F32) {
+        acc = fmaf(__uint_as_float(ow[i]), __uint_as_float(gw[i]), acc);
+      } else {
+        const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[i]));
+        const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[i]));
+        acc = fmaf(of.x, gf.x, acc);
+        acc = fmaf(of.y, gf.y, acc);
+      }
+    }
+    float4* z = reinterpret_cast<float4*>(a.dq_acc + off);
+#pragma unroll
+    for (int i = 0; i < EPL / 4; ++i) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int o = lpr >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, lpr);
+  if (in && part == 0) {
+    const size_t so = (static_cast<size_t>(b) * a.Hq + h) * a.Tpad + t;
+    a.dvec[so] = live ? acc : 0.f;
+    a.lse2[so] = live ? a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.T + t] * 1.4426950408889634f
+                      : INFINITY;
+  }
+}
+
+// ----------------------------------------------------------------------------
+// dQ convert
+// ----------------------------------------------------------------------------
+template <bool F32>
+__global__ void __launch_bounds__(256)
+    attn_bwd_dq_convert_kernel(const float* __restrict__ acc, void* __restrict__ dq, long long n4,
+                               float scale) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const float4 v = reinterpret_cast<const float4*>(acc)[i];
+    if constexpr (F32) {
+      reinterpret_cast<float4*>(dq)[i] = make_float4(v.x * scale, v.y * scale, v.z * scale, v.w * scale);
+    } else {
+      reinterpret_cast<uint2*>(dq)[i] = make_uint2(pack_bf16(v.x * scale, v.y * scale),
+                                                   pack_bf16(v.z * scale, v.w * scale));
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// main
+// ----------------------------------------------------------------------------
+template <bool TF32, int DHP>
+struct BwdCfg {
+  static constexpr int ES = TF32 ? 4 : 2;
+  static constexpr int PE = 128 / ES;
+  static constexpr int PANEL = 128 * 128;
+  static constexpr int DPANELS = DHP / PE;
+  static constexpr int KV_BYTES = DPANELS * PANEL;  // K or V tile (128 keys)
+  static constexpr int QT_BYTES = DPANELS * PANEL;  // Q or dO tile (128 queries)
+  static constexpr int P_BYTES = (128 / PE) * PANEL;
+  static constexpr int KSTEP = TF32 ? 8 : 16;
+  static constexpr int SPP = PE / KSTEP;
+  static constexpr int SMEM_LIMIT = 232448;
+  static constexpr int BAR_BYTES = 1024;
+  static constexpr int STAGE_BYTES = 2 * QT_BYTES + 1024;  // Q, dO, LSE2[128], D[128]
+  static constexpr int AVAIL = SMEM_LIMIT - 1024 - BAR_BYTES - 2 * KV_BYTES;
+  static constexpr int NQS_SEP = (AVAIL - 2 * P_BYTES) / STAGE_BYTES;
+  static constexpr int NQS_SHR = (AVAIL - P_BYTES) / STAGE_BYTES;
+  // P^T and dS^T share one buffer only when separate buffers leave < 2 stages.
+  static constexpr bool SHARE = NQS_SEP < 2 && NQS_SHR > NQS_SEP;
+  static constexpr int NQS_RAW = SHARE ? NQS_SHR : NQS_SEP;
+  static constexpr int NQS = NQS_RAW > 4 ? 4 : NQS_RAW;
+  static_assert(NQS >= 1, "backward needs at least one Q/dO stage");
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = KV_BYTES;
+  static constexpr int OFF_P = 2 * KV_BYTES;
+  static constexpr int OFF_DS = SHARE ? OFF_P : OFF_P + P_BYTES;
+  static constexpr int OFF_STAGE = OFF_DS + P_BYTES;
+  static constexpr int OFF_BAR = OFF_STAGE + NQS * STAGE_BYTES;
+  static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;
+  static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
+  // TMEM columns
+  static constexpr int TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + DHP;
+  static constexpr bool DQ_ALIAS = 256 + 3 * DHP > 512;
+  static constexpr int TM_DQ = DQ_ALIAS ? 0 : 256 + 2 * DHP;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr uint32_t IDESC_T = make_idesc(TF32, 128, 128, false, false);   // S^T, dP^T
+  static constexpr uint32_t IDESC_KV = make_idesc(TF32, 128, DHP, false, true);   // dV, dK
+  static constexpr uint32_t IDESC_Q = make_idesc(TF32, 128, DHP, true, true);     // dQ
+  // barriers
+  static constexpr int B_KV = 0;
+  static constexpr int B_QF = 1;
+  static constexpr int B_QE = B_QF + NQS;
+  static constexpr int B_SDP = B_QE + NQS;
+  static constexpr int B_PR = B_SDP + 1;
+  static constexpr int B_DVD = B_PR + 1;
+  static constexpr int B_DSR = B_DVD + 1;
+  static constexpr int B_DQF = B_DSR + 1;
+  static constexpr int B_ITF = B_DQF + 1;
+  static constexpr int B_FIN = B_ITF + 1;
+  static constexpr int NBAR = B_FIN + 1;
+};
+
+struct BwdArgs {
+  void* dk;
+  void* dv;
+  float* dq_acc;       // [B, T, Hq, Dh]
+  const float* lse2;   // [B, Hq, Tpad]
+  const float* dvec;   // [B, Hq, Tpad]
+  int* status;
+  unsigned long long timeout_ns;
+  int B, Hq, Hkv, T, Dh, group, n_t, Tpad;
+  float scale, scale_log2;
+};
+
+template <bool TF32, int DHP>
+__global__ void __launch_bounds__(192, 1)
+    attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                         const BwdArgs a) {
+  using C = BwdCfg<TF32, DHP>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * i; };
+  auto stage = [&](int s) -> uint32_t { return sbase + C::OFF_STAGE + s * C::STAGE_BYTES; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * C::NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 8 * C::NBAR + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bk_count = a.B * a.Hkv;
+  const int lin = blockIdx.x;
+  const int j = lin / bk_count;  // key tile; small j = most work, scheduled first
+  const int bk = lin % bk_count;
+  const int b = bk / a.Hkv, kvh = bk % a.Hkv;
+  const int n_i = a.n_t - j;           // query tiles j .. n_t-1
+  const int n_it = a.group * n_i;      // times every query head of the group
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::B_KV), 1);
+    for (int s = 0; s < C::NQS; ++s) {
+      mbar_init(bar(C::B_QF + s), 1);
+      mbar_init(bar(C::B_QE + s), 1);
+    }
+    mbar_init(bar(C::B_SDP), 1);
+    mbar_init(bar(C::B_PR), 128);
+    mbar_init(bar(C::B_DVD), 1);
+    mbar_init(bar(C::B_DSR), 128);
+    mbar_init(bar(C::B_DQF), 1);
+    mbar_init(bar(C::B_ITF), 128);
+    mbar_init(bar(C::B_FIN), 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl w{a.status, abort_flag, a.timeout_ns};
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmdO);
+      mbar_expect_tx(bar(C::B_KV), 2 * C::KV_BYTES);
+      for (int p = 0; p < C::DPANELS; ++p) {
+        tma_load_4d(sbase + C::OFF_K + p * C::PANEL, &tmK, bar(C::B_KV), p * C::PE, kvh, j * 128, b);
+        tma_load_4d(sbase + C::OFF_V + p * C::PANEL, &tmV, bar(C::B_KV), p * C::PE, kvh, j * 128, b);
+      }
+      int it = 0;
+      for (; it < n_it; ++it) {
+        const int s = it % C::NQS;
+        if (it >= C::NQS && !mbar_wait(bar(C::B_QE + s), ((it / C::NQS) - 1) & 1, w)) break;
+        const int h = kvh * a.group + it / n_i;
+        const int i = j + it % n_i;
+        const uint32_t st = stage(s);
+        mbar_expect_tx(bar(C::B_QF + s), 2 * C::QT_BYTES + 1024);
+        for (int p = 0; p < C::DPANELS; ++p) {
+          tma_load_4d(st + p * C::PANEL, &tmQ, bar(C::B_QF + s), p * C::PE, h, i * 128, b);
+          tma_load_4d(st + C::QT_BYTES + p * C::PANEL, &tmdO, bar(C::B_QF + s), p * C::PE, h, i * 128, b);
+        }
+        const size_t ro = (static_cast<size_t>(b) * a.Hq + h) * a.Tpad + static_cast<size_t>(i) * 128;
+        bulk_load(st + 2 * C::QT_BYTES, a.lse2 + ro, 512, bar(C::B_QF + s));
+        bulk_load(st + 2 * C::QT_BYTES + 512, a.dvec + ro, 512, bar(C::B_QF + s));
+      }
+      mbar_drain(bar(C::B_KV), 0, a.timeout_ns);
+      for (int s = 0; s < C::NQS && s < it; ++s) {
+        const int last = s + ((it - 1 - s) / C::NQS) * C::NQS;
+        mbar_drain(bar(C::B_QF + s), (last / C::NQS) & 1, a.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- tcgen05 MMA issuer ----------------
+    if (lane == 0) {
+      bool ok = mbar_wait(bar(C::B_KV), 0, w);
+      const uint32_t kb = sbase + C::OFF_K, vb = sbase + C::OFF_V;
+      const uint32_t pb = sbase + C::OFF_P, dsb = sbase + C::OFF_DS;
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int s = it % C::NQS;
+        const uint32_t qb = stage(s), dob = stage(s) + C::QT_BYTES;
+        if (!mbar_wait(bar(C::B_QF + s), (it / C::NQS) & 1, w)) { ok = false; break; }
+        if (it > 0 && !mbar_wait(bar(C::B_ITF), (it - 1) & 1, w)) { ok = false; break; }
+        tc_fence_after();
+        // S^T = K Q^T and dP^T = V dO^T   (M = keys, N = queries, K = head dim)
+#pragma unroll
+        for (int k = 0; k < DHP / C::KSTEP; ++k) {
+          const uint32_t off = (k / C::SPP) * C::PANEL + (k % C::SPP) * 32;
+          mma_ss<TF32>(tmem + C::TM_S, make_sdesc(kb + off, 16, 1024), make_sdesc(qb + off, 16, 1024),
+                       C::IDESC_T, k > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < DHP / C::KSTEP; ++k) {
+          const uint32_t off = (k / C::SPP) * C::PANEL + (k % C::SPP) * 32;
+          mma_ss<TF32>(tmem + C::TM_DP, make_sdesc(vb + off, 16, 1024), make_sdesc(dob + off, 16, 1024),
+                       C::IDESC_T, k > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(C::B_SDP));
+        // dV += P^T dO   (M = keys, N = head dim, K = queries)
+        if (!mbar_wait(bar(C::B_PR), it & 1, w)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 128 / C::KSTEP; ++k) {
+          const uint32_t aoff = (k / C::SPP) * C::PANEL + (k % C::SPP) * 32;
+          mma_ss<TF32>(tmem + C::TM_DV, make_sdesc(pb + aoff, 16, 1024),
+                       make_sdesc(dob + k * C::KSTEP * 128, C::PANEL, 1024), C::IDESC_KV,
+                       (it > 0 || k > 0) ? 1u : 0u);
+        }
+        if constexpr (C::SHARE) tc_commit(bar(C::B_DVD));
+        // dK += dS^T Q   and   dQ_partial = dS K
+        if (!mbar_wait(bar(C::B_DSR), it & 1, w)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 128 / C::KSTEP; ++k) {
+          const uint32_t aoff = (k / C::SPP) * C::PANEL + (k % C::SPP) * 32;
+          mma_ss<TF32>(tmem + C::TM_DK, make_sdesc(dsb + aoff, 16, 1024),
+                       make_sdesc(qb + k * C::KSTEP * 128, C::PANEL, 1024), C::IDESC_KV,
+                       (it > 0 || k > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < 128 / C::KSTEP; ++k) {
+          mma_ss<TF32>(tmem + C::TM_DQ, make_sdesc(dsb + k * C::KSTEP * 128, C::PANEL, 1024),
+                       make_sdesc(kb + k * C::KSTEP * 128, C::PANEL, 1024), C::IDESC_Q,
+                       k > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(C::B_DQF));
+        tc_commit(bar(C::B_QE + s));
+      }
+      tc_commit(bar(C::B_FIN));
+      mbar_drain(bar(C::B_FIN), 0, a.timeout_ns);
+    }
+  } else {
+    // ---------------- compute warpgroup ----------------
+    const int quarter = warp & 3;
+    const int rl = quarter * 32 + lane;  // key row for P^T/dS^T, query row for dQ
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float sl2 = a.scale_log2;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it % C::NQS;
+      const int h = kvh * a.group + it / n_i;
+      const int i = j + it % n_i;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SDP), it & 1, w) &&
+                                       mbar_wait(bar(C::B_QF + s), (it / C::NQS) & 1, w));
+      if (!ok) break;
+      tc_fence_after();
+      const float* lse2s = reinterpret_cast<const float*>(smem + (stage(s) - sbase) + 2 * C::QT_BYTES);
+      const float* ds_ = lse2s + 128;
+      float p[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tl + C::TM_S + c * 32, r);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) p[c * 32 + q] = __uint_as_float(r[q]);
+      }
+      const bool diag = (i == j);
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const float e = ex2(fmaf(p[c], sl2, -lse2s[c]));
+        p[c] = (diag && c < rl) ? 0.f : e;  // key rl is after query c: dropped
+      }
+      const uint32_t prow = sbase + C::OFF_P + rl * 128;
+      const uint32_t dsrow = sbase + C::OFF_DS + rl * 128;
+      if constexpr (TF32) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          st_shared_v4(prow + (c >> 3) * C::PANEL + (((c & 7) ^ (rl & 7)) << 4), to_tf32(p[4 * c]),
+                       to_tf32(p[4 * c + 1]), to_tf32(p[4 * c + 2]), to_tf32(p[4 * c + 3]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          st_shared_v4(prow + (c >> 3) * C::PANEL + (((c & 7) ^ (rl & 7)) << 4),
+                       pack_bf16(p[8 * c], p[8 * c + 1]), pack_bf16(p[8 * c + 2], p[8 * c + 3]),
+                       pack_bf16(p[8 * c + 4], p[8 * c + 5]), pack_bf16(p[8 * c + 6], p[8 * c + 7]));
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_PR));
+      // dS^T = P^T * (dP^T - D)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tl + C::TM_DP + c * 32, r);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) p[c * 32 + q] = p[c * 32 + q] * (__uint_as_float(r[q]) - ds_[c * 32 + q]);
+      }
+      if constexpr (C::SHARE) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DVD), it & 1, w));
+        if (!ok) break;
+      }
+      if constexpr (TF32) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          st_shared_v4(dsrow + (c >> 3) * C::PANEL + (((c & 7) ^ (rl & 7)) << 4), to_tf32(p[4 * c]),
+                       to_tf32(p[4 * c + 1]), to_tf32(p[4 * c + 2]), to_tf32(p[4 * c + 3]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          st_shared_v4(dsrow + (c >> 3) * C::PANEL + (((c & 7) ^ (rl & 7)) << 4),
+                       pack_bf16(p[8 * c], p[8 * c + 1]), pack_bf16(p[8 * c + 2], p[8 * c + 3]),
+                       pack_bf16(p[8 * c + 4], p[8 * c + 5]), pack_bf16(p[8 * c + 6], p[8 * c + 7]));
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_DSR));
+      // dQ partial for query row rl of tile i -> fp32 accumulator
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DQF), it & 1, w));
+      if (!ok) break;
+      tc_fence_after();
+      const int qrow = i * 128 + rl;
+      float* dst = a.dq_acc + ((static_cast<size_t>(b) * a.T + qrow) * a.Hq + h) * a.Dh;
+#pragma unroll
+      for (int c = 0; c < DHP / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tl + C::TM_DQ + c * 32, r);
+        const int ncol = a.Dh - c * 32;
+        if (qrow < a.T && ncol > 0) {
+          const int nv = (ncol >= 32 ? 32 : ncol) / 4;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (u < nv)
+              atomicAdd(reinterpret_cast<float4*>(dst + c * 32) + u,
+                        make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                                    __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::B_ITF));
+    }
+    if (ok) {
+      // The last dQ commit covered every MMA, including the final dK/dV updates.
+      tc_fence_after();
+      const int key = j * 128 + rl;
+      const bool valid = key < a.T;
+      const size_t row_off = ((static_cast<size_t>(b) * a.T + key) * a.Hkv + kvh) * a.Dh;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col0 = which == 0 ? C::TM_DV : C::TM_DK;
+        const float mul = which == 0 ? 1.f : a.scale;
+        void* base = which == 0 ? a.dv : a.dk;
+#pragma unroll
+        for (int c = 0; c < DHP / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tl + col0 + c * 32, r);
+          const int ncol = a.Dh - c * 32;
+          if (!valid || ncol <= 0) continue;
+          if constexpr (TF32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(base) + row_off + c * 32);
+            const int nv = (ncol >= 32 ? 32 : ncol) / 4;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              if (u < nv)
+                dst[u] = make_float4(__uint_as_float(r[4 * u]) * mul, __uint_as_float(r[4 * u + 1]) * mul,
+                                     __uint_as_float(r[4 * u + 2]) * mul, __uint_as_float(r[4 * u + 3]) * mul);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + row_off + c * 32);
+            const int nv = (ncol >= 32 ? 32 : ncol) / 8;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (u < nv)
+                dst[u] = make_uint4(
+                    pack_bf16(__uint_as_float(r[8 * u]) * mul, __uint_as_float(r[8 * u + 1]) * mul),
+                    pack_bf16(__uint_as_float(r[8 * u + 2]) * mul, __uint_as_float(r[8 * u + 3]) * mul),
+                    pack_bf16(__uint_as_float(r[8 * u + 4]) * mul, __uint_as_float(r[8 * u + 5]) * mul),
+                    pack_bf16(__uint_as_float(r[8 * u + 6]) * mul, __uint_as_float(r[8 * u + 7]) * mul));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace rca

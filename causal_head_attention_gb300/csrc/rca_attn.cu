@@ -1,0 +1,441 @@
+// C ABI of librca_attn.so: argument validation, TMA descriptor encoding and
+// kernel launches on the caller's stream. See include/rca_attn.h for the
+// contract (layouts, ownership, errors).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "rca_attn.h"
+#include "bwd.cuh"
+#include "fwd.cuh"
+
+namespace {
+
+thread_local std::string g_err;
+
+rca_status fail(rca_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+rca_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(RCA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+
+// ---------------------------------------------------------------------------
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+// ---------------------------------------------------------------------------
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                              CUtensorMapFloatOOBfill);
+EncodeFn g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+EncodeFn get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                    cudaEnableDefault, &q);
+    if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeFn>(fn);
+  });
+  return g_encode;
+}
+
+// [B, T, H, Dh] row-major tensor, tiles of 128 rows (positions) x one 128-byte
+// panel of the head dimension, 128-byte swizzle. Positions past T and head
+// columns past Dh read as zero.
+rca_status make_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t H, int64_t Dh,
+                    bool f32, const char* name) {
+  EncodeFn enc = get_encode();
+  if (!enc) return fail(RCA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorName(g_encode_err));
+  const uint64_t es = f32 ? 4 : 2;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(Dh), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(Dh * es), static_cast<cuuint64_t>(H * Dh * es),
+                           static_cast<cuuint64_t>(T * H * Dh * es)};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / es), 1, 128, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(RCA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name, (int)r);
+  return RCA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Per-device status word (device timeouts), allocated on first use.
+// ---------------------------------------------------------------------------
+std::mutex g_status_mu;
+int* g_status[256] = {};
+
+rca_status status_word(int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 256) return fail(RCA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_status_mu);
+  if (!g_status[dev]) {
+    int* p = nullptr;
+    e = cudaMalloc(&p, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(status word)");
+    e = cudaMemset(p, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(status word)");
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    g_status[dev] = p;
+  }
+  *out = g_status[dev];
+  return RCA_OK;
+}
+
+template <typename K>
+cudaError_t ensure_smem(K kernel, int bytes, std::atomic<unsigned long long>& mask) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (mask.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) mask.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+// ---------------------------------------------------------------------------
+// Validation
+// ---------------------------------------------------------------------------
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+rca_status check_shape(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt) {
+  if (B < 1 || Hq < 1 || Hkv < 1)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "B, Hq and Hkv must be >= 1 (got B=%lld Hq=%lld Hkv=%lld)",
+                (long long)B, (long long)Hq, (long long)Hkv);
+  if (T < 1)
+    return fail(RCA_ERR_INVALID_ARGUMENT,
+                "T must be >= 1 (got %lld): an empty causal row is a fully masked softmax slice",
+                (long long)T);
+  if (Hq % Hkv != 0)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "grouped-query attention needs Hq %% Hkv == 0 (Hq=%lld Hkv=%lld)",
+                (long long)Hq, (long long)Hkv);
+  if (dt != RCA_BF16 && dt != RCA_F32_TF32)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "unknown dtype %d", (int)dt);
+  const bool ok_dh = Dh == 16 || Dh == 32 || Dh == 64 || (Dh == 128 && dt == RCA_BF16);
+  if (!ok_dh)
+    return fail(RCA_ERR_UNSUPPORTED,
+                "head width Dh=%lld is not supported for %s (supported: 16, 32, 64%s)", (long long)Dh,
+                dt == RCA_BF16 ? "bf16" : "fp32/tf32", dt == RCA_BF16 ? ", 128" : "");
+  const int64_t n_t = (T + 127) / 128;
+  if (T > (int64_t(1) << 30) || B * Hq * n_t > 0x7fffffffLL || B * T * Hq * Dh > (int64_t(1) << 38))
+    return fail(RCA_ERR_INVALID_ARGUMENT, "problem too large (B=%lld T=%lld Hq=%lld Dh=%lld)",
+                (long long)B, (long long)T, (long long)Hq, (long long)Dh);
+  return RCA_OK;
+}
+
+struct WsLayout {
+  size_t dq_off, lse2_off, d_off, total;
+  int64_t Tpad;
+};
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+WsLayout ws_layout(int64_t B, int64_t Hq, int64_t T, int64_t Dh) {
+  WsLayout w{};
+  w.Tpad = (T + 127) / 128 * 128;
+  w.dq_off = 0;
+  w.lse2_off = round256(size_t(B) * T * Hq * Dh * 4);
+  w.d_off = w.lse2_off + round256(size_t(B) * Hq * w.Tpad * 4);
+  w.total = w.d_off + round256(size_t(B) * Hq * w.Tpad * 4);
+  return w;
+}
+
+rca_status check_ws(const void* ws, size_t bytes, const WsLayout& L) {
+  if (!ws) return fail(RCA_ERR_INVALID_ARGUMENT, "workspace is null");
+  if (reinterpret_cast<uintptr_t>(ws) & 255u)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
+  if (bytes < L.total)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "workspace too small: %zu bytes given, %zu needed", bytes, L.total);
+  return RCA_OK;
+}
+
+#define RCA_CHECK(x)              \
+  do {                            \
+    rca_status _s = (x);          \
+    if (_s != RCA_OK) return _s;  \
+  } while (0)
+
+#define RCA_GUARD_BEGIN try {
+#define RCA_GUARD_END                                                  \
+  }                                                                    \
+  catch (...) {                                                        \
+    return fail(RCA_ERR_CUDA, "internal error (C++ exception caught)"); \
+  }
+
+// ---------------------------------------------------------------------------
+// Launchers
+// ---------------------------------------------------------------------------
+template <bool TF32, int DHP>
+rca_status launch_fwd(const void* q, const void* k, const void* v, int64_t B, int64_t Hq, int64_t Hkv,
+                      int64_t T, int64_t Dh, void* out, float* lse, cudaStream_t st) {
+  using C = rca::FwdCfg<TF32, DHP>;
+  static std::atomic<unsigned long long> smem_set{0};
+  CUtensorMap mq, mk, mv;
+  RCA_CHECK(make_map(&mq, q, B, T, Hq, Dh, TF32, "q"));
+  RCA_CHECK(make_map(&mk, k, B, T, Hkv, Dh, TF32, "k"));
+  RCA_CHECK(make_map(&mv, v, B, T, Hkv, Dh, TF32, "v"));
+  int* status = nullptr;
+  RCA_CHECK(status_word(&status));
+  auto kern = rca::attn_fwd_kernel<TF32, DHP>;
+  cudaError_t e = ensure_smem(kern, C::SMEM_BYTES, smem_set);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fwd)");
+  rca::FwdArgs a{};
+  a.out = out;
+  a.lse = lse;
+  a.status = status;
+  a.timeout_ns = g_timeout_ns.load();
+  a.B = int(B); a.Hq = int(Hq); a.Hkv = int(Hkv); a.T = int(T); a.Dh = int(Dh);
+  a.group = int(Hq / Hkv);
+  a.n_qt = int((T + 127) / 128);
+  a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(Dh)));
+  const unsigned grid = unsigned(int64_t(a.n_qt) * B * Hq);
+  kern<<<grid, 192, C::SMEM_BYTES, st>>>(mq, mk, mv, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch attn_fwd_kernel");
+  return RCA_OK;
+}
+
+template <bool TF32, int DHP>
+rca_status launch_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
+                           int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, void* ws,
+                           const WsLayout& L, cudaStream_t st) {
+  using C = rca::BwdCfg<TF32, DHP>;
+  static std::atomic<unsigned long long> smem_set{0};
+  CUtensorMap mq, mk, mv, mdo;
+  RCA_CHECK(make_map(&mq, q, B, T, Hq, Dh, TF32, "q"));
+  RCA_CHECK(make_map(&mk, k, B, T, Hkv, Dh, TF32, "k"));
+  RCA_CHECK(make_map(&mv, v, B, T, Hkv, Dh, TF32, "v"));
+  RCA_CHECK(make_map(&mdo, dout, B, T, Hq, Dh, TF32, "dout"));
+  int* status = nullptr;
+  RCA_CHECK(status_word(&status));
+  auto kern = rca::attn_bwd_main_kernel<TF32, DHP>;
+  cudaError_t e = ensure_smem(kern, C::SMEM_BYTES, smem_set);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  rca::BwdArgs a{};
+  a.dk = dk;
+  a.dv = dv;
+  a.dq_acc = reinterpret_cast<float*>(w + L.dq_off);
+  a.lse2 = reinterpret_cast<const float*>(w + L.lse2_off);
+  a.dvec = reinterpret_cast<const float*>(w + L.d_off);
+  a.status = status;
+  a.timeout_ns = g_timeout_ns.load();
+  a.B = int(B); a.Hq = int(Hq); a.Hkv = int(Hkv); a.T = int(T); a.Dh = int(Dh);
+  a.group = int(Hq / Hkv);
+  a.n_t = int((T + 127) / 128);
+  a.Tpad = int(L.Tpad);
+  a.scale = float(1.0 / std::sqrt(double(Dh)));
+  a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(Dh)));
+  const unsigned grid = unsigned(int64_t(a.n_t) * B * Hkv);
+  kern<<<grid, 192, C::SMEM_BYTES, st>>>(mq, mk, mv, mdo, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch attn_bwd_main_kernel");
+  return RCA_OK;
+}
+
+rca_status do_fwd(const void* q, const void* k, const void* v, int64_t B, int64_t Hq, int64_t Hkv, int64_t T,
+                  int64_t Dh, void* out, float* lse, rca_dtype dt, cudaStream_t st) {
+  if (dt == RCA_BF16) {
+    if (Dh <= 64) return launch_fwd<false, 64>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st);
+    return launch_fwd<false, 128>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st);
+  }
+  if (Dh <= 32) return launch_fwd<true, 32>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st);
+  return launch_fwd<true, 64>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st);
+}
+
+rca_status do_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
+                       int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt, void* ws,
+                       const WsLayout& L, cudaStream_t st) {
+  if (dt == RCA_BF16) {
+    if (Dh <= 64) return launch_bwd_main<false, 64>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st);
+    return launch_bwd_main<false, 128>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st);
+  }
+  if (Dh <= 32) return launch_bwd_main<true, 32>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st);
+  return launch_bwd_main<true, 64>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st);
+}
+
+rca_status do_preprocess(const void* out, const float* lse, const void* dout, int64_t B, int64_t Hq, int64_t T,
+                         int64_t Dh, rca_dtype dt, void* ws, const WsLayout& L, cudaStream_t st) {
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  rca::PreArgs a{};
+  a.out = out;
+  a.lse = lse;
+  a.dout = dout;
+  a.dq_acc = reinterpret_cast<float*>(w + L.dq_off);
+  a.lse2 = reinterpret_cast<float*>(w + L.lse2_off);
+  a.dvec = reinterpret_cast<float*>(w + L.d_off);
+  a.B = int(B); a.Hq = int(Hq); a.T = int(T); a.Dh = int(Dh); a.Tpad = int(L.Tpad);
+  const int64_t lpr = Dh / (dt == RCA_BF16 ? 8 : 4);
+  const int64_t threads = B * L.Tpad * Hq * lpr;
+  const unsigned grid = unsigned((threads + 255) / 256);
+  if (dt == RCA_BF16)
+    rca::attn_bwd_preprocess_kernel<false><<<grid, 256, 0, st>>>(a);
+  else
+    rca::attn_bwd_preprocess_kernel<true><<<grid, 256, 0, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch attn_bwd_preprocess_kernel");
+  return RCA_OK;
+}
+
+rca_status do_convert(void* dq, int64_t B, int64_t Hq, int64_t T, int64_t Dh, rca_dtype dt, const void* ws,
+                      const WsLayout& L, cudaStream_t st) {
+  const float* acc = reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws) + L.dq_off);
+  const long long n4 = (long long)(B * T * Hq * Dh / 4);
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long want = (n4 + 255) / 256;
+  const long long cap = (long long)sms * 8;
+  const unsigned grid = unsigned(want < cap ? (want > 0 ? want : 1) : cap);
+  const float scale = float(1.0 / std::sqrt(double(Dh)));
+  if (dt == RCA_BF16)
+    rca::attn_bwd_dq_convert_kernel<false><<<grid, 256, 0, st>>>(acc, dq, n4, scale);
+  else
+    rca::attn_bwd_dq_convert_kernel<true><<<grid, 256, 0, st>>>(acc, dq, n4, scale);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch attn_bwd_dq_convert_kernel");
+  return RCA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+uint32_t rca_abi_version(void) { return RCA_ABI_VERSION; }
+
+const char* rca_last_error(void) { return g_err.c_str(); }
+
+uint64_t rca_set_wait_timeout_ns(uint64_t ns) {
+  if (ns < 1000000ull) ns = 1000000ull;
+  return g_timeout_ns.exchange(ns);
+}
+
+rca_status rca_attn_fwd(const void* q, const void* k, const void* v, int64_t B, int64_t Hq, int64_t Hkv,
+                        int64_t T, int64_t Dh, void* out, float* lse, rca_dtype dt, void* cuda_stream) {
+  RCA_GUARD_BEGIN
+  g_err.clear();
+  if (!q || !k || !v || !out || !lse) return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_fwd: null pointer");
+  RCA_CHECK(check_shape(B, Hq, Hkv, T, Dh, dt));
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_fwd: q, k, v, out and lse must be 16-byte aligned");
+  return do_fwd(q, k, v, B, Hq, Hkv, T, Dh, out, lse, dt, static_cast<cudaStream_t>(cuda_stream));
+  RCA_GUARD_END
+}
+
+size_t rca_attn_bwd_workspace_size(int64_t B, int64_t Hq, int64_t T, int64_t Dh) {
+  if (B < 1 || Hq < 1 || T < 1 || Dh < 1 || T > (int64_t(1) << 30)) return 0;
+  return ws_layout(B, Hq, T, Dh).total;
+}
+
+rca_status rca_attn_bwd_preprocess(const void* out, const float* lse, const void* dout, int64_t B, int64_t Hq,
+                                   int64_t T, int64_t Dh, rca_dtype dt, void* workspace, size_t workspace_bytes,
+                                   void* cuda_stream) {
+  RCA_GUARD_BEGIN
+  g_err.clear();
+  if (!out || !lse || !dout) return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd_preprocess: null pointer");
+  RCA_CHECK(check_shape(B, Hq, Hq, T, Dh, dt));
+  if (!aligned16(out) || !aligned16(dout) || !aligned16(lse))
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd_preprocess: out, dout and lse must be 16-byte aligned");
+  const WsLayout L = ws_layout(B, Hq, T, Dh);
+  RCA_CHECK(check_ws(workspace, workspace_bytes, L));
+  return do_preprocess(out, lse, dout, B, Hq, T, Dh, dt, workspace, L, static_cast<cudaStream_t>(cuda_stream));
+  RCA_GUARD_END
+}
+
+rca_status rca_attn_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
+                             int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt,
+                             void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  RCA_GUARD_BEGIN
+  g_err.clear();
+  if (!q || !k || !v || !dout || !dk || !dv)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd_main: null pointer");
+  RCA_CHECK(check_shape(B, Hq, Hkv, T, Dh, dt));
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dk) || !aligned16(dv))
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd_main: tensors must be 16-byte aligned");
+  const WsLayout L = ws_layout(B, Hq, T, Dh);
+  RCA_CHECK(check_ws(workspace, workspace_bytes, L));
+  return do_bwd_main(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, dt, workspace, L,
+                     static_cast<cudaStream_t>(cuda_stream));
+  RCA_GUARD_END
+}
+
+rca_status rca_attn_bwd_dq_convert(void* dq, int64_t B, int64_t Hq, int64_t T, int64_t Dh, rca_dtype dt,
+                                   const void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  RCA_GUARD_BEGIN
+  g_err.clear();
+  if (!dq) return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd_dq_convert: null pointer");
+  RCA_CHECK(check_shape(B, Hq, Hq, T, Dh, dt));
+  if (!aligned16(dq)) return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd_dq_convert: dq must be 16-byte aligned");
+  const WsLayout L = ws_layout(B, Hq, T, Dh);
+  RCA_CHECK(check_ws(workspace, workspace_bytes, L));
+  return do_convert(dq, B, Hq, T, Dh, dt, workspace, L, static_cast<cudaStream_t>(cuda_stream));
+  RCA_GUARD_END
+}
+
+rca_status rca_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, int64_t B, int64_t Hq, int64_t Hkv,
+                        int64_t T, int64_t Dh, rca_dtype dt, void* workspace, size_t workspace_bytes,
+                        void* cuda_stream) {
+  RCA_GUARD_BEGIN
+  g_err.clear();
+  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd: null pointer");
+  RCA_CHECK(check_shape(B, Hq, Hkv, T, Dh, dt));
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd: tensors must be 16-byte aligned");
+  const WsLayout L = ws_layout(B, Hq, T, Dh);
+  RCA_CHECK(check_ws(workspace, workspace_bytes, L));
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  RCA_CHECK(do_preprocess(out, lse, dout, B, Hq, T, Dh, dt, workspace, L, st));
+  RCA_CHECK(do_bwd_main(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, dt, workspace, L, st));
+  return do_convert(dq, B, Hq, T, Dh, dt, workspace, L, st);
+  RCA_GUARD_END
+}
+
+rca_status rca_stream_status(void* cuda_stream) {
+  RCA_GUARD_BEGIN
+  g_err.clear();
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "asynchronous CUDA error");
+  int* status = nullptr;
+  RCA_CHECK(status_word(&status));
+  int h = 0;
+  e = cudaMemcpy(&h, status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status word)");
+  if (h != 0) {
+    cudaMemset(status, 0, sizeof(int));
+    cudaDeviceSynchronize();
+    return fail(RCA_ERR_DEVICE_TIMEOUT, "a device-side wait exceeded its time limit (status %d); outputs are invalid", h);
+  }
+  return RCA_OK;
+  RCA_GUARD_END
+}
+
+}  // extern "C"

@@ -1,0 +1,155 @@
+/*
+ * rca_attn.h — C ABI of the GB300 (sm_103a) causal multi-head attention library
+ * (librca_attn.so).
+ *
+ * What it computes. Memory-linear ("Flash") causal self-attention and its
+ * vector-Jacobian product, as described by the riftco-transformer pages:
+ *   - "Architecture" (docs/concepts/architecture.html), "Tensor conventions":
+ *     contiguous row-major storage; scores [B,H,Tq,Tk]; a key at t_k is not
+ *     used by a query at t_q when t_k > t_q.
+ *   - "Execution Backends and the Python ABI" (docs/internals/backends_and_python.html),
+ *     "What the Metal slice does": the Flash path is exact, saves only per-row
+ *     [B,H,T] statistics, and its backward recomputes scores and probabilities
+ *     from Q, K and those statistics.
+ *   - Neural-network page (docs/learn/neural_network.html), "Stable softmax and
+ *     cross-entropy": max-subtracted softmax; a fully masked row is rejected.
+ *   - algo-v1-codepoint "docs/ARCHITECTURE.md", "config.py": grouped-query
+ *     attention requires Hq % Hkv == 0.
+ *
+ * Per batch b and query head h (KV head kv = h / (Hq/Hkv), consecutive groups):
+ *   S[i,j]  = scale * sum_d Q[b,i,h,d] K[b,j,kv,d],   kept for j <= i only
+ *   LSE[i]  = ln sum_{j<=i} exp(S[i,j])                 (natural log, fp32)
+ *   O[i,:]  = sum_{j<=i} exp(S[i,j] - LSE[i]) V[b,j,kv,:]
+ * with scale = 1/sqrt(Dh). The backward, for upstream gradient dO:
+ *   D[i]  = sum_d dO[i,d] O[i,d];  P = exp(S - LSE);  dP = dO V^T
+ *   dS    = P * (dP - D);  dQ = scale dS K;  dK = scale dS^T Q;  dV = P^T dO
+ * dK and dV sum over the query heads that share a KV head.
+ *
+ * Layouts (all contiguous, row-major, element strides implied by the shape):
+ *   q, out, dout, dq : [B, T, Hq,  Dh]   storage dtype
+ *   k, v, dk, dv     : [B, T, Hkv, Dh]   storage dtype
+ *   lse              : [B, Hq, T]        float32
+ * Storage dtype: RCA_BF16 (bfloat16 operands, fp32 accumulation) or
+ * RCA_F32_TF32 (float32 storage, TF32 tensor-core operands, fp32 accumulation).
+ * Supported head widths: Dh in {16, 32, 64, 128} for RCA_BF16 and
+ * {16, 32, 64} for RCA_F32_TF32; anything else is RCA_ERR_UNSUPPORTED.
+ *
+ * Ownership and execution. Every pointer except cuda_stream is a DEVICE pointer
+ * owned by the caller (e.g. torch CUDA tensors) that stays valid until the
+ * work queued on cuda_stream has finished. Calls only enqueue work on
+ * cuda_stream (a cudaStream_t; NULL means the legacy default stream) and
+ * return; they never synchronise. Inputs are never written. Outputs are fully
+ * overwritten. The library keeps, per device, a small cache of TMA descriptors
+ * and one device status word used by the bounded-wait timeout described below.
+ *
+ * Errors. Every argument is validated before anything is launched; on a
+ * validation failure nothing is enqueued. No C++ exception crosses this
+ * boundary. A failed call returns a non-zero rca_status and records a message
+ * retrievable with rca_last_error() on the calling thread. Device-side waits
+ * are bounded in time; a kernel that gives up records RCA_ERR_DEVICE_TIMEOUT in
+ * the status word, which rca_stream_status() reports.
+ *
+ * All entry points are thread-safe with respect to one another.
+ */
+#ifndef RCA_ATTN_H
+#define RCA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. Published values are never renumbered. */
+typedef enum {
+  RCA_OK = 0,
+  RCA_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad size, Hq % Hkv != 0, misalignment, small workspace */
+  RCA_ERR_UNSUPPORTED = 2,      /* valid request this build does not implement (e.g. Dh = 96) */
+  RCA_ERR_CUDA = 3,             /* a CUDA runtime/driver call failed; message holds the CUDA error text */
+  RCA_ERR_DEVICE_TIMEOUT = 4    /* a device-side wait exceeded its time limit; outputs are invalid */
+} rca_status;
+
+/* Storage dtype of q/k/v/out/dout/dq/dk/dv; selects the tensor-core operand type. */
+typedef enum { RCA_F32_TF32 = 0, RCA_BF16 = 1 } rca_dtype;
+
+/* ABI version: upper 16 bits major, lower 16 bits minor (0x00010000 = 1.0). */
+#define RCA_ABI_VERSION 0x00010000u
+uint32_t rca_abi_version(void);
+
+/* Message of the last failed call on this thread ("" if none). The pointer is
+ * owned by the library and valid until the next call on this thread. */
+const char* rca_last_error(void);
+
+/*
+ * Forward. Writes out [B,T,Hq,Dh] (storage dtype) and lse [B,Hq,T] (float32).
+ * Requires B, Hq, Hkv, T >= 1 (T = 0 would be a fully masked row: rejected),
+ * Hq % Hkv == 0, and 16-byte aligned q, k, v, out, lse.
+ */
+rca_status rca_attn_fwd(const void* q, const void* k, const void* v,
+                        int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
+                        void* out, float* lse, rca_dtype dt, void* cuda_stream);
+
+/*
+ * Bytes of device scratch rca_attn_bwd needs: an fp32 dQ accumulator and the
+ * per-row D and LSE rows, each padded to a multiple of 128 positions.
+ * Returns 0 for invalid sizes.
+ */
+size_t rca_attn_bwd_workspace_size(int64_t B, int64_t Hq, int64_t T, int64_t Dh);
+
+/*
+ * Backward. Given the forward's out and lse and the upstream gradient dout,
+ * writes dq [B,T,Hq,Dh], dk and dv [B,T,Hkv,Dh] (storage dtype). workspace is
+ * caller-owned device memory of at least rca_attn_bwd_workspace_size(...)
+ * bytes, 256-byte aligned; its contents on entry do not matter and are
+ * clobbered. Runs rca_attn_bwd_preprocess, rca_attn_bwd_main and
+ * rca_attn_bwd_dq_convert in order on cuda_stream.
+ */
+rca_status rca_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                        int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
+                        rca_dtype dt, void* workspace, size_t workspace_bytes,
+                        void* cuda_stream);
+
+/*
+ * The three stages of rca_attn_bwd, exposed so a caller can time or schedule
+ * them separately. They must run in this order on one stream with the same
+ * arguments and workspace.
+ *  preprocess: D = rowsum(dout * out), LSE in base 2, zeroes the dQ accumulator
+ *              (memory-bound).
+ *  main:       recomputes P from Q, K and LSE; accumulates dK, dV per key tile
+ *              (written to dk, dv) and adds dQ partials into the workspace.
+ *  dq_convert: dq = scale * accumulator, cast to the storage dtype.
+ */
+rca_status rca_attn_bwd_preprocess(const void* out, const float* lse, const void* dout,
+                                   int64_t B, int64_t Hq, int64_t T, int64_t Dh,
+                                   rca_dtype dt, void* workspace, size_t workspace_bytes,
+                                   void* cuda_stream);
+rca_status rca_attn_bwd_main(const void* q, const void* k, const void* v, const void* dout,
+                             void* dk, void* dv,
+                             int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
+                             rca_dtype dt, void* workspace, size_t workspace_bytes,
+                             void* cuda_stream);
+rca_status rca_attn_bwd_dq_convert(void* dq, int64_t B, int64_t Hq, int64_t T, int64_t Dh,
+                                   rca_dtype dt, const void* workspace, size_t workspace_bytes,
+                                   void* cuda_stream);
+
+/*
+ * Synchronises cuda_stream, then reports (and clears) an asynchronous CUDA
+ * error or a device-side timeout recorded by a kernel of this library on the
+ * current device. RCA_OK if neither happened.
+ */
+rca_status rca_stream_status(void* cuda_stream);
+
+/*
+ * Sets the device-side wait limit in nanoseconds for subsequent launches from
+ * any thread (default 2e9 = 2 s; values < 1e6 are raised to 1e6). Returns the
+ * previous value.
+ */
+uint64_t rca_set_wait_timeout_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RCA_ATTN_H */

@@ -1,0 +1,106 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads,
+exports every function include/rca_attn.h declares, and rejects invalid
+arguments before touching any pointer or launching anything."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from causal_head_attention_gb300 import _native
+from causal_head_attention_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rca_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return _native.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rca_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    for n in ("rca_attn_fwd", "rca_attn_bwd", "rca_attn_bwd_workspace_size", "rca_stream_status",
+              "rca_last_error", "rca_abi_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} declared in rca_attn.h but not exported"
+        assert n in _native._SIG, f"{n} has no binding signature"
+
+
+def test_abi_version(lib):
+    v = lib.rca_abi_version()
+    assert v >> 16 == 1
+
+
+FAKE = ctypes.c_void_p(4096)  # never dereferenced: every call below fails validation first
+NULL = ctypes.c_void_p(0)
+
+
+def fwd(lib, q=FAKE, B=1, Hq=2, Hkv=2, T=8, Dh=64, dt=1, out=FAKE, lse=FAKE):
+    return lib.rca_attn_fwd(q, FAKE, FAKE, B, Hq, Hkv, T, Dh, out, lse, dt, NULL)
+
+
+@pytest.mark.parametrize(
+    "kw,status,needle",
+    [
+        (dict(q=NULL), 1, "null"),
+        (dict(out=NULL), 1, "null"),
+        (dict(T=0), 1, "fully masked"),
+        (dict(B=0), 1, ">= 1"),
+        (dict(Hq=3, Hkv=2), 1, "Hq % Hkv"),
+        (dict(Dh=96), 2, "Dh=96"),
+        (dict(Dh=128, dt=0), 2, "Dh=128"),
+        (dict(dt=7), 1, "dtype"),
+        (dict(q=ctypes.c_void_p(4100)), 1, "aligned"),
+    ],
+)
+def test_fwd_validation(lib, kw, status, needle):
+    assert fwd(lib, **kw) == status
+    assert needle in lib.rca_last_error().decode()
+
+
+def test_workspace_size_and_checks(lib):
+    n = lib.rca_attn_bwd_workspace_size(4, 16, 2048, 64)
+    assert n >= 4 * 2048 * 16 * 64 * 4 + 2 * 4 * 16 * 2048 * 4
+    assert lib.rca_attn_bwd_workspace_size(0, 16, 2048, 64) == 0
+    # too small a workspace is rejected before anything runs
+    st = lib.rca_attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 2, 8, 64, 1,
+                          ctypes.c_void_p(4096), 16, NULL)
+    assert st == 1 and "workspace too small" in lib.rca_last_error().decode()
+    st = lib.rca_attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 2, 8, 64, 1,
+                          ctypes.c_void_p(4096 + 16), 1 << 30, NULL)
+    assert st == 1 and "256-byte" in lib.rca_last_error().decode()
+
+
+def test_error_text_is_per_thread(lib):
+    import threading
+
+    assert fwd(lib, Dh=96) == 2
+    seen = {}
+
+    def other():
+        seen["msg"] = lib.rca_last_error().decode()
+
+    t = threading.Thread(target=other)
+    t.start()
+    t.join()
+    assert seen["msg"] == ""
+    assert "Dh=96" in lib.rca_last_error().decode()
+
+
+def test_timeout_setter(lib):
+    old = lib.rca_set_wait_timeout_ns(5)
+    assert lib.rca_set_wait_timeout_ns(old) == 1000000
