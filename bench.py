@@ -245,7 +245,7 @@ def run_gpu(args, w, world, rank, local):
     dq = torch.empty_like(sets[0][0])
     dk = torch.empty_like(sets[0][1])
     dv = torch.empty_like(sets[0][2])
-    ws = rca.workspace_for(sets[0][0])
+    ws = rca.workspace_for(sets[0][0], sets[0][1])
 
     def step(i, ev=None):
         q, k, v, do = sets[i % nsets]
@@ -254,30 +254,38 @@ def run_gpu(args, w, world, rank, local):
         rca.rca_attn_fwd(q, k, v, out, lse, stream)
         if ev is not None:
             ev[1].record(stream)
-        rca.rca_attn_bwd_preprocess(out, lse, do, ws, stream)
+        rca.rca_attn_bwd_preprocess(out, lse, do, ws, Hkv=w.Hkv, stream=stream)
         if ev is not None:
             ev[2].record(stream)
         rca.rca_attn_bwd_main(q, k, v, do, dk, dv, ws, stream)
         if ev is not None:
             ev[3].record(stream)
-        rca.rca_attn_bwd_dq_convert(dq, ws, stream)
+        rca.rca_attn_bwd_dq_convert(dq, ws, Hkv=w.Hkv, stream=stream)
         if ev is not None:
             ev[4].record(stream)
 
-    for i in range(args.warmup):
+    # Warm-up: at least W steps and at least ~1 s of work, with the clock sampler
+    # already running, so that clock samples cover the GPU under this load.
+    clk = ClockSampler(local)
+    clk.start()
+    t_w = time.perf_counter()
+    i = 0
+    while i < args.warmup or time.perf_counter() - t_w < args.min_warmup_s:
         step(i)
+        i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize(dev)
+    n_warm = i
     rca.rca_stream_status(stream)
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    clk = ClockSampler(local)
-    clk.start()
     barrier(world)
     torch.cuda.synchronize(dev)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
-        step(args.warmup + i, evs[i])
+        step(n_warm + i, evs[i])
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -380,7 +388,7 @@ def run_gpu(args, w, world, rank, local):
     if rank == 0:
         line = {
             "metric": args.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "warmup": n_warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32 (tf32 MMA)", "data": "synthetic",
             "config": {"workload": w.describe(), "name": w.name, "global_batch": w.B * world, "seq_len": w.T,
                        "heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.Dh, "parallelism": f"independent units x{world}",
@@ -409,6 +417,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(BY_NAME))
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--min-warmup-s", type=float, default=1.0,
+                    help="warm-up runs at least this long (clock samples under load)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()

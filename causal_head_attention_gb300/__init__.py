@@ -52,11 +52,12 @@ def attention_forward(q, k, v, stream=None):
     return out, lse
 
 
-def workspace_for(q):
+def workspace_for(q, k):
+    """Device scratch for the backward of these q [B,T,Hq,Dh] / k [B,T,Hkv,Dh]."""
     import torch
 
     B, T, Hq, Dh = q.shape
-    n = rca_attn_bwd_workspace_size(B, Hq, T, Dh)
+    n = rca_attn_bwd_workspace_size(B, Hq, k.shape[2], T, Dh, q.dtype)
     return torch.empty(n, dtype=torch.uint8, device=q.device)
 
 
@@ -67,7 +68,7 @@ def attention_backward(q, k, v, out, lse, dout, workspace=None, stream=None):
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
-    ws = workspace if workspace is not None else workspace_for(q)
+    ws = workspace if workspace is not None else workspace_for(q, k)
     rca_attn_bwd(q, k, v, out, lse, dout.contiguous(), dq, dk, dv, ws, stream)
     return dq, dk, dv
 

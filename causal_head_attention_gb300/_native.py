@@ -36,14 +36,14 @@ _SIG = {
     "rca_abi_version": (ctypes.c_uint32, []),
     "rca_last_error": (ctypes.c_char_p, []),
     "rca_attn_fwd": (ctypes.c_int, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_int, _P]),
-    "rca_attn_bwd_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "rca_attn_bwd_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I, _I, ctypes.c_int]),
     "rca_attn_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                     ctypes.c_int, _P, ctypes.c_size_t, _P]),
-    "rca_attn_bwd_preprocess": (ctypes.c_int, [_P, _P, _P, _I, _I, _I, _I, ctypes.c_int, _P,
+    "rca_attn_bwd_preprocess": (ctypes.c_int, [_P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_int, _P,
                                                ctypes.c_size_t, _P]),
     "rca_attn_bwd_main": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_int,
                                          _P, ctypes.c_size_t, _P]),
-    "rca_attn_bwd_dq_convert": (ctypes.c_int, [_P, _I, _I, _I, _I, ctypes.c_int, _P,
+    "rca_attn_bwd_dq_convert": (ctypes.c_int, [_P, _I, _I, _I, _I, _I, ctypes.c_int, _P,
                                                ctypes.c_size_t, _P]),
     "rca_stream_status": (ctypes.c_int, [_P]),
     "rca_set_wait_timeout_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
@@ -144,8 +144,12 @@ def rca_attn_fwd(q, k, v, out, lse, stream=None):
                               _dtype_code(q), _stream(stream)))
 
 
-def rca_attn_bwd_workspace_size(B, Hq, T, Dh) -> int:
-    return lib().rca_attn_bwd_workspace_size(B, Hq, T, Dh)
+def rca_attn_bwd_workspace_size(B, Hq, Hkv, T, Dh, dt) -> int:
+    """dt: RCA_BF16 / RCA_F32_TF32, or a torch dtype."""
+    if not isinstance(dt, int):
+        torch = _torch()
+        dt = RCA_BF16 if dt == torch.bfloat16 else RCA_F32_TF32
+    return lib().rca_attn_bwd_workspace_size(B, Hq, Hkv, T, Dh, dt)
 
 
 def rca_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, workspace, stream=None):
@@ -155,9 +159,10 @@ def rca_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, workspace, stream=None):
                               workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
-def rca_attn_bwd_preprocess(out, lse, dout, workspace, stream=None):
+def rca_attn_bwd_preprocess(out, lse, dout, workspace, Hkv=None, stream=None):
     B, T, Hq, Dh = out.shape
-    _check(lib().rca_attn_bwd_preprocess(_ptr(out), _ptr(lse), _ptr(dout), B, Hq, T, Dh, _dtype_code(out),
+    Hkv = Hq if Hkv is None else Hkv
+    _check(lib().rca_attn_bwd_preprocess(_ptr(out), _ptr(lse), _ptr(dout), B, Hq, Hkv, T, Dh, _dtype_code(out),
                                          _ptr(workspace), workspace.numel() * workspace.element_size(),
                                          _stream(stream)))
 
@@ -169,9 +174,10 @@ def rca_attn_bwd_main(q, k, v, dout, dk, dv, workspace, stream=None):
                                    workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
-def rca_attn_bwd_dq_convert(dq, workspace, stream=None):
+def rca_attn_bwd_dq_convert(dq, workspace, Hkv=None, stream=None):
     B, T, Hq, Dh = dq.shape
-    _check(lib().rca_attn_bwd_dq_convert(_ptr(dq), B, Hq, T, Dh, _dtype_code(dq), _ptr(workspace),
+    Hkv = Hq if Hkv is None else Hkv
+    _check(lib().rca_attn_bwd_dq_convert(_ptr(dq), B, Hq, Hkv, T, Dh, _dtype_code(dq), _ptr(workspace),
                                          workspace.numel() * workspace.element_size(), _stream(stream)))
 
 

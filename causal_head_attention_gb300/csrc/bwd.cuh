@@ -18,6 +18,8 @@
 //                               tile i >= j; dK, dV accumulate in TMEM; dQ partials
 //                               are added into the fp32 accumulator.
 //   attn_bwd_dq_convert_kernel  dQ = scale * accumulator in the storage dtype.
+//   split_hilo_kernel           fp32 storage only: bf16 hi/lo copies of Q, K, V, dO
+//                               for the main kernel (see BwdCfg).
 #pragma once
 
 #include "tc.cuh"
@@ -108,23 +110,44 @@ __global__ void __launch_bounds__(256)
 }
 
 // ----------------------------------------------------------------------------
+// fp32 storage mode: bf16 hi/lo split of an operand (x = hi + lo)
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+    split_hilo_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ hi,
+                      __nv_bfloat16* __restrict__ lo, long long n4) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const float4 v = reinterpret_cast<const float4*>(src)[i];
+    uint32_t h0, l0, h1, l1;
+    split_bf16x2(v.x, v.y, h0, l0);
+    split_bf16x2(v.z, v.w, h1, l1);
+    reinterpret_cast<uint2*>(hi)[i] = make_uint2(h0, h1);
+    reinterpret_cast<uint2*>(lo)[i] = make_uint2(l0, l1);
+  }
+}
+
+// ----------------------------------------------------------------------------
 // main
 // ----------------------------------------------------------------------------
-template <bool TF32, int DHP>
+// All tensor-core operands are bf16 tiles with DHB head columns (128-byte
+// swizzle, 64-column panels). bf16 storage: one part per operand. fp32 storage
+// (HL): two parts, hi and lo, and every product A.B is computed as
+// Ahi.Bhi + Ahi.Blo + Alo.Bhi with fp32 accumulation. (Products over key or
+// query positions need MN-major operands; kind::tf32 gave no result with
+// MN-major operands on this GPU, so fp32 storage uses the bf16 split.)
+template <bool HL, int DHB>
 struct BwdCfg {
-  static constexpr int ES = TF32 ? 4 : 2;
-  static constexpr int PE = 128 / ES;
+  static constexpr int NPART = HL ? 2 : 1;
   static constexpr int PANEL = 128 * 128;
-  static constexpr int DPANELS = DHP / PE;
-  static constexpr int KV_BYTES = DPANELS * PANEL;  // K or V tile (128 keys)
-  static constexpr int QT_BYTES = DPANELS * PANEL;  // Q or dO tile (128 queries)
-  static constexpr int P_BYTES = (128 / PE) * PANEL;
-  static constexpr int KSTEP = TF32 ? 8 : 16;
-  static constexpr int SPP = PE / KSTEP;
+  static constexpr int DPANELS = DHB / 64;
+  static constexpr int TILE = DPANELS * PANEL;          // one part of a 128-row operand tile
+  static constexpr int OPND = NPART * TILE;             // all parts of it
+  static constexpr int PT_HALF = 2 * PANEL;             // 128 x 128 bf16
+  static constexpr int P_BYTES = NPART * PT_HALF;
   static constexpr int SMEM_LIMIT = 232448;
   static constexpr int BAR_BYTES = 1024;
-  static constexpr int STAGE_BYTES = 2 * QT_BYTES + 1024;  // Q, dO, LSE2[128], D[128]
-  static constexpr int AVAIL = SMEM_LIMIT - 1024 - BAR_BYTES - 2 * KV_BYTES;
+  static constexpr int STAGE_BYTES = 2 * OPND + 1024;   // Q, dO, LSE2[128], D[128]
+  static constexpr int AVAIL = SMEM_LIMIT - 1024 - BAR_BYTES - 2 * OPND;
   static constexpr int NQS_SEP = (AVAIL - 2 * P_BYTES) / STAGE_BYTES;
   static constexpr int NQS_SHR = (AVAIL - P_BYTES) / STAGE_BYTES;
   // P^T and dS^T share one buffer only when separate buffers leave < 2 stages.
@@ -133,21 +156,21 @@ struct BwdCfg {
   static constexpr int NQS = NQS_RAW > 4 ? 4 : NQS_RAW;
   static_assert(NQS >= 1, "backward needs at least one Q/dO stage");
   static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = KV_BYTES;
-  static constexpr int OFF_P = 2 * KV_BYTES;
+  static constexpr int OFF_V = OPND;
+  static constexpr int OFF_P = 2 * OPND;
   static constexpr int OFF_DS = SHARE ? OFF_P : OFF_P + P_BYTES;
   static constexpr int OFF_STAGE = OFF_DS + P_BYTES;
   static constexpr int OFF_BAR = OFF_STAGE + NQS * STAGE_BYTES;
   static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
   // TMEM columns
-  static constexpr int TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + DHP;
-  static constexpr bool DQ_ALIAS = 256 + 3 * DHP > 512;
-  static constexpr int TM_DQ = DQ_ALIAS ? 0 : 256 + 2 * DHP;
+  static constexpr int TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + DHB;
+  static constexpr bool DQ_ALIAS = 256 + 3 * DHB > 512;
+  static constexpr int TM_DQ = DQ_ALIAS ? 0 : 256 + 2 * DHB;
   static constexpr int TMEM_COLS = 512;
-  static constexpr uint32_t IDESC_T = make_idesc(TF32, 128, 128, false, false);   // S^T, dP^T
-  static constexpr uint32_t IDESC_KV = make_idesc(TF32, 128, DHP, false, true);   // dV, dK
-  static constexpr uint32_t IDESC_Q = make_idesc(TF32, 128, DHP, true, true);     // dQ
+  static constexpr uint32_t IDESC_T = make_idesc(false, 128, 128, false, false);   // S^T, dP^T
+  static constexpr uint32_t IDESC_KV = make_idesc(false, 128, DHB, false, true);   // dV, dK
+  static constexpr uint32_t IDESC_Q = make_idesc(false, 128, DHB, true, true);     // dQ
   // barriers
   static constexpr int B_KV = 0;
   static constexpr int B_QF = 1;
@@ -160,6 +183,15 @@ struct BwdCfg {
   static constexpr int B_ITF = B_DQF + 1;
   static constexpr int B_FIN = B_ITF + 1;
   static constexpr int NBAR = B_FIN + 1;
+  // parts multiplied for one product: (hi,hi) [, (hi,lo), (lo,hi)]
+  static constexpr int NPROD = HL ? 3 : 1;
+  __device__ static constexpr int pa(int t) { return t == 2 ? 1 : 0; }
+  __device__ static constexpr int pb(int t) { return t == 1 ? 1 : 0; }
+};
+
+// bf16 tensor maps of every operand: [0] = bf16 storage or hi part, [1] = lo part.
+struct BwdMaps {
+  CUtensorMap q[2], k[2], v[2], dO[2];
 };
 
 struct BwdArgs {
@@ -174,12 +206,30 @@ struct BwdArgs {
   float scale, scale_log2;
 };
 
-template <bool TF32, int DHP>
+// Thread row `rl` of a 128 x 128 bf16 (hi[/lo]) operand tile, K-major with the
+// 128-byte swizzle: 16 chunks of 8 values.
+template <bool HL>
+__device__ __forceinline__ void store_row_bf16(uint32_t base, int rl, const float (&x)[128], int half_bytes) {
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const uint32_t addr = base + (c >> 3) * (128 * 128) + rl * 128 + (((c & 7) ^ (rl & 7)) << 4);
+    if constexpr (HL) {
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) split_bf16x2(x[8 * c + 2 * i], x[8 * c + 2 * i + 1], hi[i], lo[i]);
+      st_shared_v4(addr, hi[0], hi[1], hi[2], hi[3]);
+      st_shared_v4(addr + half_bytes, lo[0], lo[1], lo[2], lo[3]);
+    } else {
+      st_shared_v4(addr, pack_bf16(x[8 * c], x[8 * c + 1]), pack_bf16(x[8 * c + 2], x[8 * c + 3]),
+                   pack_bf16(x[8 * c + 4], x[8 * c + 5]), pack_bf16(x[8 * c + 6], x[8 * c + 7]));
+    }
+  }
+}
+
+template <bool HL, int DHB>
 __global__ void __launch_bounds__(192, 1)
-    attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                         const BwdArgs a) {
-  using C = BwdCfg<TF32, DHP>;
+    attn_bwd_main_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
+  using C = BwdCfg<HL, DHB>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -227,15 +277,20 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      tma_prefetch_desc(&tmdO);
-      mbar_expect_tx(bar(C::B_KV), 2 * C::KV_BYTES);
-      for (int p = 0; p < C::DPANELS; ++p) {
-        tma_load_4d(sbase + C::OFF_K + p * C::PANEL, &tmK, bar(C::B_KV), p * C::PE, kvh, j * 128, b);
-        tma_load_4d(sbase + C::OFF_V + p * C::PANEL, &tmV, bar(C::B_KV), p * C::PE, kvh, j * 128, b);
+      for (int part = 0; part < C::NPART; ++part) {
+        tma_prefetch_desc(&maps.q[part]);
+        tma_prefetch_desc(&maps.k[part]);
+        tma_prefetch_desc(&maps.v[part]);
+        tma_prefetch_desc(&maps.dO[part]);
       }
+      mbar_expect_tx(bar(C::B_KV), 2 * C::OPND);
+      for (int part = 0; part < C::NPART; ++part)
+        for (int p = 0; p < C::DPANELS; ++p) {
+          tma_load_4d(sbase + C::OFF_K + part * C::TILE + p * C::PANEL, &maps.k[part], bar(C::B_KV), p * 64,
+                      kvh, j * 128, b);
+          tma_load_4d(sbase + C::OFF_V + part * C::TILE + p * C::PANEL, &maps.v[part], bar(C::B_KV), p * 64,
+                      kvh, j * 128, b);
+        }
       int it = 0;
       for (; it < n_it; ++it) {
         const int s = it % C::NQS;
@@ -243,14 +298,17 @@ __global__ void __launch_bounds__(192, 1)
         const int h = kvh * a.group + it / n_i;
         const int i = j + it % n_i;
         const uint32_t st = stage(s);
-        mbar_expect_tx(bar(C::B_QF + s), 2 * C::QT_BYTES + 1024);
-        for (int p = 0; p < C::DPANELS; ++p) {
-          tma_load_4d(st + p * C::PANEL, &tmQ, bar(C::B_QF + s), p * C::PE, h, i * 128, b);
-          tma_load_4d(st + C::QT_BYTES + p * C::PANEL, &tmdO, bar(C::B_QF + s), p * C::PE, h, i * 128, b);
-        }
+        mbar_expect_tx(bar(C::B_QF + s), 2 * C::OPND + 1024);
+        for (int part = 0; part < C::NPART; ++part)
+          for (int p = 0; p < C::DPANELS; ++p) {
+            tma_load_4d(st + part * C::TILE + p * C::PANEL, &maps.q[part], bar(C::B_QF + s), p * 64, h,
+                        i * 128, b);
+            tma_load_4d(st + C::OPND + part * C::TILE + p * C::PANEL, &maps.dO[part], bar(C::B_QF + s),
+                        p * 64, h, i * 128, b);
+          }
         const size_t ro = (static_cast<size_t>(b) * a.Hq + h) * a.Tpad + static_cast<size_t>(i) * 128;
-        bulk_load(st + 2 * C::QT_BYTES, a.lse2 + ro, 512, bar(C::B_QF + s));
-        bulk_load(st + 2 * C::QT_BYTES + 512, a.dvec + ro, 512, bar(C::B_QF + s));
+        bulk_load(st + 2 * C::OPND, a.lse2 + ro, 512, bar(C::B_QF + s));
+        bulk_load(st + 2 * C::OPND + 512, a.dvec + ro, 512, bar(C::B_QF + s));
       }
       mbar_drain(bar(C::B_KV), 0, a.timeout_ns);
       for (int s = 0; s < C::NQS && s < it; ++s) {
@@ -266,51 +324,63 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t pb = sbase + C::OFF_P, dsb = sbase + C::OFF_DS;
       for (int it = 0; ok && it < n_it; ++it) {
         const int s = it % C::NQS;
-        const uint32_t qb = stage(s), dob = stage(s) + C::QT_BYTES;
+        const uint32_t qb = stage(s), dob = stage(s) + C::OPND;
         if (!mbar_wait(bar(C::B_QF + s), (it / C::NQS) & 1, w)) { ok = false; break; }
         if (it > 0 && !mbar_wait(bar(C::B_ITF), (it - 1) & 1, w)) { ok = false; break; }
         tc_fence_after();
         // S^T = K Q^T and dP^T = V dO^T   (M = keys, N = queries, K = head dim)
 #pragma unroll
-        for (int k = 0; k < DHP / C::KSTEP; ++k) {
-          const uint32_t off = (k / C::SPP) * C::PANEL + (k % C::SPP) * 32;
-          mma_ss<TF32>(tmem + C::TM_S, make_sdesc(kb + off, 16, 1024), make_sdesc(qb + off, 16, 1024),
-                       C::IDESC_T, k > 0 ? 1u : 0u);
-        }
+        for (int t = 0; t < C::NPROD; ++t)
 #pragma unroll
-        for (int k = 0; k < DHP / C::KSTEP; ++k) {
-          const uint32_t off = (k / C::SPP) * C::PANEL + (k % C::SPP) * 32;
-          mma_ss<TF32>(tmem + C::TM_DP, make_sdesc(vb + off, 16, 1024), make_sdesc(dob + off, 16, 1024),
-                       C::IDESC_T, k > 0 ? 1u : 0u);
-        }
+          for (int k = 0; k < DHB / 16; ++k) {
+            const uint32_t off = (k / 4) * C::PANEL + (k % 4) * 32;
+            mma_ss<false>(tmem + C::TM_S, make_sdesc(kb + C::pa(t) * C::TILE + off, 16, 1024),
+                          make_sdesc(qb + C::pb(t) * C::TILE + off, 16, 1024), C::IDESC_T,
+                          (t > 0 || k > 0) ? 1u : 0u);
+          }
+#pragma unroll
+        for (int t = 0; t < C::NPROD; ++t)
+#pragma unroll
+          for (int k = 0; k < DHB / 16; ++k) {
+            const uint32_t off = (k / 4) * C::PANEL + (k % 4) * 32;
+            mma_ss<false>(tmem + C::TM_DP, make_sdesc(vb + C::pa(t) * C::TILE + off, 16, 1024),
+                          make_sdesc(dob + C::pb(t) * C::TILE + off, 16, 1024), C::IDESC_T,
+                          (t > 0 || k > 0) ? 1u : 0u);
+          }
         tc_commit(bar(C::B_SDP));
         // dV += P^T dO   (M = keys, N = head dim, K = queries)
         if (!mbar_wait(bar(C::B_PR), it & 1, w)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 128 / C::KSTEP; ++k) {
-          const uint32_t aoff = (k / C::SPP) * C::PANEL + (k % C::SPP) * 32;
-          mma_ss<TF32>(tmem + C::TM_DV, make_sdesc(pb + aoff, 16, 1024),
-                       make_sdesc(dob + k * C::KSTEP * 128, C::PANEL, 1024), C::IDESC_KV,
-                       (it > 0 || k > 0) ? 1u : 0u);
-        }
+        for (int t = 0; t < C::NPROD; ++t)
+#pragma unroll
+          for (int k = 0; k < 128 / 16; ++k) {
+            const uint32_t aoff = (k / 4) * C::PANEL + (k % 4) * 32;
+            mma_ss<false>(tmem + C::TM_DV, make_sdesc(pb + C::pa(t) * C::PT_HALF + aoff, 16, 1024),
+                          make_sdesc(dob + C::pb(t) * C::TILE + k * 16 * 128, C::PANEL, 1024), C::IDESC_KV,
+                          (it > 0 || t > 0 || k > 0) ? 1u : 0u);
+          }
         if constexpr (C::SHARE) tc_commit(bar(C::B_DVD));
         // dK += dS^T Q   and   dQ_partial = dS K
         if (!mbar_wait(bar(C::B_DSR), it & 1, w)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 128 / C::KSTEP; ++k) {
-          const uint32_t aoff = (k / C::SPP) * C::PANEL + (k % C::SPP) * 32;
-          mma_ss<TF32>(tmem + C::TM_DK, make_sdesc(dsb + aoff, 16, 1024),
-                       make_sdesc(qb + k * C::KSTEP * 128, C::PANEL, 1024), C::IDESC_KV,
-                       (it > 0 || k > 0) ? 1u : 0u);
-        }
+        for (int t = 0; t < C::NPROD; ++t)
 #pragma unroll
-        for (int k = 0; k < 128 / C::KSTEP; ++k) {
-          mma_ss<TF32>(tmem + C::TM_DQ, make_sdesc(dsb + k * C::KSTEP * 128, C::PANEL, 1024),
-                       make_sdesc(kb + k * C::KSTEP * 128, C::PANEL, 1024), C::IDESC_Q,
-                       k > 0 ? 1u : 0u);
-        }
+          for (int k = 0; k < 128 / 16; ++k) {
+            const uint32_t aoff = (k / 4) * C::PANEL + (k % 4) * 32;
+            mma_ss<false>(tmem + C::TM_DK, make_sdesc(dsb + C::pa(t) * C::PT_HALF + aoff, 16, 1024),
+                          make_sdesc(qb + C::pb(t) * C::TILE + k * 16 * 128, C::PANEL, 1024), C::IDESC_KV,
+                          (it > 0 || t > 0 || k > 0) ? 1u : 0u);
+          }
+#pragma unroll
+        for (int t = 0; t < C::NPROD; ++t)
+#pragma unroll
+          for (int k = 0; k < 128 / 16; ++k) {
+            mma_ss<false>(tmem + C::TM_DQ, make_sdesc(dsb + C::pa(t) * C::PT_HALF + k * 16 * 128, C::PANEL, 1024),
+                          make_sdesc(kb + C::pb(t) * C::TILE + k * 16 * 128, C::PANEL, 1024), C::IDESC_Q,
+                          (t > 0 || k > 0) ? 1u : 0u);
+          }
         tc_commit(bar(C::B_DQF));
         tc_commit(bar(C::B_QE + s));
       }
@@ -332,7 +402,7 @@ __global__ void __launch_bounds__(192, 1)
                                        mbar_wait(bar(C::B_QF + s), (it / C::NQS) & 1, w));
       if (!ok) break;
       tc_fence_after();
-      const float* lse2s = reinterpret_cast<const float*>(smem + (stage(s) - sbase) + 2 * C::QT_BYTES);
+      const float* lse2s = reinterpret_cast<const float*>(smem + (stage(s) - sbase) + 2 * C::OPND);
       const float* ds_ = lse2s + 128;
       float p[128];
 #pragma unroll
@@ -344,24 +414,16 @@ __global__ void __launch_bounds__(192, 1)
       }
       const bool diag = (i == j);
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float e = ex2(fmaf(p[c], sl2, -lse2s[c]));
-        p[c] = (diag && c < rl) ? 0.f : e;  // key rl is after query c: dropped
-      }
-      const uint32_t prow = sbase + C::OFF_P + rl * 128;
-      const uint32_t dsrow = sbase + C::OFF_DS + rl * 128;
-      if constexpr (TF32) {
+      for (int c = 0; c < 128; c += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(lse2s + c);
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          st_shared_v4(prow + (c >> 3) * C::PANEL + (((c & 7) ^ (rl & 7)) << 4), to_tf32(p[4 * c]),
-                       to_tf32(p[4 * c + 1]), to_tf32(p[4 * c + 2]), to_tf32(p[4 * c + 3]));
-      } else {
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          st_shared_v4(prow + (c >> 3) * C::PANEL + (((c & 7) ^ (rl & 7)) << 4),
-                       pack_bf16(p[8 * c], p[8 * c + 1]), pack_bf16(p[8 * c + 2], p[8 * c + 3]),
-                       pack_bf16(p[8 * c + 4], p[8 * c + 5]), pack_bf16(p[8 * c + 6], p[8 * c + 7]));
+        for (int u = 0; u < 4; ++u) {
+          const float e = ex2(fmaf(p[c + u], sl2, -lv[u]));
+          p[c + u] = (diag && c + u < rl) ? 0.f : e;  // key rl is after query c: dropped
+        }
       }
+      store_row_bf16<HL>(sbase + C::OFF_P, rl, p, C::PT_HALF);
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::B_PR));
@@ -371,24 +433,19 @@ __global__ void __launch_bounds__(192, 1)
         uint32_t r[32];
         tmem_ld32(tl + C::TM_DP + c * 32, r);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) p[c * 32 + q] = p[c * 32 + q] * (__uint_as_float(r[q]) - ds_[c * 32 + q]);
+        for (int q = 0; q < 32; q += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(ds_ + c * 32 + q);
+          p[c * 32 + q + 0] *= __uint_as_float(r[q + 0]) - d4.x;
+          p[c * 32 + q + 1] *= __uint_as_float(r[q + 1]) - d4.y;
+          p[c * 32 + q + 2] *= __uint_as_float(r[q + 2]) - d4.z;
+          p[c * 32 + q + 3] *= __uint_as_float(r[q + 3]) - d4.w;
+        }
       }
       if constexpr (C::SHARE) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DVD), it & 1, w));
         if (!ok) break;
       }
-      if constexpr (TF32) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          st_shared_v4(dsrow + (c >> 3) * C::PANEL + (((c & 7) ^ (rl & 7)) << 4), to_tf32(p[4 * c]),
-                       to_tf32(p[4 * c + 1]), to_tf32(p[4 * c + 2]), to_tf32(p[4 * c + 3]));
-      } else {
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          st_shared_v4(dsrow + (c >> 3) * C::PANEL + (((c & 7) ^ (rl & 7)) << 4),
-                       pack_bf16(p[8 * c], p[8 * c + 1]), pack_bf16(p[8 * c + 2], p[8 * c + 3]),
-                       pack_bf16(p[8 * c + 4], p[8 * c + 5]), pack_bf16(p[8 * c + 6], p[8 * c + 7]));
-      }
+      store_row_bf16<HL>(sbase + C::OFF_DS, rl, p, C::PT_HALF);
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::B_DSR));
@@ -399,7 +456,7 @@ __global__ void __launch_bounds__(192, 1)
       const int qrow = i * 128 + rl;
       float* dst = a.dq_acc + ((static_cast<size_t>(b) * a.T + qrow) * a.Hq + h) * a.Dh;
 #pragma unroll
-      for (int c = 0; c < DHP / 32; ++c) {
+      for (int c = 0; c < DHB / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(tl + C::TM_DQ + c * 32, r);
         const int ncol = a.Dh - c * 32;
@@ -428,12 +485,12 @@ __global__ void __launch_bounds__(192, 1)
         const float mul = which == 0 ? 1.f : a.scale;
         void* base = which == 0 ? a.dv : a.dk;
 #pragma unroll
-        for (int c = 0; c < DHP / 32; ++c) {
+        for (int c = 0; c < DHB / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(tl + col0 + c * 32, r);
           const int ncol = a.Dh - c * 32;
           if (!valid || ncol <= 0) continue;
-          if constexpr (TF32) {
+          if constexpr (HL) {
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(base) + row_off + c * 32);
             const int nv = (ncol >= 32 ? 32 : ncol) / 4;
 #pragma unroll

@@ -9,7 +9,7 @@
 // neural-network page, "Stable softmax and cross-entropy".
 //
 // CTA layout (192 threads):
-//   warp 0      TMA producer: Q tile once, then K_j / V_j into an NS-stage ring
+//   warp 0      TMA producer: Q tile once, then K_j / V_j into NSK / NSV-stage rings
 //   warp 1      TMEM owner + single-thread tcgen05 MMA issuer
 //   warps 2..5  softmax warpgroup: thread t owns query row t of the tile
 // Per key tile j (only tiles 0..qt are visited; tile qt is the diagonal):
@@ -18,8 +18,14 @@
 //                            base-2 units; O is rescaled only when the running
 //                            max grows by more than 2^8 (exact: l uses the same
 //                            reference max)
-//   P_j -> shared memory     bf16 (or TF32-rounded fp32), K-major, 128-B swizzle
+//   P_j -> shared memory     bf16, K-major, 128-B swizzle
 //   O += P_j V_j             tcgen05, into TMEM O
+// fp32 storage mode: S = Q K^T runs as kind::tf32 on the fp32 tiles (the head
+// dimension is contiguous, so both operands are K-major). P V contracts over
+// keys, which needs V as an MN-major operand; kind::tf32 produced no result
+// with MN-major operands on this GPU, so P and V are split into bf16 pairs
+// x = hi + lo and O += Phi Vhi + Phi Vlo + Plo Vhi (relative error ~2^-16,
+// below TF32's 2^-11).
 // S_{j+1} is issued before O += P_j V_j so the tensor core works while the
 // softmax warps handle the next tile.
 #pragma once
@@ -37,33 +43,44 @@ struct FwdCfg {
   static constexpr int DPANELS = DHP / PE;    // panels across the head width
   static constexpr int Q_BYTES = DPANELS * PANEL;
   static constexpr int KV_BYTES = DPANELS * PANEL;
-  static constexpr int P_BYTES = (BN / PE) * PANEL;
-  static constexpr int KSTEP = TF32 ? 8 : 16;  // K of one MMA instruction
-  static constexpr int SPP = PE / KSTEP;       // MMA k-steps per panel
+  static constexpr int KSTEP = TF32 ? 8 : 16;  // K of one QK^T MMA instruction
+  static constexpr int SPP = PE / KSTEP;       // QK^T k-steps per panel
+  // P.V operands. bf16 mode: P (bf16) and the V stage itself. fp32 mode: P and
+  // V as bf16 hi/lo pairs (x = hi + lo), V converted from its fp32 stage into
+  // a DHB-column bf16 tile (zero-padded past the head width).
+  static constexpr int DHB = TF32 ? (DHP > 64 ? DHP : 64) : DHP;
+  static constexpr int VB_PANELS = DHB / 64;
+  static constexpr int VHL_BYTES = TF32 ? 2 * VB_PANELS * PANEL : 0;
+  static constexpr int P_HALF = 2 * PANEL;                    // 128 x 128 bf16
+  static constexpr int P_BYTES = TF32 ? 2 * P_HALF : P_HALF;  // hi (+ lo)
   static constexpr int SMEM_LIMIT = 232448;
   static constexpr int BAR_BYTES = 1024;
-  static constexpr int NS_FIT =
-      (SMEM_LIMIT - 1024 - BAR_BYTES - Q_BYTES - P_BYTES) / (2 * KV_BYTES);
-  static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;
-  static_assert(NS >= 2, "forward needs at least two K/V stages");
+  static constexpr int AVAIL = SMEM_LIMIT - 1024 - BAR_BYTES - Q_BYTES - P_BYTES - VHL_BYTES;
+  static constexpr int NS_BF = AVAIL / (2 * KV_BYTES) > 4 ? 4 : AVAIL / (2 * KV_BYTES);
+  static constexpr int NSV = TF32 ? (AVAIL >= 4 * KV_BYTES ? 2 : 1) : NS_BF;
+  static constexpr int NSK_FIT = TF32 ? (AVAIL - NSV * KV_BYTES) / KV_BYTES : NS_BF;
+  static constexpr int NSK = NSK_FIT > 4 ? 4 : NSK_FIT;
+  static_assert(NSK >= 2 && NSV >= 1, "forward needs at least two K stages and one V stage");
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + NS * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + NS * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int OFF_V = OFF_K + NSK * KV_BYTES;
+  static constexpr int OFF_P = OFF_V + NSV * KV_BYTES;
+  static constexpr int OFF_VHL = OFF_P + P_BYTES;
+  static constexpr int OFF_BAR = OFF_VHL + VHL_BYTES;
   static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
   static constexpr int TMEM_S = 0;          // two buffers: columns [0,128) and [128,256)
-  static constexpr int TMEM_O = 256;        // DHP columns
+  static constexpr int TMEM_O = 256;        // DHB columns
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_QK = make_idesc(TF32, 128, 128, false, false);
-  static constexpr uint32_t IDESC_PV = make_idesc(TF32, 128, DHP, false, true);
+  static constexpr uint32_t IDESC_PV = make_idesc(false, 128, DHB, false, true);  // bf16 operands
   // barrier slots
   static constexpr int B_Q = 0;
   static constexpr int B_KF = 1;
-  static constexpr int B_VF = B_KF + NS;
-  static constexpr int B_KVE = B_VF + NS;
-  static constexpr int B_SF = B_KVE + NS;   // 2
+  static constexpr int B_KE = B_KF + NSK;
+  static constexpr int B_VF = B_KE + NSK;
+  static constexpr int B_VE = B_VF + NSV;
+  static constexpr int B_SF = B_VE + NSV;   // 2
   static constexpr int B_SFREE = B_SF + 2;  // 2
   static constexpr int B_PF = B_SFREE + 2;
   static constexpr int B_OD = B_PF + 1;     // 2
@@ -79,6 +96,36 @@ struct FwdArgs {
   int B, Hq, Hkv, T, Dh, group, n_qt;
   float scale_log2;  // (1/sqrt(Dh)) * log2(e)
 };
+
+// fp32 mode: split the fp32 V stage (MN-major, 32-element panels) into bf16
+// hi/lo tiles (MN-major, 64-element panels). Thread t converts key row t; head
+// columns past DHP are written as zeros.
+template <class C>
+__device__ __forceinline__ void split_v_row(uint32_t vsrc, uint32_t vhi, uint32_t vlo, int row) {
+  const uint32_t sw = row & 7;
+#pragma unroll
+  for (int g = 0; g < C::DHB / 8; ++g) {
+    const uint32_t dst = (g >> 3) * C::PANEL + row * 128 + (((g & 7) ^ sw) << 4);
+    if (g < C::DPANELS * 4) {
+      const uint32_t pf = g >> 2;                // fp32 panel
+      const uint32_t c0 = (2 * g) & 7, c1 = c0 + 1;
+      const uint32_t base = vsrc + pf * C::PANEL + row * 128;
+      float x[8];
+      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(x[0]), "=f"(x[1]), "=f"(x[2]), "=f"(x[3]) : "r"(base + ((c0 ^ sw) << 4)));
+      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(x[4]), "=f"(x[5]), "=f"(x[6]), "=f"(x[7]) : "r"(base + ((c1 ^ sw) << 4)));
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) split_bf16x2(x[2 * i], x[2 * i + 1], hi[i], lo[i]);
+      st_shared_v4(vhi + dst, hi[0], hi[1], hi[2], hi[3]);
+      st_shared_v4(vlo + dst, lo[0], lo[1], lo[2], lo[3]);
+    } else {
+      st_shared_v4(vhi + dst, 0u, 0u, 0u, 0u);
+      st_shared_v4(vlo + dst, 0u, 0u, 0u, 0u);
+    }
+  }
+}
 
 template <bool TF32, int DHP>
 __global__ void __launch_bounds__(192, 1)
@@ -103,10 +150,13 @@ __global__ void __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_Q), 1);
-    for (int s = 0; s < C::NS; ++s) {
+    for (int s = 0; s < C::NSK; ++s) {
       mbar_init(bar(C::B_KF + s), 1);
+      mbar_init(bar(C::B_KE + s), 1);
+    }
+    for (int s = 0; s < C::NSV; ++s) {
       mbar_init(bar(C::B_VF + s), 1);
-      mbar_init(bar(C::B_KVE + s), 1);
+      mbar_init(bar(C::B_VE + s), TF32 ? 128 : 1);  // fp32: released by the converting warps
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(C::B_SF + i), 1);
@@ -137,27 +187,34 @@ __global__ void __launch_bounds__(192, 1)
       mbar_expect_tx(bar(C::B_Q), C::Q_BYTES);
       for (int p = 0; p < C::DPANELS; ++p)
         tma_load_4d(sbase + C::OFF_Q + p * C::PANEL, &tmQ, bar(C::B_Q), p * C::PE, h, qt * C::BM, b);
-      int j = 0;
-      for (; j < nkv; ++j) {
-        const int s = j % C::NS;
-        if (j >= C::NS && !mbar_wait(bar(C::B_KVE + s), ((j / C::NS) - 1) & 1, w)) break;
-        mbar_expect_tx(bar(C::B_KF + s), C::KV_BYTES);
+      int jk = 0, jv = 0;
+      for (; jv < nkv; ++jv) {
+        // K_j then V_j; K stages are released after S_j, V stages after P_j V_j
+        // (bf16) or after the V_j hi/lo split (fp32).
+        const int sk = jk % C::NSK;
+        if (jk >= C::NSK && !mbar_wait(bar(C::B_KE + sk), ((jk / C::NSK) - 1) & 1, w)) break;
+        mbar_expect_tx(bar(C::B_KF + sk), C::KV_BYTES);
         for (int p = 0; p < C::DPANELS; ++p)
-          tma_load_4d(sbase + C::OFF_K + s * C::KV_BYTES + p * C::PANEL, &tmK, bar(C::B_KF + s),
-                      p * C::PE, kvh, j * C::BN, b);
-        mbar_expect_tx(bar(C::B_VF + s), C::KV_BYTES);
+          tma_load_4d(sbase + C::OFF_K + sk * C::KV_BYTES + p * C::PANEL, &tmK, bar(C::B_KF + sk),
+                      p * C::PE, kvh, jk * C::BN, b);
+        ++jk;
+        const int sv = jv % C::NSV;
+        if (jv >= C::NSV && !mbar_wait(bar(C::B_VE + sv), ((jv / C::NSV) - 1) & 1, w)) break;
+        mbar_expect_tx(bar(C::B_VF + sv), C::KV_BYTES);
         for (int p = 0; p < C::DPANELS; ++p)
-          tma_load_4d(sbase + C::OFF_V + s * C::KV_BYTES + p * C::PANEL, &tmV, bar(C::B_VF + s),
-                      p * C::PE, kvh, j * C::BN, b);
+          tma_load_4d(sbase + C::OFF_V + sv * C::KV_BYTES + p * C::PANEL, &tmV, bar(C::B_VF + sv),
+                      p * C::PE, kvh, jv * C::BN, b);
       }
       // Exit path: every load this thread issued has landed before shared
       // memory is released (immediate unless a wait above gave up).
       mbar_drain(bar(C::B_Q), 0, a.timeout_ns);
-      for (int s = 0; s < C::NS && s < j; ++s) {
-        const int last = s + ((j - 1 - s) / C::NS) * C::NS;
-        const uint32_t par = (last / C::NS) & 1;
-        mbar_drain(bar(C::B_KF + s), par, a.timeout_ns);
-        mbar_drain(bar(C::B_VF + s), par, a.timeout_ns);
+      for (int s = 0; s < C::NSK && s < jk; ++s) {
+        const int last = s + ((jk - 1 - s) / C::NSK) * C::NSK;
+        mbar_drain(bar(C::B_KF + s), (last / C::NSK) & 1, a.timeout_ns);
+      }
+      for (int s = 0; s < C::NSV && s < jv; ++s) {
+        const int last = s + ((jv - 1 - s) / C::NSV) * C::NSV;
+        mbar_drain(bar(C::B_VF + s), (last / C::NSV) & 1, a.timeout_ns);
       }
     }
   } else if (warp == 1) {
@@ -168,27 +225,46 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t pb = sbase + C::OFF_P;
       auto issue_pv = [&](int jj) -> bool {
         if (!mbar_wait(bar(C::B_PF), jj & 1, w)) return false;
-        const int s = jj % C::NS;
-        if (!mbar_wait(bar(C::B_VF + s), (jj / C::NS) & 1, w)) return false;
-        tc_fence_after();
-        const uint32_t vb = sbase + C::OFF_V + s * C::KV_BYTES;
-#pragma unroll
-        for (int k = 0; k < C::BN / C::KSTEP; ++k) {
-          const uint64_t ad = make_sdesc(pb + (k / C::SPP) * C::PANEL + (k % C::SPP) * 32, 16, 1024);
-          const uint64_t bd = make_sdesc(vb + k * C::KSTEP * 128, C::PANEL, 1024);
-          mma_ss<TF32>(tmem + C::TMEM_O, ad, bd, C::IDESC_PV, (jj > 0 || k > 0) ? 1u : 0u);
+        const int sv = jj % C::NSV;
+        if constexpr (!TF32) {
+          if (!mbar_wait(bar(C::B_VF + sv), (jj / C::NSV) & 1, w)) return false;
         }
-        tc_commit(bar(C::B_OD + (jj & 1)));
-        tc_commit(bar(C::B_KVE + s));
+        tc_fence_after();
+        if constexpr (TF32) {
+          // O += Phi Vhi + Phi Vlo + Plo Vhi  (bf16 products, fp32 accumulate)
+          const uint32_t vh = sbase + C::OFF_VHL, vl = vh + C::VB_PANELS * C::PANEL;
+#pragma unroll
+          for (int k = 0; k < C::BN / 16; ++k) {
+            const uint32_t aoff = (k / 4) * C::PANEL + (k % 4) * 32;
+            const uint64_t ah = make_sdesc(pb + aoff, 16, 1024);
+            const uint64_t al = make_sdesc(pb + C::P_HALF + aoff, 16, 1024);
+            const uint64_t bh_ = make_sdesc(vh + k * 16 * 128, C::PANEL, 1024);
+            const uint64_t bl = make_sdesc(vl + k * 16 * 128, C::PANEL, 1024);
+            mma_ss<false>(tmem + C::TMEM_O, ah, bh_, C::IDESC_PV, (jj > 0 || k > 0) ? 1u : 0u);
+            mma_ss<false>(tmem + C::TMEM_O, ah, bl, C::IDESC_PV, 1u);
+            mma_ss<false>(tmem + C::TMEM_O, al, bh_, C::IDESC_PV, 1u);
+          }
+          tc_commit(bar(C::B_OD + (jj & 1)));
+        } else {
+          const uint32_t vb = sbase + C::OFF_V + sv * C::KV_BYTES;
+#pragma unroll
+          for (int k = 0; k < C::BN / 16; ++k) {
+            const uint64_t ad = make_sdesc(pb + (k / 4) * C::PANEL + (k % 4) * 32, 16, 1024);
+            const uint64_t bd = make_sdesc(vb + k * 16 * 128, C::PANEL, 1024);
+            mma_ss<false>(tmem + C::TMEM_O, ad, bd, C::IDESC_PV, (jj > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(bar(C::B_OD + (jj & 1)));
+          tc_commit(bar(C::B_VE + sv));
+        }
         return true;
       };
       for (int j = 0; ok && j < nkv; ++j) {
-        const int s = j % C::NS;
+        const int sk = j % C::NSK;
         const int sb = j & 1;
-        if (!mbar_wait(bar(C::B_KF + s), (j / C::NS) & 1, w)) { ok = false; break; }
+        if (!mbar_wait(bar(C::B_KF + sk), (j / C::NSK) & 1, w)) { ok = false; break; }
         if (j >= 2 && !mbar_wait(bar(C::B_SFREE + sb), ((j - 2) >> 1) & 1, w)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kb = sbase + C::OFF_K + s * C::KV_BYTES;
+        const uint32_t kb = sbase + C::OFF_K + sk * C::KV_BYTES;
 #pragma unroll
         for (int k = 0; k < DHP / C::KSTEP; ++k) {
           const uint32_t off = (k / C::SPP) * C::PANEL + (k % C::SPP) * 32;
@@ -196,6 +272,7 @@ __global__ void __launch_bounds__(192, 1)
                        make_sdesc(kb + off, 16, 1024), C::IDESC_QK, k > 0 ? 1u : 0u);
         }
         tc_commit(bar(C::B_SF + sb));
+        tc_commit(bar(C::B_KE + sk));
         if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
       }
       if (ok) issue_pv(nkv - 1);
@@ -238,7 +315,8 @@ __global__ void __launch_bounds__(192, 1)
       for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
       const float m_cand = mx * sl2;
       if (j > 0) {
-        // P_{j-1} has been consumed and O holds all earlier tiles.
+        // P_{j-1} V_{j-1} is complete: P (and the fp32-mode V hi/lo tile) may be
+        // overwritten and O holds every earlier tile.
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_OD + ((j - 1) & 1)), ((j - 1) >> 1) & 1, w));
         if (!ok) break;
         tc_fence_after();
@@ -268,19 +346,28 @@ __global__ void __launch_bounds__(192, 1)
         sum += s[c];
       }
       l += sum;
-      // P row -> shared memory, K-major with the 128-byte swizzle the MMA expects.
-      const uint32_t prow = sbase + C::OFF_P + row * 128;
       if constexpr (TF32) {
+        // V_j: fp32 stage -> bf16 hi/lo tile, then release the stage.
+        const int sv = j % C::NSV;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_VF + sv), (j / C::NSV) & 1, w));
+        if (!ok) break;
+        const uint32_t vh = sbase + C::OFF_VHL;
+        split_v_row<C>(sbase + C::OFF_V + sv * C::KV_BYTES, vh, vh + C::VB_PANELS * C::PANEL, row);
+        mbar_arrive(bar(C::B_VE + sv));
+      }
+      // P row -> shared memory (bf16; fp32 mode writes hi and lo), K-major with
+      // the 128-byte swizzle the MMA expects.
+      const uint32_t prow = sbase + C::OFF_P + row * 128;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const uint32_t addr = prow + (c >> 3) * C::PANEL + (((c & 7) ^ (row & 7)) << 4);
-          st_shared_v4(addr, to_tf32(s[4 * c]), to_tf32(s[4 * c + 1]), to_tf32(s[4 * c + 2]),
-                       to_tf32(s[4 * c + 3]));
-        }
-      } else {
+      for (int c = 0; c < 16; ++c) {
+        const uint32_t addr = prow + (c >> 3) * C::PANEL + (((c & 7) ^ (row & 7)) << 4);
+        if constexpr (TF32) {
+          uint32_t hi[4], lo[4];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint32_t addr = prow + (c >> 3) * C::PANEL + (((c & 7) ^ (row & 7)) << 4);
+          for (int i = 0; i < 4; ++i) split_bf16x2(s[8 * c + 2 * i], s[8 * c + 2 * i + 1], hi[i], lo[i]);
+          st_shared_v4(addr, hi[0], hi[1], hi[2], hi[3]);
+          st_shared_v4(addr + C::P_HALF, lo[0], lo[1], lo[2], lo[3]);
+        } else {
           st_shared_v4(addr, pack_bf16(s[8 * c], s[8 * c + 1]), pack_bf16(s[8 * c + 2], s[8 * c + 3]),
                        pack_bf16(s[8 * c + 4], s[8 * c + 5]), pack_bf16(s[8 * c + 6], s[8 * c + 7]));
         }

@@ -62,6 +62,7 @@ EncodeFn get_encode() {
 // columns past Dh read as zero.
 rca_status make_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t H, int64_t Dh,
                     bool f32, const char* name) {
+  // (f32 selects fp32 elements with 32-element panels; bf16 uses 64-element panels)
   EncodeFn enc = get_encode();
   if (!enc) return fail(RCA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorName(g_encode_err));
   const uint64_t es = f32 ? 4 : 2;
@@ -148,19 +149,28 @@ rca_status check_shape(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh
 }
 
 struct WsLayout {
-  size_t dq_off, lse2_off, d_off, total;
+  size_t dq_off, lse2_off, d_off, hl_off, total;
+  size_t q_part, kv_part;  // bytes of one bf16 part of Q/dO and of K/V (fp32 storage only)
   int64_t Tpad;
 };
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
-WsLayout ws_layout(int64_t B, int64_t Hq, int64_t T, int64_t Dh) {
+// fp32 accumulator for dQ [B,T,Hq,Dh]; base-2 LSE and D rows [B,Hq,Tpad]; and,
+// for fp32 storage, bf16 hi/lo copies of Q, dO [B,T,Hq,Dh] and K, V [B,T,Hkv,Dh].
+WsLayout ws_layout(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt) {
   WsLayout w{};
   w.Tpad = (T + 127) / 128 * 128;
   w.dq_off = 0;
   w.lse2_off = round256(size_t(B) * T * Hq * Dh * 4);
   w.d_off = w.lse2_off + round256(size_t(B) * Hq * w.Tpad * 4);
-  w.total = w.d_off + round256(size_t(B) * Hq * w.Tpad * 4);
+  w.hl_off = w.d_off + round256(size_t(B) * Hq * w.Tpad * 4);
+  w.total = w.hl_off;
+  if (dt == RCA_F32_TF32) {
+    w.q_part = round256(size_t(B) * T * Hq * Dh * 2);
+    w.kv_part = round256(size_t(B) * T * Hkv * Dh * 2);
+    w.total += 4 * w.q_part + 4 * w.kv_part;  // Qhi, Qlo, dOhi, dOlo, Khi, Klo, Vhi, Vlo
+  }
   return w;
 }
 
@@ -219,23 +229,67 @@ rca_status launch_fwd(const void* q, const void* k, const void* v, int64_t B, in
   return RCA_OK;
 }
 
-template <bool TF32, int DHP>
+rca_status launch_split(const void* src, void* hi, void* lo, size_t n, cudaStream_t st) {
+  const long long n4 = (long long)(n / 4);
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long want = (n4 + 255) / 256, cap = (long long)sms * 8;
+  const unsigned grid = unsigned(want < cap ? (want > 0 ? want : 1) : cap);
+  rca::split_hilo_kernel<<<grid, 256, 0, st>>>(static_cast<const float*>(src), static_cast<__nv_bfloat16*>(hi),
+                                                static_cast<__nv_bfloat16*>(lo), n4);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch split_hilo_kernel");
+  return RCA_OK;
+}
+
+template <bool HL, int DHB>
 rca_status launch_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
                            int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, void* ws,
                            const WsLayout& L, cudaStream_t st) {
-  using C = rca::BwdCfg<TF32, DHP>;
+  using C = rca::BwdCfg<HL, DHB>;
   static std::atomic<unsigned long long> smem_set{0};
-  CUtensorMap mq, mk, mv, mdo;
-  RCA_CHECK(make_map(&mq, q, B, T, Hq, Dh, TF32, "q"));
-  RCA_CHECK(make_map(&mk, k, B, T, Hkv, Dh, TF32, "k"));
-  RCA_CHECK(make_map(&mv, v, B, T, Hkv, Dh, TF32, "v"));
-  RCA_CHECK(make_map(&mdo, dout, B, T, Hq, Dh, TF32, "dout"));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  rca::BwdMaps maps;
+  if constexpr (HL) {
+    // fp32 storage: bf16 hi/lo copies live in the workspace.
+    uint8_t* hl = w + L.hl_off;
+    void* qh = hl;
+    void* ql = hl + L.q_part;
+    void* dh = hl + 2 * L.q_part;
+    void* dl = hl + 3 * L.q_part;
+    void* kh = hl + 4 * L.q_part;
+    void* kl = kh + L.kv_part;
+    void* vh = static_cast<uint8_t*>(kh) + 2 * L.kv_part;
+    void* vl = static_cast<uint8_t*>(kh) + 3 * L.kv_part;
+    const size_t nq = size_t(B) * T * Hq * Dh, nkv = size_t(B) * T * Hkv * Dh;
+    RCA_CHECK(launch_split(q, qh, ql, nq, st));
+    RCA_CHECK(launch_split(dout, dh, dl, nq, st));
+    RCA_CHECK(launch_split(k, kh, kl, nkv, st));
+    RCA_CHECK(launch_split(v, vh, vl, nkv, st));
+    RCA_CHECK(make_map(&maps.q[0], qh, B, T, Hq, Dh, false, "q hi"));
+    RCA_CHECK(make_map(&maps.q[1], ql, B, T, Hq, Dh, false, "q lo"));
+    RCA_CHECK(make_map(&maps.dO[0], dh, B, T, Hq, Dh, false, "dout hi"));
+    RCA_CHECK(make_map(&maps.dO[1], dl, B, T, Hq, Dh, false, "dout lo"));
+    RCA_CHECK(make_map(&maps.k[0], kh, B, T, Hkv, Dh, false, "k hi"));
+    RCA_CHECK(make_map(&maps.k[1], kl, B, T, Hkv, Dh, false, "k lo"));
+    RCA_CHECK(make_map(&maps.v[0], vh, B, T, Hkv, Dh, false, "v hi"));
+    RCA_CHECK(make_map(&maps.v[1], vl, B, T, Hkv, Dh, false, "v lo"));
+  } else {
+    RCA_CHECK(make_map(&maps.q[0], q, B, T, Hq, Dh, false, "q"));
+    RCA_CHECK(make_map(&maps.k[0], k, B, T, Hkv, Dh, false, "k"));
+    RCA_CHECK(make_map(&maps.v[0], v, B, T, Hkv, Dh, false, "v"));
+    RCA_CHECK(make_map(&maps.dO[0], dout, B, T, Hq, Dh, false, "dout"));
+    maps.q[1] = maps.q[0];
+    maps.k[1] = maps.k[0];
+    maps.v[1] = maps.v[0];
+    maps.dO[1] = maps.dO[0];
+  }
   int* status = nullptr;
   RCA_CHECK(status_word(&status));
-  auto kern = rca::attn_bwd_main_kernel<TF32, DHP>;
+  auto kern = rca::attn_bwd_main_kernel<HL, DHB>;
   cudaError_t e = ensure_smem(kern, C::SMEM_BYTES, smem_set);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
-  uint8_t* w = static_cast<uint8_t*>(ws);
   rca::BwdArgs a{};
   a.dk = dk;
   a.dv = dv;
@@ -251,7 +305,7 @@ rca_status launch_bwd_main(const void* q, const void* k, const void* v, const vo
   a.scale = float(1.0 / std::sqrt(double(Dh)));
   a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(Dh)));
   const unsigned grid = unsigned(int64_t(a.n_t) * B * Hkv);
-  kern<<<grid, 192, C::SMEM_BYTES, st>>>(mq, mk, mv, mdo, a);
+  kern<<<grid, 192, C::SMEM_BYTES, st>>>(maps, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch attn_bwd_main_kernel");
   return RCA_OK;
@@ -274,7 +328,6 @@ rca_status do_bwd_main(const void* q, const void* k, const void* v, const void* 
     if (Dh <= 64) return launch_bwd_main<false, 64>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st);
     return launch_bwd_main<false, 128>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st);
   }
-  if (Dh <= 32) return launch_bwd_main<true, 32>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st);
   return launch_bwd_main<true, 64>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st);
 }
 
@@ -346,21 +399,22 @@ rca_status rca_attn_fwd(const void* q, const void* k, const void* v, int64_t B, 
   RCA_GUARD_END
 }
 
-size_t rca_attn_bwd_workspace_size(int64_t B, int64_t Hq, int64_t T, int64_t Dh) {
-  if (B < 1 || Hq < 1 || T < 1 || Dh < 1 || T > (int64_t(1) << 30)) return 0;
-  return ws_layout(B, Hq, T, Dh).total;
+size_t rca_attn_bwd_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hkv > Hq || T < 1 || Dh < 1 || T > (int64_t(1) << 30)) return 0;
+  if (dt != RCA_BF16 && dt != RCA_F32_TF32) return 0;
+  return ws_layout(B, Hq, Hkv, T, Dh, dt).total;
 }
 
 rca_status rca_attn_bwd_preprocess(const void* out, const float* lse, const void* dout, int64_t B, int64_t Hq,
-                                   int64_t T, int64_t Dh, rca_dtype dt, void* workspace, size_t workspace_bytes,
-                                   void* cuda_stream) {
+                                   int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt, void* workspace,
+                                   size_t workspace_bytes, void* cuda_stream) {
   RCA_GUARD_BEGIN
   g_err.clear();
   if (!out || !lse || !dout) return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd_preprocess: null pointer");
-  RCA_CHECK(check_shape(B, Hq, Hq, T, Dh, dt));
+  RCA_CHECK(check_shape(B, Hq, Hkv, T, Dh, dt));
   if (!aligned16(out) || !aligned16(dout) || !aligned16(lse))
     return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd_preprocess: out, dout and lse must be 16-byte aligned");
-  const WsLayout L = ws_layout(B, Hq, T, Dh);
+  const WsLayout L = ws_layout(B, Hq, Hkv, T, Dh, dt);
   RCA_CHECK(check_ws(workspace, workspace_bytes, L));
   return do_preprocess(out, lse, dout, B, Hq, T, Dh, dt, workspace, L, static_cast<cudaStream_t>(cuda_stream));
   RCA_GUARD_END
@@ -376,21 +430,22 @@ rca_status rca_attn_bwd_main(const void* q, const void* k, const void* v, const 
   RCA_CHECK(check_shape(B, Hq, Hkv, T, Dh, dt));
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dk) || !aligned16(dv))
     return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd_main: tensors must be 16-byte aligned");
-  const WsLayout L = ws_layout(B, Hq, T, Dh);
+  const WsLayout L = ws_layout(B, Hq, Hkv, T, Dh, dt);
   RCA_CHECK(check_ws(workspace, workspace_bytes, L));
   return do_bwd_main(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, dt, workspace, L,
                      static_cast<cudaStream_t>(cuda_stream));
   RCA_GUARD_END
 }
 
-rca_status rca_attn_bwd_dq_convert(void* dq, int64_t B, int64_t Hq, int64_t T, int64_t Dh, rca_dtype dt,
-                                   const void* workspace, size_t workspace_bytes, void* cuda_stream) {
+rca_status rca_attn_bwd_dq_convert(void* dq, int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
+                                   rca_dtype dt, const void* workspace, size_t workspace_bytes,
+                                   void* cuda_stream) {
   RCA_GUARD_BEGIN
   g_err.clear();
   if (!dq) return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd_dq_convert: null pointer");
-  RCA_CHECK(check_shape(B, Hq, Hq, T, Dh, dt));
+  RCA_CHECK(check_shape(B, Hq, Hkv, T, Dh, dt));
   if (!aligned16(dq)) return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd_dq_convert: dq must be 16-byte aligned");
-  const WsLayout L = ws_layout(B, Hq, T, Dh);
+  const WsLayout L = ws_layout(B, Hq, Hkv, T, Dh, dt);
   RCA_CHECK(check_ws(workspace, workspace_bytes, L));
   return do_convert(dq, B, Hq, T, Dh, dt, workspace, L, static_cast<cudaStream_t>(cuda_stream));
   RCA_GUARD_END
@@ -408,7 +463,7 @@ rca_status rca_attn_bwd(const void* q, const void* k, const void* v, const void*
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) ||
       !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd: tensors must be 16-byte aligned");
-  const WsLayout L = ws_layout(B, Hq, T, Dh);
+  const WsLayout L = ws_layout(B, Hq, Hkv, T, Dh, dt);
   RCA_CHECK(check_ws(workspace, workspace_bytes, L));
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   RCA_CHECK(do_preprocess(out, lse, dout, B, Hq, T, Dh, dt, workspace, L, st));

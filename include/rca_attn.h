@@ -30,7 +30,11 @@
  *   k, v, dk, dv     : [B, T, Hkv, Dh]   storage dtype
  *   lse              : [B, Hq, T]        float32
  * Storage dtype: RCA_BF16 (bfloat16 operands, fp32 accumulation) or
- * RCA_F32_TF32 (float32 storage, TF32 tensor-core operands, fp32 accumulation).
+ * RCA_F32_TF32 (float32 storage, fp32 accumulation). In fp32 mode the forward's
+ * Q K^T uses TF32 tensor-core operands; the products that contract over key or
+ * query positions (P V in the forward, all five backward products) use each
+ * fp32 operand split into two bf16 values x = hi + lo and the three products
+ * hi.hi + hi.lo + lo.hi, which is at least as accurate as TF32.
  * Supported head widths: Dh in {16, 32, 64, 128} for RCA_BF16 and
  * {16, 32, 64} for RCA_F32_TF32; anything else is RCA_ERR_UNSUPPORTED.
  *
@@ -91,11 +95,13 @@ rca_status rca_attn_fwd(const void* q, const void* k, const void* v,
                         void* out, float* lse, rca_dtype dt, void* cuda_stream);
 
 /*
- * Bytes of device scratch rca_attn_bwd needs: an fp32 dQ accumulator and the
- * per-row D and LSE rows, each padded to a multiple of 128 positions.
- * Returns 0 for invalid sizes.
+ * Bytes of device scratch rca_attn_bwd needs for these sizes and dtype: an fp32
+ * dQ accumulator [B,T,Hq,Dh], the per-row D and base-2 LSE [B,Hq,Tpad] (Tpad =
+ * T rounded up to 128), and for RCA_F32_TF32 bf16 hi/lo copies of Q, dout, K
+ * and V. Returns 0 for invalid sizes.
  */
-size_t rca_attn_bwd_workspace_size(int64_t B, int64_t Hq, int64_t T, int64_t Dh);
+size_t rca_attn_bwd_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
+                                   rca_dtype dt);
 
 /*
  * Backward. Given the forward's out and lse and the upstream gradient dout,
@@ -119,10 +125,11 @@ rca_status rca_attn_bwd(const void* q, const void* k, const void* v, const void*
  *              (memory-bound).
  *  main:       recomputes P from Q, K and LSE; accumulates dK, dV per key tile
  *              (written to dk, dv) and adds dQ partials into the workspace.
+ *              For RCA_F32_TF32 it first writes the bf16 hi/lo operand copies.
  *  dq_convert: dq = scale * accumulator, cast to the storage dtype.
  */
 rca_status rca_attn_bwd_preprocess(const void* out, const float* lse, const void* dout,
-                                   int64_t B, int64_t Hq, int64_t T, int64_t Dh,
+                                   int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
                                    rca_dtype dt, void* workspace, size_t workspace_bytes,
                                    void* cuda_stream);
 rca_status rca_attn_bwd_main(const void* q, const void* k, const void* v, const void* dout,
@@ -130,9 +137,9 @@ rca_status rca_attn_bwd_main(const void* q, const void* k, const void* v, const 
                              int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
                              rca_dtype dt, void* workspace, size_t workspace_bytes,
                              void* cuda_stream);
-rca_status rca_attn_bwd_dq_convert(void* dq, int64_t B, int64_t Hq, int64_t T, int64_t Dh,
-                                   rca_dtype dt, const void* workspace, size_t workspace_bytes,
-                                   void* cuda_stream);
+rca_status rca_attn_bwd_dq_convert(void* dq, int64_t B, int64_t Hq, int64_t Hkv, int64_t T,
+                                   int64_t Dh, rca_dtype dt, const void* workspace,
+                                   size_t workspace_bytes, void* cuda_stream);
 
 /*
  * Synchronises cuda_stream, then reports (and clears) an asynchronous CUDA

@@ -73,9 +73,14 @@ def test_fwd_validation(lib, kw, status, needle):
 
 
 def test_workspace_size_and_checks(lib):
-    n = lib.rca_attn_bwd_workspace_size(4, 16, 2048, 64)
+    n = lib.rca_attn_bwd_workspace_size(4, 16, 16, 2048, 64, 1)
     assert n >= 4 * 2048 * 16 * 64 * 4 + 2 * 4 * 16 * 2048 * 4
-    assert lib.rca_attn_bwd_workspace_size(0, 16, 2048, 64) == 0
+    # fp32 storage adds bf16 hi/lo copies of Q, dO, K, V
+    n32 = lib.rca_attn_bwd_workspace_size(4, 16, 4, 2048, 64, 0)
+    assert n32 >= n + 4 * 2048 * 64 * 2 * 2 * (2 * 16 + 2 * 4) - 4096
+    assert lib.rca_attn_bwd_workspace_size(0, 16, 16, 2048, 64, 1) == 0
+    assert lib.rca_attn_bwd_workspace_size(1, 4, 8, 16, 64, 1) == 0  # Hkv > Hq
+    assert lib.rca_attn_bwd_workspace_size(1, 4, 4, 16, 64, 9) == 0  # unknown dtype
     # too small a workspace is rejected before anything runs
     st = lib.rca_attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 2, 8, 64, 1,
                           ctypes.c_void_p(4096), 16, NULL)

@@ -99,11 +99,11 @@ def test_stages_equal_composite():
     q, k, v, do = (x.cuda() for x in make_inputs(w))
     out, lse = rca.attention_forward(q, k, v)
     dq1, dk1, dv1 = rca.attention_backward(q, k, v, out, lse, do)
-    ws = rca.workspace_for(q)
+    ws = rca.workspace_for(q, k)
     dq2, dk2, dv2 = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    rca.rca_attn_bwd_preprocess(out, lse, do, ws)
+    rca.rca_attn_bwd_preprocess(out, lse, do, ws, Hkv=k.shape[2])
     rca.rca_attn_bwd_main(q, k, v, do, dk2, dv2, ws)
-    rca.rca_attn_bwd_dq_convert(dq2, ws)
+    rca.rca_attn_bwd_dq_convert(dq2, ws, Hkv=k.shape[2])
     rca.rca_stream_status()
     # dK/dV are written once per key tile: identical. dQ sums atomics: order may differ.
     assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
