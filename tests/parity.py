@@ -13,19 +13,31 @@ TOL = {
     "fp32": {"O": 1e-3, "LSE": 1e-3, "dQ": 3e-3, "dK": 3e-3, "dV": 3e-3},
 }
 
-# Absolute floor (RMS per element) added to the denominator of the relative
-# error. It only matters where the reference vanishes identically, e.g. dQ and
-# dK at T = 1, which are exactly 0 in exact arithmetic (the oracle returns
-# ~1e-17 from rounding, so a pure ratio would be meaningless there).
-ATOL_RMS = 1e-5
 
-
-def rel_fro(got, ref, atol_rms: float = ATOL_RMS) -> float:
-    """||got - ref||_F / (||ref||_F + atol_rms * sqrt(n)), in fp64."""
+def rel_fro(got, ref, den=None) -> float:
+    """||got - ref||_F / ||ref||_F in fp64 (or / den when given)."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
-    den = np.linalg.norm(ref) + atol_rms * np.sqrt(max(ref.size, 1))
+    if den is None:
+        den = np.linalg.norm(ref)
+    if den == 0.0:
+        return float(np.linalg.norm(got - ref))
     return float(np.linalg.norm(got - ref) / den)
+
+
+def uncancelled_norms(q, k, v, do):
+    """For T = 1, dQ and dK vanish identically (dS = P (dP - D) with P = 1 and
+    D = dP): their relative error is undefined. The error is then measured
+    against the size of the terms that cancel, scale * (P * dP) K for dQ and
+    scale * (P * dP)^T Q for dK. Returns (||.||_F for dQ, for dK)."""
+    q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
+    assert q.shape[1] == 1
+    g = q.shape[2] // k.shape[2]
+    scale = oracle.default_scale(q.shape[3])
+    kk = np.repeat(k, g, axis=2)
+    vv = np.repeat(v, g, axis=2)
+    dp = np.sum(do * vv, axis=-1, keepdims=True)  # [B,1,Hq,1]
+    return float(np.linalg.norm(scale * dp * kk)), float(np.linalg.norm(scale * dp * q))
 
 
 def to64(t) -> np.ndarray:
