@@ -138,6 +138,19 @@ def dist_setup():
     return world, rank, local
 
 
+def rank_workload(w, rank: int):
+    """This rank's batch: same shapes, its own seed, so ranks process distinct
+    (batch, head) units with nothing to exchange (weak scaling)."""
+    from dataclasses import replace
+
+    return w if rank == 0 else replace(w, seed=w.seed + 1000 * rank)
+
+
+def aggregate_tflops(step_flops: float, world: int, ms_per_step_max: float) -> float:
+    """Whole-job throughput: every rank's FLOPs over the slowest rank's time."""
+    return step_flops * world / (ms_per_step_max * 1e-3) / 1e12
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -233,7 +246,7 @@ def run_gpu(args, w, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     P = peaks()
 
-    q0, k0, v0, do0 = make_inputs(w)
+    q0, k0, v0, do0 = make_inputs(rank_workload(w, rank))
     set_bytes = sum(x.numel() * x.element_size() for x in (q0, k0, v0, do0))
     nsets = max(2, -(-2 * L2_BYTES // set_bytes) + 1)
     # Distinct copies of the same inputs, so each step reads memory the previous
@@ -302,7 +315,7 @@ def run_gpu(args, w, world, rank, local):
     ms = max_over_ranks(total_ms, world) / args.steps
     F = fwd_flops(w)
     step_flops = 3.5 * F
-    value = step_flops * world / (ms * 1e-3) / 1e12
+    value = aggregate_tflops(step_flops, world, ms)
 
     es = 2 if w.dtype == "bf16" else 4
     n_q = w.B * w.T * w.Hq * w.Dh
@@ -375,7 +388,7 @@ def run_gpu(args, w, world, rank, local):
         e_ms = max_over_ranks(a.elapsed_time(bev), world) / args.steps
         h2d = sum(x.numel() * x.element_size() for x in (hq_, hk_, hv_, hdo_))
         d2h = sum(x.numel() * x.element_size() for x in (ho, hl, hdq, hdk, hdv))
-        e2e = {"value": step_flops * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": aggregate_tflops(step_flops, world, e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
 
     cpu = None
