@@ -14,6 +14,7 @@ from ._native import (  # noqa: F401  (C-ABI names)
     rca_attn_bwd,
     rca_attn_bwd_dq_convert,
     rca_attn_bwd_main,
+    rca_attn_bwd_noalloc,
     rca_attn_bwd_preprocess,
     rca_attn_bwd_workspace_size,
     rca_attn_fwd,
@@ -35,6 +36,7 @@ __all__ = [
     "rca_attn_bwd_preprocess",
     "rca_attn_bwd_main",
     "rca_attn_bwd_dq_convert",
+    "rca_attn_bwd_noalloc",
     "rca_stream_status",
     "rca_last_error",
     "rca_set_wait_timeout_ns",

@@ -45,6 +45,8 @@ _SIG = {
                                          _P, ctypes.c_size_t, _P]),
     "rca_attn_bwd_dq_convert": (ctypes.c_int, [_P, _I, _I, _I, _I, _I, ctypes.c_int, _P,
                                                ctypes.c_size_t, _P]),
+    "rca_attn_bwd_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                            ctypes.c_int, _P]),
     "rca_stream_status": (ctypes.c_int, [_P]),
     "rca_set_wait_timeout_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
 }
@@ -179,6 +181,13 @@ def rca_attn_bwd_dq_convert(dq, workspace, Hkv=None, stream=None):
     Hkv = Hq if Hkv is None else Hkv
     _check(lib().rca_attn_bwd_dq_convert(_ptr(dq), B, Hq, Hkv, T, Dh, _dtype_code(dq), _ptr(workspace),
                                          workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def rca_attn_bwd_noalloc(q, k, v, out, lse, dout, dq, dk, dv, stream=None):
+    """Backward with the library's built-in scratch (no workspace, no allocation)."""
+    B, Hq, Hkv, T, Dh = _shape(q, k)
+    _check(lib().rca_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
+                                      _ptr(dk), _ptr(dv), B, Hq, Hkv, T, Dh, _dtype_code(q), _stream(stream)))
 
 
 def rca_stream_status(stream=None):

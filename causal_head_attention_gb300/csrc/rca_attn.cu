@@ -246,7 +246,7 @@ rca_status launch_split(const void* src, void* hi, void* lo, size_t n, cudaStrea
 template <bool HL, int DHB>
 rca_status launch_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
                            int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, void* ws,
-                           const WsLayout& L, cudaStream_t st) {
+                           const WsLayout& L, cudaStream_t st, int* status_override = nullptr) {
   using C = rca::BwdCfg<HL, DHB>;
   static std::atomic<unsigned long long> smem_set{0};
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -285,8 +285,8 @@ rca_status launch_bwd_main(const void* q, const void* k, const void* v, const vo
     maps.v[1] = maps.v[0];
     maps.dO[1] = maps.dO[0];
   }
-  int* status = nullptr;
-  RCA_CHECK(status_word(&status));
+  int* status = status_override;
+  if (!status) RCA_CHECK(status_word(&status));
   auto kern = rca::attn_bwd_main_kernel<HL, DHB>;
   cudaError_t e = ensure_smem(kern, C::SMEM_BYTES, smem_set);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
@@ -323,12 +323,13 @@ rca_status do_fwd(const void* q, const void* k, const void* v, int64_t B, int64_
 
 rca_status do_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
                        int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt, void* ws,
-                       const WsLayout& L, cudaStream_t st) {
+                       const WsLayout& L, cudaStream_t st, int* status_override = nullptr) {
   if (dt == RCA_BF16) {
-    if (Dh <= 64) return launch_bwd_main<false, 64>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st);
-    return launch_bwd_main<false, 128>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st);
+    if (Dh <= 64)
+      return launch_bwd_main<false, 64>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st, status_override);
+    return launch_bwd_main<false, 128>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st, status_override);
   }
-  return launch_bwd_main<true, 64>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st);
+  return launch_bwd_main<true, 64>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st, status_override);
 }
 
 rca_status do_preprocess(const void* out, const float* lse, const void* dout, int64_t B, int64_t Hq, int64_t T,
@@ -494,3 +495,79 @@ rca_status rca_stream_status(void* cuda_stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward without any device allocation (rca_attn_bwd_noalloc).
+//
+// Some callers cannot allocate device memory when they call the backward: a
+// plugin interface that hands over only the input and output buffers, or a
+// latency-bound loop that must never hit cudaMalloc (which can synchronise the
+// device and take unbounded time). For them the scratch lives in this file-scope
+// device array instead of a caller workspace. It is part of the library image,
+// so every GPU that loads the library holds it until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(40) << 20;  // 40 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+static __device__ __align__(256) int g_noalloc_status;
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_scratch_ptr[256] = {};
+int* g_noalloc_status_ptr[256] = {};
+
+// Once per device, with that device current: the device addresses of the
+// scratch array and of its status word (host code cannot use the symbols'
+// names as device addresses).
+rca_status noalloc_setup(void** scratch, int** status) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 256) return fail(RCA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    void* ps = nullptr;
+    e = cudaGetSymbolAddress(&ps, g_noalloc_status);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    g_noalloc_scratch_ptr[dev] = p;
+    g_noalloc_status_ptr[dev] = static_cast<int*>(ps);
+  }
+  *scratch = g_noalloc_scratch_ptr[dev];
+  *status = g_noalloc_status_ptr[dev];
+  return RCA_OK;
+}
+
+}  // namespace
+
+extern "C" rca_status rca_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* out,
+                                           const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                           int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
+                                           rca_dtype dt, void* cuda_stream) {
+  RCA_GUARD_BEGIN
+  g_err.clear();
+  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd_noalloc: null pointer");
+  RCA_CHECK(check_shape(B, Hq, Hkv, T, Dh, dt));
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd_noalloc: tensors must be 16-byte aligned");
+  const WsLayout L = ws_layout(B, Hq, Hkv, T, Dh, dt);
+  if (L.total > kNoAllocScratchBytes)
+    return fail(RCA_ERR_INVALID_ARGUMENT,
+                "rca_attn_bwd_noalloc: these sizes need %zu bytes of scratch but the built-in scratch "
+                "holds %zu bytes; use rca_attn_bwd with a caller workspace",
+                L.total, kNoAllocScratchBytes);
+  void* ws = nullptr;
+  int* status = nullptr;
+  RCA_CHECK(noalloc_setup(&ws, &status));
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  // The preprocess kernel rewrites every scratch word the later kernels read
+  // (it zeroes the dQ accumulator), so leftovers of an earlier call do not matter.
+  RCA_CHECK(do_preprocess(out, lse, dout, B, Hq, T, Dh, dt, ws, L, st));
+  RCA_CHECK(do_bwd_main(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, dt, ws, L, st, status));
+  return do_convert(dq, B, Hq, T, Dh, dt, ws, L, st);
+  RCA_GUARD_END
+}

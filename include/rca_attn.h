@@ -142,6 +142,31 @@ rca_status rca_attn_bwd_dq_convert(void* dq, int64_t B, int64_t Hq, int64_t Hkv,
                                    size_t workspace_bytes, void* cuda_stream);
 
 /*
+ * Backward that allocates nothing (no counterpart on the pages; an addition of
+ * this library). Same arguments and results as rca_attn_bwd minus the
+ * workspace: its scratch is a 40 MiB array built into the library, for callers
+ * that cannot allocate device memory when they call the backward (a plugin
+ * interface that passes only input and output buffers, or a latency-bound loop
+ * that must never reach cudaMalloc, which can synchronise the device).
+ *  - Sizes whose scratch (rca_attn_bwd_workspace_size) exceeds 40 MiB are
+ *    rejected with RCA_ERR_INVALID_ARGUMENT before anything is launched.
+ *  - The first call on a device looks up the array's device address with that
+ *    device current; make that first call before any stream capture.
+ *  - All calls share the one array and it keeps the last call's contents (each
+ *    call rewrites what it reads, so the leftovers never matter). Calls whose
+ *    work overlaps on the GPU (other streams, other threads) race on it:
+ *    serialise them.
+ *  - A device-side timeout in these kernels is recorded in a status word of
+ *    the built-in region, not in the one rca_stream_status reports; the
+ *    kernels still end within the wait limit.
+ * Never calls cudaMalloc, cudaFree or any allocating routine.
+ */
+rca_status rca_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* out,
+                                const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
+                                rca_dtype dt, void* cuda_stream);
+
+/*
  * Synchronises cuda_stream, then reports (and clears) an asynchronous CUDA
  * error or a device-side timeout recorded by a kernel of this library on the
  * current device. RCA_OK if neither happened.
