@@ -165,22 +165,31 @@ struct BwdCfg {
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
   // TMEM columns
   static constexpr int TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + DHB;
+  // dQ gets its own columns when they fit; otherwise it reuses the dP^T columns
+  // once both compute warpgroups have read dP^T.
   static constexpr bool DQ_ALIAS = 256 + 3 * DHB > 512;
-  static constexpr int TM_DQ = DQ_ALIAS ? 0 : 256 + 2 * DHB;
+  static constexpr int TM_DQ = DQ_ALIAS ? TM_DP : 256 + 2 * DHB;
+  // S^T / dP^T of the next iteration are computed while this iteration's dK and
+  // dQ products are pending; that needs a second Q/dO stage, separate P^T and
+  // dS^T buffers and dQ columns of its own.
+  static constexpr bool PREFETCH = (NQS >= 2) && !DQ_ALIAS && !SHARE;
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_T = make_idesc(false, 128, 128, false, false);   // S^T, dP^T
   static constexpr uint32_t IDESC_KV = make_idesc(false, 128, DHB, false, true);   // dV, dK
   static constexpr uint32_t IDESC_Q = make_idesc(false, 128, DHB, true, true);     // dQ
+  static constexpr int NTHREADS = 320;
   // barriers
   static constexpr int B_KV = 0;
   static constexpr int B_QF = 1;
   static constexpr int B_QE = B_QF + NQS;
-  static constexpr int B_SDP = B_QE + NQS;
-  static constexpr int B_PR = B_SDP + 1;
-  static constexpr int B_DVD = B_PR + 1;
-  static constexpr int B_DSR = B_DVD + 1;
-  static constexpr int B_DQF = B_DSR + 1;
-  static constexpr int B_ITF = B_DQF + 1;
+  static constexpr int B_SR = B_QE + NQS;   // S^T(it) in TMEM
+  static constexpr int B_DPR = B_SR + 1;    // dP^T(it) in TMEM
+  static constexpr int B_PR = B_DPR + 1;    // [2] P^T half g written
+  static constexpr int B_SDPF = B_PR + 2;   // S^T, dP^T of it read by both warpgroups
+  static constexpr int B_DVD = B_SDPF + 1;  // [2] dV half g done (shared P/dS buffer only)
+  static constexpr int B_DSR = B_DVD + 2;   // [2] dS^T half g written
+  static constexpr int B_DQF = B_DSR + 2;   // dQ(it) in TMEM (all MMAs of it done)
+  static constexpr int B_ITF = B_DQF + 1;   // dQ(it) drained by both warpgroups
   static constexpr int B_FIN = B_ITF + 1;
   static constexpr int NBAR = B_FIN + 1;
   // parts multiplied for one product: (hi,hi) [, (hi,lo), (lo,hi)]
@@ -206,13 +215,13 @@ struct BwdArgs {
   float scale, scale_log2;
 };
 
-// Thread row `rl` of a 128 x 128 bf16 (hi[/lo]) operand tile, K-major with the
-// 128-byte swizzle: 16 chunks of 8 values.
+// Thread row `rl` of one 64-column panel of a 128 x 128 bf16 (hi[/lo])
+// operand tile, K-major with the 128-byte swizzle: 8 chunks of 8 values.
 template <bool HL>
-__device__ __forceinline__ void store_row_bf16(uint32_t base, int rl, const float (&x)[128], int half_bytes) {
+__device__ __forceinline__ void store_half_row_bf16(uint32_t panel, int rl, const float (&x)[64], int half_bytes) {
 #pragma unroll
-  for (int c = 0; c < 16; ++c) {
-    const uint32_t addr = base + (c >> 3) * (128 * 128) + rl * 128 + (((c & 7) ^ (rl & 7)) << 4);
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t addr = panel + rl * 128 + ((c ^ (rl & 7)) << 4);
     if constexpr (HL) {
       uint32_t hi[4], lo[4];
 #pragma unroll
@@ -227,7 +236,7 @@ __device__ __forceinline__ void store_row_bf16(uint32_t base, int rl, const floa
 }
 
 template <bool HL, int DHB>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     attn_bwd_main_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   using C = BwdCfg<HL, DHB>;
   extern __shared__ uint8_t smem_raw[];
@@ -254,12 +263,16 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(bar(C::B_QF + s), 1);
       mbar_init(bar(C::B_QE + s), 1);
     }
-    mbar_init(bar(C::B_SDP), 1);
-    mbar_init(bar(C::B_PR), 128);
-    mbar_init(bar(C::B_DVD), 1);
-    mbar_init(bar(C::B_DSR), 128);
+    mbar_init(bar(C::B_SR), 1);
+    mbar_init(bar(C::B_DPR), 1);
+    mbar_init(bar(C::B_SDPF), 256);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(bar(C::B_PR + g), 128);
+      mbar_init(bar(C::B_DVD + g), 1);
+      mbar_init(bar(C::B_DSR + g), 128);
+    }
     mbar_init(bar(C::B_DQF), 1);
-    mbar_init(bar(C::B_ITF), 128);
+    mbar_init(bar(C::B_ITF), 256);
     mbar_init(bar(C::B_FIN), 1);
     *abort_flag = 0;
     mbar_init_fence();
@@ -275,8 +288,9 @@ __global__ void __launch_bounds__(192, 1)
   const WaitCtl w{a.status, abort_flag, a.timeout_ns};
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
+    // ---------------- TMA producer (whole warp; one elected lane issues) ----------------
+    const bool leader = elect_one();
+    if (leader) {
       for (int part = 0; part < C::NPART; ++part) {
         tma_prefetch_desc(&maps.q[part]);
         tma_prefetch_desc(&maps.k[part]);
@@ -291,13 +305,15 @@ __global__ void __launch_bounds__(192, 1)
           tma_load_4d(sbase + C::OFF_V + part * C::TILE + p * C::PANEL, &maps.v[part], bar(C::B_KV), p * 64,
                       kvh, j * 128, b);
         }
-      int it = 0;
-      for (; it < n_it; ++it) {
-        const int s = it % C::NQS;
-        if (it >= C::NQS && !mbar_wait(bar(C::B_QE + s), ((it / C::NQS) - 1) & 1, w)) break;
-        const int h = kvh * a.group + it / n_i;
-        const int i = j + it % n_i;
-        const uint32_t st = stage(s);
+    }
+    int it = 0;
+    for (; it < n_it; ++it) {
+      const int s = it % C::NQS;
+      if (it >= C::NQS && !mbar_wait_warp(bar(C::B_QE + s), ((it / C::NQS) - 1) & 1, w)) break;
+      const int h = kvh * a.group + it / n_i;
+      const int i = j + it % n_i;
+      const uint32_t st = stage(s);
+      if (leader) {
         mbar_expect_tx(bar(C::B_QF + s), 2 * C::OPND + 1024);
         for (int part = 0; part < C::NPART; ++part)
           for (int p = 0; p < C::DPANELS; ++p) {
@@ -310,6 +326,8 @@ __global__ void __launch_bounds__(192, 1)
         bulk_load(st + 2 * C::OPND, a.lse2 + ro, 512, bar(C::B_QF + s));
         bulk_load(st + 2 * C::OPND + 512, a.dvec + ro, 512, bar(C::B_QF + s));
       }
+    }
+    if (leader) {
       mbar_drain(bar(C::B_KV), 0, a.timeout_ns);
       for (int s = 0; s < C::NQS && s < it; ++s) {
         const int last = s + ((it - 1 - s) / C::NQS) * C::NQS;
@@ -317,199 +335,274 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else if (warp == 1) {
-    // ---------------- tcgen05 MMA issuer ----------------
-    if (lane == 0) {
-      bool ok = mbar_wait(bar(C::B_KV), 0, w);
-      const uint32_t kb = sbase + C::OFF_K, vb = sbase + C::OFF_V;
-      const uint32_t pb = sbase + C::OFF_P, dsb = sbase + C::OFF_DS;
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int s = it % C::NQS;
-        const uint32_t qb = stage(s), dob = stage(s) + C::OPND;
-        if (!mbar_wait(bar(C::B_QF + s), (it / C::NQS) & 1, w)) { ok = false; break; }
-        if (it > 0 && !mbar_wait(bar(C::B_ITF), (it - 1) & 1, w)) { ok = false; break; }
+    // ---------------- tcgen05 MMA issuer (whole warp; one elected lane issues) ----------------
+    const bool leader = elect_one();
+    const uint32_t kb = sbase + C::OFF_K, vb = sbase + C::OFF_V;
+    const uint32_t pb = sbase + C::OFF_P, dsb = sbase + C::OFF_DS;
+    // S^T = K Q^T (M = keys, N = queries, K = head dim) into TMEM_S
+    auto issue_s = [&](int it2) {
+      const uint32_t qb = stage(it2 % C::NQS);
+#pragma unroll
+      for (int t = 0; t < C::NPROD; ++t)
+#pragma unroll
+        for (int k = 0; k < DHB / 16; ++k) {
+          const uint32_t off = (k / 4) * C::PANEL + (k % 4) * 32;
+          const uint64_t ad = make_sdesc(kb + C::pa(t) * C::TILE + off, 16, 1024);
+          const uint64_t bd = make_sdesc(qb + C::pb(t) * C::TILE + off, 16, 1024);
+          if (leader) mma_ss<false>(tmem + C::TM_S, ad, bd, C::IDESC_T, (t > 0 || k > 0) ? 1u : 0u);
+        }
+      if (leader) tc_commit(bar(C::B_SR));
+    };
+    // dP^T = V dO^T into TMEM_DP
+    auto issue_dp = [&](int it2) {
+      const uint32_t dob = stage(it2 % C::NQS) + C::OPND;
+#pragma unroll
+      for (int t = 0; t < C::NPROD; ++t)
+#pragma unroll
+        for (int k = 0; k < DHB / 16; ++k) {
+          const uint32_t off = (k / 4) * C::PANEL + (k % 4) * 32;
+          const uint64_t ad = make_sdesc(vb + C::pa(t) * C::TILE + off, 16, 1024);
+          const uint64_t bd = make_sdesc(dob + C::pb(t) * C::TILE + off, 16, 1024);
+          if (leader) mma_ss<false>(tmem + C::TM_DP, ad, bd, C::IDESC_T, (t > 0 || k > 0) ? 1u : 0u);
+        }
+      if (leader) tc_commit(bar(C::B_DPR));
+    };
+    bool ok = mbar_wait_warp(bar(C::B_KV), 0, w) && mbar_wait_warp(bar(C::B_QF), 0, w);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0);
+      issue_dp(0);
+    }
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int s = it % C::NQS;
+      const uint32_t qb = stage(s), dob = stage(s) + C::OPND;
+      // dV += P^T dO, one query half per warpgroup as soon as it is written
+      // (M = keys, N = head dim, K = queries 64g .. 64g+63).
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        if (!mbar_wait_warp(bar(C::B_PR + g), it & 1, w)) { ok = false; break; }
         tc_fence_after();
-        // S^T = K Q^T and dP^T = V dO^T   (M = keys, N = queries, K = head dim)
 #pragma unroll
         for (int t = 0; t < C::NPROD; ++t)
 #pragma unroll
-          for (int k = 0; k < DHB / 16; ++k) {
-            const uint32_t off = (k / 4) * C::PANEL + (k % 4) * 32;
-            mma_ss<false>(tmem + C::TM_S, make_sdesc(kb + C::pa(t) * C::TILE + off, 16, 1024),
-                          make_sdesc(qb + C::pb(t) * C::TILE + off, 16, 1024), C::IDESC_T,
-                          (t > 0 || k > 0) ? 1u : 0u);
-          }
-#pragma unroll
-        for (int t = 0; t < C::NPROD; ++t)
-#pragma unroll
-          for (int k = 0; k < DHB / 16; ++k) {
-            const uint32_t off = (k / 4) * C::PANEL + (k % 4) * 32;
-            mma_ss<false>(tmem + C::TM_DP, make_sdesc(vb + C::pa(t) * C::TILE + off, 16, 1024),
-                          make_sdesc(dob + C::pb(t) * C::TILE + off, 16, 1024), C::IDESC_T,
-                          (t > 0 || k > 0) ? 1u : 0u);
-          }
-        tc_commit(bar(C::B_SDP));
-        // dV += P^T dO   (M = keys, N = head dim, K = queries)
-        if (!mbar_wait(bar(C::B_PR), it & 1, w)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int t = 0; t < C::NPROD; ++t)
-#pragma unroll
-          for (int k = 0; k < 128 / 16; ++k) {
+          for (int k = 4 * g; k < 4 * g + 4; ++k) {
             const uint32_t aoff = (k / 4) * C::PANEL + (k % 4) * 32;
-            mma_ss<false>(tmem + C::TM_DV, make_sdesc(pb + C::pa(t) * C::PT_HALF + aoff, 16, 1024),
-                          make_sdesc(dob + C::pb(t) * C::TILE + k * 16 * 128, C::PANEL, 1024), C::IDESC_KV,
-                          (it > 0 || t > 0 || k > 0) ? 1u : 0u);
+            const uint64_t ad = make_sdesc(pb + C::pa(t) * C::PT_HALF + aoff, 16, 1024);
+            const uint64_t bd = make_sdesc(dob + C::pb(t) * C::TILE + k * 16 * 128, C::PANEL, 1024);
+            if (leader)
+              mma_ss<false>(tmem + C::TM_DV, ad, bd, C::IDESC_KV, (it > 0 || g > 0 || t > 0 || k > 0) ? 1u : 0u);
           }
-        if constexpr (C::SHARE) tc_commit(bar(C::B_DVD));
-        // dK += dS^T Q   and   dQ_partial = dS K
-        if (!mbar_wait(bar(C::B_DSR), it & 1, w)) { ok = false; break; }
+        if constexpr (C::SHARE) {
+          if (leader) tc_commit(bar(C::B_DVD + g));
+        }
+      }
+      if (!ok) break;
+      const bool more = it + 1 < n_it;
+      if constexpr (C::PREFETCH) {
+        // Next iteration's S^T and dP^T while dK and dQ of this one are pending.
+        if (more) {
+          if (!mbar_wait_warp(bar(C::B_QF + (it + 1) % C::NQS), ((it + 1) / C::NQS) & 1, w) ||
+              !mbar_wait_warp(bar(C::B_SDPF), it & 1, w)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(it + 1);
+          issue_dp(it + 1);
+        }
+      }
+      // dK += dS^T Q, one query half at a time (M = keys, N = head dim).
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        if (!mbar_wait_warp(bar(C::B_DSR + g), it & 1, w)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < C::NPROD; ++t)
 #pragma unroll
-          for (int k = 0; k < 128 / 16; ++k) {
+          for (int k = 4 * g; k < 4 * g + 4; ++k) {
             const uint32_t aoff = (k / 4) * C::PANEL + (k % 4) * 32;
-            mma_ss<false>(tmem + C::TM_DK, make_sdesc(dsb + C::pa(t) * C::PT_HALF + aoff, 16, 1024),
-                          make_sdesc(qb + C::pb(t) * C::TILE + k * 16 * 128, C::PANEL, 1024), C::IDESC_KV,
-                          (it > 0 || t > 0 || k > 0) ? 1u : 0u);
+            const uint64_t ad = make_sdesc(dsb + C::pa(t) * C::PT_HALF + aoff, 16, 1024);
+            const uint64_t bd = make_sdesc(qb + C::pb(t) * C::TILE + k * 16 * 128, C::PANEL, 1024);
+            if (leader)
+              mma_ss<false>(tmem + C::TM_DK, ad, bd, C::IDESC_KV, (it > 0 || g > 0 || t > 0 || k > 0) ? 1u : 0u);
           }
+      }
+      if (!ok) break;
+      // dQ partial = dS K (M = queries, N = head dim, K = keys): the previous
+      // partial must have been drained, and (aliased columns) dP^T fully read.
+      if (it > 0 && !mbar_wait_warp(bar(C::B_ITF), (it - 1) & 1, w)) { ok = false; break; }
+      if constexpr (!C::PREFETCH) {
+        if (!mbar_wait_warp(bar(C::B_SDPF), it & 1, w)) { ok = false; break; }
+      }
+      tc_fence_after();
 #pragma unroll
-        for (int t = 0; t < C::NPROD; ++t)
+      for (int t = 0; t < C::NPROD; ++t)
 #pragma unroll
-          for (int k = 0; k < 128 / 16; ++k) {
-            mma_ss<false>(tmem + C::TM_DQ, make_sdesc(dsb + C::pa(t) * C::PT_HALF + k * 16 * 128, C::PANEL, 1024),
-                          make_sdesc(kb + C::pb(t) * C::TILE + k * 16 * 128, C::PANEL, 1024), C::IDESC_Q,
-                          (t > 0 || k > 0) ? 1u : 0u);
-          }
+        for (int k = 0; k < 128 / 16; ++k) {
+          const uint64_t ad = make_sdesc(dsb + C::pa(t) * C::PT_HALF + k * 16 * 128, C::PANEL, 1024);
+          const uint64_t bd = make_sdesc(kb + C::pb(t) * C::TILE + k * 16 * 128, C::PANEL, 1024);
+          if (leader) mma_ss<false>(tmem + C::TM_DQ, ad, bd, C::IDESC_Q, (t > 0 || k > 0) ? 1u : 0u);
+        }
+      if (leader) {
         tc_commit(bar(C::B_DQF));
         tc_commit(bar(C::B_QE + s));
       }
+      if constexpr (!C::PREFETCH) {
+        if (more) {
+          // With aliased dQ columns, dP^T(it+1) may only be written once dQ(it)
+          // has been drained.
+          if (!mbar_wait_warp(bar(C::B_QF + (it + 1) % C::NQS), ((it + 1) / C::NQS) & 1, w)) { ok = false; break; }
+          if (C::DQ_ALIAS && !mbar_wait_warp(bar(C::B_ITF), it & 1, w)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(it + 1);
+          issue_dp(it + 1);
+        }
+      }
+    }
+    if (leader) {
       tc_commit(bar(C::B_FIN));
       mbar_drain(bar(C::B_FIN), 0, a.timeout_ns);
     }
   } else {
-    // ---------------- compute warpgroup ----------------
+    // ---------------- compute warpgroups ----------------
+    // Warpgroup g owns query columns 64g .. 64g+63 of every S^T / dP^T tile
+    // and drains head columns [g W, g W + W) of dQ, dK and dV.
+    const int g = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int rl = quarter * 32 + lane;  // key row for P^T/dS^T, query row for dQ
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = a.scale_log2;
+    constexpr int W = DHB / 2;  // 32 or 64 head columns drained per warpgroup
     bool ok = true;
+    // dQ(it2) partial -> fp32 accumulator, rows of query tile i2 of head h2.
+    auto drain_dq = [&](int it2) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(C::B_DQF), it2 & 1, w))) return false;
+      tc_fence_after();
+      const int h2 = kvh * a.group + it2 / n_i;
+      const int i2 = j + it2 % n_i;
+      const int qrow = i2 * 128 + rl;
+      float* dst = a.dq_acc + ((static_cast<size_t>(b) * a.T + qrow) * a.Hq + h2) * a.Dh + g * W;
+      const int ncol = a.Dh - g * W;
+      uint32_t r[W];
+      if constexpr (W == 64) tmem_ld64(tl + C::TM_DQ + g * W, r);
+      else tmem_ld32(tl + C::TM_DQ + g * W, r);
+      tc_fence_before();
+      mbar_arrive(bar(C::B_ITF));
+      if (qrow < a.T && ncol > 0) {
+#pragma unroll
+        for (int u = 0; u < W / 4; ++u)
+          if (4 * u < ncol)
+            atomicAdd(reinterpret_cast<float4*>(dst) + u,
+                      make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                                  __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])));
+      }
+      return true;
+    };
     for (int it = 0; it < n_it; ++it) {
       const int s = it % C::NQS;
-      const int h = kvh * a.group + it / n_i;
       const int i = j + it % n_i;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SDP), it & 1, w) &&
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SR), it & 1, w) &&
                                        mbar_wait(bar(C::B_QF + s), (it / C::NQS) & 1, w));
       if (!ok) break;
       tc_fence_after();
-      const float* lse2s = reinterpret_cast<const float*>(smem + (stage(s) - sbase) + 2 * C::OPND);
-      const float* ds_ = lse2s + 128;
-      float p[128];
+      const float* lse2s = reinterpret_cast<const float*>(smem + (stage(s) - sbase) + 2 * C::OPND) + 64 * g;
+      const float* dvs = lse2s + 128;
+      float p[64];
+      {
+        uint32_t r[64];
+        tmem_ld64(tl + C::TM_S + 64 * g, r);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tl + C::TM_S + c * 32, r);
-#pragma unroll
-        for (int q = 0; q < 32; ++q) p[c * 32 + q] = __uint_as_float(r[q]);
+        for (int q = 0; q < 64; ++q) p[q] = __uint_as_float(r[q]);
       }
+      // P^T = 2^(S^T * scale * log2 e - LSE2); key rl is after query 64g + c on
+      // the diagonal tile: dropped.
       const bool diag = (i == j);
+      const int lim = rl - 64 * g;
 #pragma unroll
-      for (int c = 0; c < 128; c += 4) {
+      for (int c = 0; c < 64; c += 4) {
         const float4 l4 = *reinterpret_cast<const float4*>(lse2s + c);
         const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const float e = ex2(fmaf(p[c + u], sl2, -lv[u]));
-          p[c + u] = (diag && c + u < rl) ? 0.f : e;  // key rl is after query c: dropped
+          p[c + u] = (diag && c + u < lim) ? 0.f : e;
         }
       }
-      store_row_bf16<HL>(sbase + C::OFF_P, rl, p, C::PT_HALF);
+      store_half_row_bf16<HL>(sbase + C::OFF_P + g * C::PANEL, rl, p, C::PT_HALF);
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(C::B_PR));
+      mbar_arrive(bar(C::B_PR + g));
       // dS^T = P^T * (dP^T - D)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DPR), it & 1, w));
+      if (!ok) break;
+      tc_fence_after();
+      {
+        uint32_t r[64];
+        tmem_ld64(tl + C::TM_DP + 64 * g, r);
+        tc_fence_before();
+        mbar_arrive(bar(C::B_SDPF));
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tl + C::TM_DP + c * 32, r);
-#pragma unroll
-        for (int q = 0; q < 32; q += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(ds_ + c * 32 + q);
-          p[c * 32 + q + 0] *= __uint_as_float(r[q + 0]) - d4.x;
-          p[c * 32 + q + 1] *= __uint_as_float(r[q + 1]) - d4.y;
-          p[c * 32 + q + 2] *= __uint_as_float(r[q + 2]) - d4.z;
-          p[c * 32 + q + 3] *= __uint_as_float(r[q + 3]) - d4.w;
+        for (int q = 0; q < 64; q += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(dvs + q);
+          p[q + 0] *= __uint_as_float(r[q + 0]) - d4.x;
+          p[q + 1] *= __uint_as_float(r[q + 1]) - d4.y;
+          p[q + 2] *= __uint_as_float(r[q + 2]) - d4.z;
+          p[q + 3] *= __uint_as_float(r[q + 3]) - d4.w;
+        }
+      }
+      // Prefetch mode: the dS^T buffer is free once dK(it-1) and dQ(it-1) are
+      // done, which is also when dQ(it-1) can be drained. (Otherwise S^T(it)
+      // was issued after dQ(it-1), which was drained at the end of it-1.)
+      if constexpr (C::PREFETCH) {
+        if (it > 0) {
+          ok = drain_dq(it - 1);
+          if (!ok) break;
         }
       }
       if constexpr (C::SHARE) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DVD), it & 1, w));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DVD + g), it & 1, w));
         if (!ok) break;
       }
-      store_row_bf16<HL>(sbase + C::OFF_DS, rl, p, C::PT_HALF);
+      store_half_row_bf16<HL>(sbase + C::OFF_DS + g * C::PANEL, rl, p, C::PT_HALF);
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(C::B_DSR));
-      // dQ partial for query row rl of tile i -> fp32 accumulator
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DQF), it & 1, w));
-      if (!ok) break;
-      tc_fence_after();
-      const int qrow = i * 128 + rl;
-      float* dst = a.dq_acc + ((static_cast<size_t>(b) * a.T + qrow) * a.Hq + h) * a.Dh;
-#pragma unroll
-      for (int c = 0; c < DHB / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tl + C::TM_DQ + c * 32, r);
-        const int ncol = a.Dh - c * 32;
-        if (qrow < a.T && ncol > 0) {
-          const int nv = (ncol >= 32 ? 32 : ncol) / 4;
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (u < nv)
-              atomicAdd(reinterpret_cast<float4*>(dst + c * 32) + u,
-                        make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
-                                    __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])));
-        }
+      mbar_arrive(bar(C::B_DSR + g));
+      if constexpr (!C::PREFETCH) {
+        // dP^T(it+1) may reuse dQ's columns: drain dQ(it) before going on.
+        ok = drain_dq(it);
+        if (!ok) break;
       }
-      tc_fence_before();
-      mbar_arrive(bar(C::B_ITF));
     }
+    if (C::PREFETCH && ok) ok = drain_dq(n_it - 1);
     if (ok) {
       // The last dQ commit covered every MMA, including the final dK/dV updates.
-      tc_fence_after();
       const int key = j * 128 + rl;
       const bool valid = key < a.T;
-      const size_t row_off = ((static_cast<size_t>(b) * a.T + key) * a.Hkv + kvh) * a.Dh;
+      const size_t row_off = ((static_cast<size_t>(b) * a.T + key) * a.Hkv + kvh) * a.Dh + g * W;
+      const int ncol = a.Dh - g * W;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const uint32_t col0 = which == 0 ? C::TM_DV : C::TM_DK;
+        const uint32_t col0 = (which == 0 ? C::TM_DV : C::TM_DK) + g * W;
         const float mul = which == 0 ? 1.f : a.scale;
         void* base = which == 0 ? a.dv : a.dk;
+        uint32_t r[W];
+        if constexpr (W == 64) tmem_ld64(tl + col0, r);
+        else tmem_ld32(tl + col0, r);
+        if (!valid || ncol <= 0) continue;
+        if constexpr (HL) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(base) + row_off);
 #pragma unroll
-        for (int c = 0; c < DHB / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tl + col0 + c * 32, r);
-          const int ncol = a.Dh - c * 32;
-          if (!valid || ncol <= 0) continue;
-          if constexpr (HL) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(base) + row_off + c * 32);
-            const int nv = (ncol >= 32 ? 32 : ncol) / 4;
+          for (int u = 0; u < W / 4; ++u)
+            if (4 * u < ncol)
+              dst[u] = make_float4(__uint_as_float(r[4 * u]) * mul, __uint_as_float(r[4 * u + 1]) * mul,
+                                   __uint_as_float(r[4 * u + 2]) * mul, __uint_as_float(r[4 * u + 3]) * mul);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + row_off);
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-              if (u < nv)
-                dst[u] = make_float4(__uint_as_float(r[4 * u]) * mul, __uint_as_float(r[4 * u + 1]) * mul,
-                                     __uint_as_float(r[4 * u + 2]) * mul, __uint_as_float(r[4 * u + 3]) * mul);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + row_off + c * 32);
-            const int nv = (ncol >= 32 ? 32 : ncol) / 8;
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              if (u < nv)
-                dst[u] = make_uint4(
-                    pack_bf16(__uint_as_float(r[8 * u]) * mul, __uint_as_float(r[8 * u + 1]) * mul),
-                    pack_bf16(__uint_as_float(r[8 * u + 2]) * mul, __uint_as_float(r[8 * u + 3]) * mul),
-                    pack_bf16(__uint_as_float(r[8 * u + 4]) * mul, __uint_as_float(r[8 * u + 5]) * mul),
-                    pack_bf16(__uint_as_float(r[8 * u + 6]) * mul, __uint_as_float(r[8 * u + 7]) * mul));
-          }
+          for (int u = 0; u < W / 8; ++u)
+            if (8 * u < ncol)
+              dst[u] = make_uint4(
+                  pack_bf16(__uint_as_float(r[8 * u]) * mul, __uint_as_float(r[8 * u + 1]) * mul),
+                  pack_bf16(__uint_as_float(r[8 * u + 2]) * mul, __uint_as_float(r[8 * u + 3]) * mul),
+                  pack_bf16(__uint_as_float(r[8 * u + 4]) * mul, __uint_as_float(r[8 * u + 5]) * mul),
+                  pack_bf16(__uint_as_float(r[8 * u + 6]) * mul, __uint_as_float(r[8 * u + 7]) * mul));
         }
       }
     }

@@ -223,7 +223,7 @@ rca_status launch_fwd(const void* q, const void* k, const void* v, int64_t B, in
   a.n_qt = int((T + 127) / 128);
   a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(Dh)));
   const unsigned grid = unsigned(int64_t(a.n_qt) * B * Hq);
-  kern<<<grid, 192, C::SMEM_BYTES, st>>>(mq, mk, mv, a);
+  kern<<<grid, C::NTHREADS, C::SMEM_BYTES, st>>>(mq, mk, mv, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch attn_fwd_kernel");
   return RCA_OK;
@@ -305,7 +305,7 @@ rca_status launch_bwd_main(const void* q, const void* k, const void* v, const vo
   a.scale = float(1.0 / std::sqrt(double(Dh)));
   a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(Dh)));
   const unsigned grid = unsigned(int64_t(a.n_t) * B * Hkv);
-  kern<<<grid, 192, C::SMEM_BYTES, st>>>(maps, a);
+  kern<<<grid, C::NTHREADS, C::SMEM_BYTES, st>>>(maps, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch attn_bwd_main_kernel");
   return RCA_OK;
