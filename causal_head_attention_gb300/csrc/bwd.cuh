@@ -173,6 +173,10 @@ struct BwdCfg {
   // dQ products are pending; that needs a second Q/dO stage, separate P^T and
   // dS^T buffers and dQ columns of its own.
   static constexpr bool PREFETCH = (NQS >= 2) && !DQ_ALIAS && !SHARE;
+  // In prefetch mode each compute warpgroup adds its 32-column half of a dQ
+  // partial to the accumulator with one bulk tensor reduction, staged as fp32
+  // in its own panel of the (then unused) dS^T buffer.
+  static constexpr bool TMA_DQ = PREFETCH && DHB == 64;
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_T = make_idesc(false, 128, 128, false, false);   // S^T, dP^T
   static constexpr uint32_t IDESC_KV = make_idesc(false, 128, DHB, false, true);   // dV, dK
@@ -198,9 +202,10 @@ struct BwdCfg {
   __device__ static constexpr int pb(int t) { return t == 1 ? 1 : 0; }
 };
 
-// bf16 tensor maps of every operand: [0] = bf16 storage or hi part, [1] = lo part.
+// bf16 tensor maps of every operand: [0] = bf16 storage or hi part, [1] = lo part;
+// dq: the fp32 dQ accumulator [B,T,Hq,Dh], 128 rows x 32 columns per box.
 struct BwdMaps {
-  CUtensorMap q[2], k[2], v[2], dO[2];
+  CUtensorMap q[2], k[2], v[2], dO[2], dq;
 };
 
 struct BwdArgs {
@@ -471,27 +476,44 @@ __global__ void __launch_bounds__(320, 1)
     const float sl2 = a.scale_log2;
     constexpr int W = DHB / 2;  // 32 or 64 head columns drained per warpgroup
     bool ok = true;
+    const int t = threadIdx.x - 64 - 128 * g;  // 0..127 within the warpgroup
     // dQ(it2) partial -> fp32 accumulator, rows of query tile i2 of head h2.
     auto drain_dq = [&](int it2) -> bool {
       if (!__all_sync(0xffffffffu, mbar_wait(bar(C::B_DQF), it2 & 1, w))) return false;
       tc_fence_after();
       const int h2 = kvh * a.group + it2 / n_i;
       const int i2 = j + it2 % n_i;
-      const int qrow = i2 * 128 + rl;
-      float* dst = a.dq_acc + ((static_cast<size_t>(b) * a.T + qrow) * a.Hq + h2) * a.Dh + g * W;
-      const int ncol = a.Dh - g * W;
       uint32_t r[W];
       if constexpr (W == 64) tmem_ld64(tl + C::TM_DQ + g * W, r);
       else tmem_ld32(tl + C::TM_DQ + g * W, r);
       tc_fence_before();
       mbar_arrive(bar(C::B_ITF));
-      if (qrow < a.T && ncol > 0) {
+      if constexpr (C::TMA_DQ) {
+        // Stage the fp32 [128 x 32] half in 128-byte-swizzled rows, then one
+        // thread adds the whole box to global memory.
+        const uint32_t panel = sbase + C::OFF_DS + g * C::PANEL;
 #pragma unroll
-        for (int u = 0; u < W / 4; ++u)
-          if (4 * u < ncol)
-            atomicAdd(reinterpret_cast<float4*>(dst) + u,
-                      make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
-                                  __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])));
+        for (int c = 0; c < 8; ++c)
+          st_shared_v4(panel + rl * 128 + ((c ^ (rl & 7)) << 4), r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+        fence_async_smem();
+        named_bar(2 + g, 128);
+        if (t == 0 && g * W < a.Dh) {  // a half past the head width has nothing to add
+          tma_reduce_add_4d(&maps.dq, panel, g * W, h2, i2 * 128, b);
+          bulk_commit();
+          bulk_wait_read0();
+        }
+        named_bar(2 + g, 128);
+      } else {
+        const int qrow = i2 * 128 + rl;
+        float* dst = a.dq_acc + ((static_cast<size_t>(b) * a.T + qrow) * a.Hq + h2) * a.Dh + g * W;
+        const int ncol = a.Dh - g * W;
+        if (qrow < a.T && ncol > 0) {
+#pragma unroll
+          for (int u = 0; u < W / 4; ++u)
+            if (4 * u < ncol)
+              red_add_v4(dst + 4 * u, __uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                         __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+        }
       }
       return true;
     };
@@ -571,6 +593,9 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
     if (C::PREFETCH && ok) ok = drain_dq(n_it - 1);
+    if constexpr (C::TMA_DQ) {
+      if (t == 0) bulk_wait0();  // every bulk reduction of this CTA has landed
+    }
     if (ok) {
       // The last dQ commit covered every MMA, including the final dK/dV updates.
       const int key = j * 128 + rl;

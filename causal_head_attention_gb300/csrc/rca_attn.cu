@@ -285,6 +285,7 @@ rca_status launch_bwd_main(const void* q, const void* k, const void* v, const vo
     maps.v[1] = maps.v[0];
     maps.dO[1] = maps.dO[0];
   }
+  RCA_CHECK(make_map(&maps.dq, w + L.dq_off, B, T, Hq, Dh, true, "dq accumulator"));
   int* status = status_override;
   if (!status) RCA_CHECK(status_word(&status));
   auto kern = rca::attn_bwd_main_kernel<HL, DHB>;
