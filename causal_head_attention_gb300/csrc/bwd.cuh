@@ -147,7 +147,11 @@ struct BwdCfg {
   static constexpr int SMEM_LIMIT = 232448;
   static constexpr int BAR_BYTES = 1024;
   static constexpr int STAGE_BYTES = 2 * OPND + 1024;   // Q, dO, LSE2[128], D[128]
-  static constexpr int AVAIL = SMEM_LIMIT - 1024 - BAR_BYTES - 2 * OPND;
+  // bf16 storage with a 64-column head: dQ halves are staged as fp32 for bulk
+  // tensor reductions in a buffer of their own (two 16 KB panels).
+  static constexpr bool TMA_DQ = !HL && DHB == 64;
+  static constexpr int DQS_BYTES = TMA_DQ ? 2 * PANEL : 0;
+  static constexpr int AVAIL = SMEM_LIMIT - 1024 - BAR_BYTES - 2 * OPND - DQS_BYTES;
   static constexpr int NQS_SEP = (AVAIL - 2 * P_BYTES) / STAGE_BYTES;
   static constexpr int NQS_SHR = (AVAIL - P_BYTES) / STAGE_BYTES;
   // P^T and dS^T share one buffer only when separate buffers leave < 2 stages.
@@ -159,7 +163,8 @@ struct BwdCfg {
   static constexpr int OFF_V = OPND;
   static constexpr int OFF_P = 2 * OPND;
   static constexpr int OFF_DS = SHARE ? OFF_P : OFF_P + P_BYTES;
-  static constexpr int OFF_STAGE = OFF_DS + P_BYTES;
+  static constexpr int OFF_DQS = OFF_DS + P_BYTES;
+  static constexpr int OFF_STAGE = OFF_DQS + DQS_BYTES;
   static constexpr int OFF_BAR = OFF_STAGE + NQS * STAGE_BYTES;
   static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
@@ -173,10 +178,7 @@ struct BwdCfg {
   // dQ products are pending; that needs a second Q/dO stage, separate P^T and
   // dS^T buffers and dQ columns of its own.
   static constexpr bool PREFETCH = (NQS >= 2) && !DQ_ALIAS && !SHARE;
-  // In prefetch mode each compute warpgroup adds its 32-column half of a dQ
-  // partial to the accumulator with one bulk tensor reduction, staged as fp32
-  // in its own panel of the (then unused) dS^T buffer.
-  static constexpr bool TMA_DQ = PREFETCH && DHB == 64;
+  static_assert(!TMA_DQ || PREFETCH, "bulk dQ reduction assumes the prefetch schedule");
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_T = make_idesc(false, 128, 128, false, false);   // S^T, dP^T
   static constexpr uint32_t IDESC_KV = make_idesc(false, 128, DHB, false, true);   // dV, dK
@@ -489,9 +491,13 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       mbar_arrive(bar(C::B_ITF));
       if constexpr (C::TMA_DQ) {
-        // Stage the fp32 [128 x 32] half in 128-byte-swizzled rows, then one
-        // thread adds the whole box to global memory.
-        const uint32_t panel = sbase + C::OFF_DS + g * C::PANEL;
+        // Stage the fp32 [128 x 32] half in 128-byte-swizzled rows of this
+        // warpgroup's staging panel, then one thread adds the whole box to
+        // global memory. The panel is rewritten only after the previous
+        // reduction (one iteration earlier) has finished reading it.
+        const uint32_t panel = sbase + C::OFF_DQS + g * C::PANEL;
+        if (t == 0) bulk_wait_read0();
+        named_bar(2 + g, 128);
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           st_shared_v4(panel + rl * 128 + ((c ^ (rl & 7)) << 4), r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
@@ -500,9 +506,7 @@ __global__ void __launch_bounds__(320, 1)
         if (t == 0 && g * W < a.Dh) {  // a half past the head width has nothing to add
           tma_reduce_add_4d(&maps.dq, panel, g * W, h2, i2 * 128, b);
           bulk_commit();
-          bulk_wait_read0();
         }
-        named_bar(2 + g, 128);
       } else {
         const int qrow = i2 * 128 + rl;
         float* dst = a.dq_acc + ((static_cast<size_t>(b) * a.T + qrow) * a.Hq + h2) * a.Dh + g * W;
