@@ -19,6 +19,7 @@ from ._native import (  # noqa: F401  (C-ABI names)
     rca_attn_bwd_workspace_size,
     rca_attn_fwd,
     rca_last_error,
+    rca_selftest_device_timeout,
     rca_set_wait_timeout_ns,
     rca_stream_status,
 )
@@ -40,6 +41,7 @@ __all__ = [
     "rca_stream_status",
     "rca_last_error",
     "rca_set_wait_timeout_ns",
+    "rca_selftest_device_timeout",
 ]
 
 

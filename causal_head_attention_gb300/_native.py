@@ -47,6 +47,7 @@ _SIG = {
                                                ctypes.c_size_t, _P]),
     "rca_attn_bwd_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                             ctypes.c_int, _P]),
+    "rca_selftest_device_timeout": (ctypes.c_int, [_P]),
     "rca_stream_status": (ctypes.c_int, [_P]),
     "rca_set_wait_timeout_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
 }
@@ -188,6 +189,10 @@ def rca_attn_bwd_noalloc(q, k, v, out, lse, dout, dq, dk, dv, stream=None):
     B, Hq, Hkv, T, Dh = _shape(q, k)
     _check(lib().rca_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
                                       _ptr(dk), _ptr(dv), B, Hq, Hkv, T, Dh, _dtype_code(q), _stream(stream)))
+
+
+def rca_selftest_device_timeout(stream=None):
+    _check(lib().rca_selftest_device_timeout(_stream(stream)))
 
 
 def rca_stream_status(stream=None):

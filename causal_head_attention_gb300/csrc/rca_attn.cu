@@ -14,6 +14,25 @@
 #include "bwd.cuh"
 #include "fwd.cuh"
 
+namespace rca {
+// Failure-detection self-test: one warp waits, with the same time-bounded wait
+// the attention kernels use, on an mbarrier that nothing ever arrives on. The
+// wait gives up after the configured limit, records the timeout status and the
+// kernel returns; the CUDA context stays usable.
+__global__ void __launch_bounds__(32) selftest_wait_kernel(int* status, unsigned long long timeout_ns) {
+  __shared__ __align__(8) unsigned long long bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    mbar_init_fence();
+  }
+  __syncwarp();
+  const WaitCtl w{status, &abort_flag, timeout_ns};
+  mbar_wait_warp(smem_u32(&bar), 0, w);
+}
+}  // namespace rca
+
 namespace {
 
 thread_local std::string g_err;
@@ -259,7 +278,7 @@ rca_status launch_bwd_main(const void* q, const void* k, const void* v, const vo
     void* dh = hl + 2 * L.q_part;
     void* dl = hl + 3 * L.q_part;
     void* kh = hl + 4 * L.q_part;
-    void* kl = kh + L.kv_part;
+    void* kl = static_cast<uint8_t*>(kh) + L.kv_part;
     void* vh = static_cast<uint8_t*>(kh) + 2 * L.kv_part;
     void* vl = static_cast<uint8_t*>(kh) + 3 * L.kv_part;
     const size_t nq = size_t(B) * T * Hq * Dh, nkv = size_t(B) * T * Hkv * Dh;
@@ -471,6 +490,18 @@ rca_status rca_attn_bwd(const void* q, const void* k, const void* v, const void*
   RCA_CHECK(do_preprocess(out, lse, dout, B, Hq, T, Dh, dt, workspace, L, st));
   RCA_CHECK(do_bwd_main(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, dt, workspace, L, st));
   return do_convert(dq, B, Hq, T, Dh, dt, workspace, L, st);
+  RCA_GUARD_END
+}
+
+rca_status rca_selftest_device_timeout(void* cuda_stream) {
+  RCA_GUARD_BEGIN
+  g_err.clear();
+  int* status = nullptr;
+  RCA_CHECK(status_word(&status));
+  rca::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(cuda_stream)>>>(status, g_timeout_ns.load());
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch selftest_wait_kernel");
+  return RCA_OK;
   RCA_GUARD_END
 }
 

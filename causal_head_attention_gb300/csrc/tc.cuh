@@ -288,6 +288,7 @@ __device__ __forceinline__ void tmem_ld64x2(uint32_t ta, uint32_t tb, uint32_t (
       : "memory");
 }
 
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "

@@ -174,6 +174,16 @@ rca_status rca_attn_bwd_noalloc(const void* q, const void* k, const void* v, con
 rca_status rca_stream_status(void* cuda_stream);
 
 /*
+ * Failure-detection self-test (no counterpart on the pages). Enqueues a small
+ * kernel that waits, with the same time-bounded wait the attention kernels
+ * use, on a barrier that nothing ever completes. After the current wait limit
+ * (rca_set_wait_timeout_ns) the kernel gives up and records a timeout, so the
+ * next rca_stream_status() on this stream returns RCA_ERR_DEVICE_TIMEOUT (and
+ * clears it); the CUDA context remains usable. Nothing faults or hangs.
+ */
+rca_status rca_selftest_device_timeout(void* cuda_stream);
+
+/*
  * Sets the device-side wait limit in nanoseconds for subsequent launches from
  * any thread (default 2e9 = 2 s; values < 1e6 are raised to 1e6). Returns the
  * previous value.
