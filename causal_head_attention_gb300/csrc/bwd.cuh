@@ -432,6 +432,8 @@ __global__ void __launch_bounds__(320, 1)
           }
       }
       if (!ok) break;
+      // The Q/dO stage is no longer read (dQ reads dS^T and K): release it now.
+      if (leader) tc_commit(bar(C::B_QE + s));
       // dQ partial = dS K (M = queries, N = head dim, K = keys): the previous
       // partial must have been drained, and (aliased columns) dP^T fully read.
       if (it > 0 && !mbar_wait_warp(bar(C::B_ITF), (it - 1) & 1, w)) { ok = false; break; }
@@ -447,10 +449,7 @@ __global__ void __launch_bounds__(320, 1)
           const uint64_t bd = make_sdesc(kb + C::pb(t) * C::TILE + k * 16 * 128, C::PANEL, 1024);
           if (leader) mma_ss<false>(tmem + C::TM_DQ, ad, bd, C::IDESC_Q, (t > 0 || k > 0) ? 1u : 0u);
         }
-      if (leader) {
-        tc_commit(bar(C::B_DQF));
-        tc_commit(bar(C::B_QE + s));
-      }
+      if (leader) tc_commit(bar(C::B_DQF));
       if constexpr (!C::PREFETCH) {
         if (more) {
           // With aliased dQ columns, dP^T(it+1) may only be written once dQ(it)
@@ -527,11 +526,23 @@ __global__ void __launch_bounds__(320, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SR), it & 1, w) &&
                                        mbar_wait(bar(C::B_QF + s), (it / C::NQS) & 1, w));
       if (!ok) break;
-      tc_fence_after();
       const float* lse2s = reinterpret_cast<const float*>(smem + (stage(s) - sbase) + 2 * C::OPND) + 64 * g;
       const float* dvs = lse2s + 128;
       float p[64];
-      {
+      uint32_t dpr[64];  // prefetch schedule: dP^T half, loaded together with S^T
+      if constexpr (C::PREFETCH) {
+        // S^T(it) and dP^T(it) are issued together: one TMEM round trip for both.
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DPR), it & 1, w));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t r[64];
+        tmem_ld64x2(tl + C::TM_S + 64 * g, tl + C::TM_DP + 64 * g, r, dpr);
+        tc_fence_before();
+        mbar_arrive(bar(C::B_SDPF));
+#pragma unroll
+        for (int q = 0; q < 64; ++q) p[q] = __uint_as_float(r[q]);
+      } else {
+        tc_fence_after();
         uint32_t r[64];
         tmem_ld64(tl + C::TM_S + 64 * g, r);
 #pragma unroll
@@ -556,29 +567,26 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       mbar_arrive(bar(C::B_PR + g));
       // dS^T = P^T * (dP^T - D)
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DPR), it & 1, w));
-      if (!ok) break;
-      tc_fence_after();
-      {
-        uint32_t r[64];
-        tmem_ld64(tl + C::TM_DP + 64 * g, r);
+      if constexpr (!C::PREFETCH) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DPR), it & 1, w));
+        if (!ok) break;
+        tc_fence_after();
+        tmem_ld64(tl + C::TM_DP + 64 * g, dpr);
         tc_fence_before();
         mbar_arrive(bar(C::B_SDPF));
-#pragma unroll
-        for (int q = 0; q < 64; q += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(dvs + q);
-          p[q + 0] *= __uint_as_float(r[q + 0]) - d4.x;
-          p[q + 1] *= __uint_as_float(r[q + 1]) - d4.y;
-          p[q + 2] *= __uint_as_float(r[q + 2]) - d4.z;
-          p[q + 3] *= __uint_as_float(r[q + 3]) - d4.w;
-        }
       }
-      // Prefetch mode: the dS^T buffer is free once dK(it-1) and dQ(it-1) are
-      // done, which is also when dQ(it-1) can be drained. (Otherwise S^T(it)
-      // was issued after dQ(it-1), which was drained at the end of it-1.)
+#pragma unroll
+      for (int q = 0; q < 64; q += 4) {
+        const float4 d4 = *reinterpret_cast<const float4*>(dvs + q);
+        p[q + 0] *= __uint_as_float(dpr[q + 0]) - d4.x;
+        p[q + 1] *= __uint_as_float(dpr[q + 1]) - d4.y;
+        p[q + 2] *= __uint_as_float(dpr[q + 2]) - d4.z;
+        p[q + 3] *= __uint_as_float(dpr[q + 3]) - d4.w;
+      }
       if constexpr (C::PREFETCH) {
+        // The dS^T buffer is free once dK(it-1) and dQ(it-1) are done.
         if (it > 0) {
-          ok = drain_dq(it - 1);
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DQF), (it - 1) & 1, w));
           if (!ok) break;
         }
       }
@@ -590,8 +598,14 @@ __global__ void __launch_bounds__(320, 1)
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::B_DSR + g));
-      if constexpr (!C::PREFETCH) {
-        // dP^T(it+1) may reuse dQ's columns: drain dQ(it) before going on.
+      // dQ of the previous iteration (prefetch schedule), or of this one (dP^T
+      // of the next iteration may reuse dQ's columns), goes to the accumulator.
+      if constexpr (C::PREFETCH) {
+        if (it > 0) {
+          ok = drain_dq(it - 1);
+          if (!ok) break;
+        }
+      } else {
         ok = drain_dq(it);
         if (!ok) break;
       }
