@@ -334,6 +334,11 @@ __global__ void __launch_bounds__(320, 1)
     const uint64_t sl2x2 = f2pack(a.scale_log2, a.scale_log2);
     float m = -INFINITY, l = 0.f;
     bool ok = true;
+    // Warpgroup 1 starts about half a tile after warpgroup 0 (it waits until
+    // warpgroup 0 has its first scores in registers), so that from then on one
+    // warpgroup's exponentials overlap the other's TMEM load and barrier waits
+    // instead of both contending for the same units at the same time.
+    if (g == 1) named_bar(3, 256);
     for (int j = 0; j < nkv; ++j) {
       const int sb = j & 1;
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SF + sb), (j >> 1) & 1, w));
@@ -348,6 +353,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_before();
       mbar_arrive(bar(C::B_SFREE + sb));
+      if (g == 0 && j == 0) named_bar_arrive(3, 256);
       if (j == nkv - 1) {  // diagonal tile: drop keys after this row's query
         const int lim = q_idx - j * C::BN - 64 * g;
 #pragma unroll
