@@ -125,6 +125,25 @@ rca_status status_word(int** out) {
   return RCA_OK;
 }
 
+// Streaming-multiprocessor count of the current device (cached per device).
+int g_sms[256] = {};
+rca_status sm_count(int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 256) return fail(RCA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_status_mu);
+  if (g_sms[dev] <= 0) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(multiProcessorCount)");
+    if (n <= 0) return fail(RCA_ERR_CUDA, "device reports %d multiprocessors", n);
+    g_sms[dev] = n;
+  }
+  *out = g_sms[dev];
+  return RCA_OK;
+}
+
 template <typename K>
 cudaError_t ensure_smem(K kernel, int bytes, std::atomic<unsigned long long>& mask) {
   int dev = 0;
@@ -240,9 +259,18 @@ rca_status launch_fwd(const void* q, const void* k, const void* v, int64_t B, in
   a.B = int(B); a.Hq = int(Hq); a.Hkv = int(Hkv); a.T = int(T); a.Dh = int(Dh);
   a.group = int(Hq / Hkv);
   a.n_qt = int((T + 127) / 128);
+  a.n_items = int(int64_t(a.n_qt) * B * Hq);
   a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(Dh)));
-  const unsigned grid = unsigned(int64_t(a.n_qt) * B * Hq);
-  kern<<<grid, C::NTHREADS, C::SMEM_BYTES, st>>>(mq, mk, mv, a);
+  // Persistent launch (one CTA per SM walking several work items) where the
+  // kernel overlaps one item's epilogue with the next item's first products;
+  // otherwise one CTA per work item.
+  int grid = a.n_items;
+  if (C::PT) {
+    int sms = 0;
+    RCA_CHECK(sm_count(&sms));
+    if (grid > sms) grid = sms;
+  }
+  kern<<<unsigned(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(mq, mk, mv, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch attn_fwd_kernel");
   return RCA_OK;
