@@ -13,10 +13,15 @@
 // Three kernels:
 //   attn_bwd_preprocess_kernel  D, LSE in base 2 (padded rows: D = 0, LSE = +inf),
 //                               zeroes the fp32 dQ accumulator. HBM-bound.
-//   attn_bwd_main_kernel        one CTA per (batch, KV head, 128-key tile j); loops
+//   attn_bwd_main_kernel        work item = (batch, KV head, 128-key tile j); loops
 //                               over every query head of the group and every query
 //                               tile i >= j; dK, dV accumulate in TMEM; dQ partials
-//                               are added into the fp32 accumulator.
+//                               are added into the fp32 accumulator. bf16 storage
+//                               with a 64-column head: P^T stays in TMEM (dV reads
+//                               it from there) and the CTAs are persistent, one per
+//                               SM walking several items, with the next item's K/V
+//                               and first S^T / dP^T fetched during the current
+//                               item's last iteration; otherwise one CTA per item.
 //   attn_bwd_dq_convert_kernel  dQ = scale * accumulator in the storage dtype.
 //   split_hilo_kernel           fp32 storage only: bf16 hi/lo copies of Q, K, V, dO
 //                               for the main kernel (see BwdCfg).
@@ -144,6 +149,14 @@ struct BwdCfg {
   static constexpr int OPND = NPART * TILE;             // all parts of it
   static constexpr int PT_HALF = 2 * PANEL;             // 128 x 128 bf16
   static constexpr int P_BYTES = NPART * PT_HALF;
+  // bf16 storage with a 64-column head: P^T stays in TMEM (dV = P^T dO reads
+  // its A operand from there), which frees the shared-memory P^T buffer for a
+  // second K/V buffer, and CTAs are persistent: the next work item's K/V tiles
+  // and first S^T / dP^T are fetched and computed during the current item's
+  // last iteration.
+  static constexpr bool PTB = !HL && DHB == 64;
+  static constexpr int KVB = PTB ? 2 : 1;               // K/V buffers
+  static constexpr int P_SMEM = PTB ? 0 : P_BYTES;      // shared-memory P^T buffer
   static constexpr int SMEM_LIMIT = 232448;
   static constexpr int BAR_BYTES = 1024;
   static constexpr int STAGE_BYTES = 2 * OPND + 1024;   // Q, dO, LSE2[128], D[128]
@@ -151,18 +164,18 @@ struct BwdCfg {
   // tensor reductions in a buffer of their own (two 16 KB panels).
   static constexpr bool TMA_DQ = !HL && DHB == 64;
   static constexpr int DQS_BYTES = TMA_DQ ? 2 * PANEL : 0;
-  static constexpr int AVAIL = SMEM_LIMIT - 1024 - BAR_BYTES - 2 * OPND - DQS_BYTES;
-  static constexpr int NQS_SEP = (AVAIL - 2 * P_BYTES) / STAGE_BYTES;
+  static constexpr int AVAIL = SMEM_LIMIT - 1024 - BAR_BYTES - KVB * 2 * OPND - DQS_BYTES;
+  static constexpr int NQS_SEP = (AVAIL - P_SMEM - P_BYTES) / STAGE_BYTES;
   static constexpr int NQS_SHR = (AVAIL - P_BYTES) / STAGE_BYTES;
   // P^T and dS^T share one buffer only when separate buffers leave < 2 stages.
-  static constexpr bool SHARE = NQS_SEP < 2 && NQS_SHR > NQS_SEP;
+  static constexpr bool SHARE = !PTB && NQS_SEP < 2 && NQS_SHR > NQS_SEP;
   static constexpr int NQS_RAW = SHARE ? NQS_SHR : NQS_SEP;
   static constexpr int NQS = NQS_RAW > 4 ? 4 : NQS_RAW;
   static_assert(NQS >= 1, "backward needs at least one Q/dO stage");
-  static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = OPND;
-  static constexpr int OFF_P = 2 * OPND;
-  static constexpr int OFF_DS = SHARE ? OFF_P : OFF_P + P_BYTES;
+  static constexpr int OFF_K = 0;                       // K of buffer x at OFF_K + x * 2 * OPND
+  static constexpr int OFF_V = OPND;                    // V of buffer x at OFF_V + x * 2 * OPND
+  static constexpr int OFF_P = KVB * 2 * OPND;
+  static constexpr int OFF_DS = SHARE ? OFF_P : OFF_P + P_SMEM;
   static constexpr int OFF_DQS = OFF_DS + P_BYTES;
   static constexpr int OFF_STAGE = OFF_DQS + DQS_BYTES;
   static constexpr int OFF_BAR = OFF_STAGE + NQS * STAGE_BYTES;
@@ -174,29 +187,34 @@ struct BwdCfg {
   // once both compute warpgroups have read dP^T.
   static constexpr bool DQ_ALIAS = 256 + 3 * DHB > 512;
   static constexpr int TM_DQ = DQ_ALIAS ? TM_DP : 256 + 2 * DHB;
+  static constexpr int TM_P = 256 + 3 * DHB;            // PTB: P^T, query pair (2c, 2c+1) in column c
+  static_assert(!PTB || TM_P + 64 <= 512, "TMEM budget for P^T");
   // S^T / dP^T of the next iteration are computed while this iteration's dK and
   // dQ products are pending; that needs a second Q/dO stage, separate P^T and
   // dS^T buffers and dQ columns of its own.
   static constexpr bool PREFETCH = (NQS >= 2) && !DQ_ALIAS && !SHARE;
   static_assert(!TMA_DQ || PREFETCH, "bulk dQ reduction assumes the prefetch schedule");
+  static_assert(!PTB || PREFETCH, "persistent CTAs assume the prefetch schedule");
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_T = make_idesc(false, 128, 128, false, false);   // S^T, dP^T
   static constexpr uint32_t IDESC_KV = make_idesc(false, 128, DHB, false, true);   // dV, dK
   static constexpr uint32_t IDESC_Q = make_idesc(false, 128, DHB, true, true);     // dQ
   static constexpr int NTHREADS = 320;
   // barriers
-  static constexpr int B_KV = 0;
-  static constexpr int B_QF = 1;
+  static constexpr int B_KVF = 0;            // [KVB] K/V tiles of a work item landed
+  static constexpr int B_KVE = B_KVF + KVB;  // [KVB] K/V buffer free (last dQ of its item done)
+  static constexpr int B_QF = B_KVE + KVB;
   static constexpr int B_QE = B_QF + NQS;
   static constexpr int B_SR = B_QE + NQS;   // S^T(it) in TMEM
   static constexpr int B_DPR = B_SR + 1;    // dP^T(it) in TMEM
   static constexpr int B_PR = B_DPR + 1;    // [2] P^T half g written
   static constexpr int B_SDPF = B_PR + 2;   // S^T, dP^T of it read by both warpgroups
-  static constexpr int B_DVD = B_SDPF + 1;  // [2] dV half g done (shared P/dS buffer only)
+  static constexpr int B_DVD = B_SDPF + 1;  // [2] dV half g done (P^T in TMEM / shared P, dS buffer)
   static constexpr int B_DSR = B_DVD + 2;   // [2] dS^T half g written
   static constexpr int B_DQF = B_DSR + 2;   // dQ(it) in TMEM (all MMAs of it done)
   static constexpr int B_ITF = B_DQF + 1;   // dQ(it) drained by both warpgroups
-  static constexpr int B_FIN = B_ITF + 1;
+  static constexpr int B_KVFREE = B_ITF + 1;  // dK, dV of a work item read by the epilogue (256)
+  static constexpr int B_FIN = B_KVFREE + 1;
   static constexpr int NBAR = B_FIN + 1;
   // parts multiplied for one product: (hi,hi) [, (hi,lo), (lo,hi)]
   static constexpr int NPROD = HL ? 3 : 1;
@@ -219,8 +237,31 @@ struct BwdArgs {
   int* status;
   unsigned long long timeout_ns;
   int B, Hq, Hkv, T, Dh, group, n_t, Tpad;
+  int n_items;  // B * Hkv * n_t work items (one key tile of one KV head each)
   float scale, scale_log2;
 };
+
+// Work item k (k = 0, 1, ...) of this CTA: items are ordered by decreasing
+// work (key tile j = 0 of every KV head first: it meets every query tile) and
+// dealt out in a snake over the grid (round k gives item k G + c for even k,
+// k G + G - 1 - c for odd k). Item (b, kvh, j) runs n_it = group * (n_t - j)
+// iterations: every query head of the group times query tiles j .. n_t - 1.
+struct BwdItem {
+  int b, kvh, j, n_i, n_it;
+};
+__device__ __forceinline__ bool bwd_item(const BwdArgs& a, int k, BwdItem& it) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  const long long idx = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
+  if (idx >= a.n_items) return false;
+  const int bk_count = a.B * a.Hkv;
+  it.j = static_cast<int>(idx / bk_count);
+  const int bk = static_cast<int>(idx % bk_count);
+  it.b = bk / a.Hkv;
+  it.kvh = bk % a.Hkv;
+  it.n_i = a.n_t - it.j;
+  it.n_it = a.group * it.n_i;
+  return true;
+}
 
 // Thread row `rl` of one 64-column panel of a 128 x 128 bf16 (hi[/lo])
 // operand tile, K-major with the 128-byte swizzle: 8 chunks of 8 values.
@@ -256,16 +297,12 @@ __global__ void __launch_bounds__(320, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 8 * C::NBAR + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bk_count = a.B * a.Hkv;
-  const int lin = blockIdx.x;
-  const int j = lin / bk_count;  // key tile; small j = most work, scheduled first
-  const int bk = lin % bk_count;
-  const int b = bk / a.Hkv, kvh = bk % a.Hkv;
-  const int n_i = a.n_t - j;           // query tiles j .. n_t-1
-  const int n_it = a.group * n_i;      // times every query head of the group
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(C::B_KV), 1);
+    for (int x = 0; x < C::KVB; ++x) {
+      mbar_init(bar(C::B_KVF + x), 1);
+      mbar_init(bar(C::B_KVE + x), 1);
+    }
     for (int s = 0; s < C::NQS; ++s) {
       mbar_init(bar(C::B_QF + s), 1);
       mbar_init(bar(C::B_QE + s), 1);
@@ -280,6 +317,7 @@ __global__ void __launch_bounds__(320, 1)
     }
     mbar_init(bar(C::B_DQF), 1);
     mbar_init(bar(C::B_ITF), 256);
+    mbar_init(bar(C::B_KVFREE), 256);
     mbar_init(bar(C::B_FIN), 1);
     *abort_flag = 0;
     mbar_init_fence();
@@ -294,178 +332,243 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl w{a.status, abort_flag, a.timeout_ns};
 
+  // Every role walks the same sequence of work items; iterations are numbered
+  // gi = 0, 1, ... across all of this CTA's items, and the Q/dO ring position
+  // and every per-iteration barrier phase is a function of gi.
   if (warp == 0) {
-    // ---------------- TMA producer (whole warp; one elected lane issues) ----------------
-    const bool leader = elect_one();
-    if (leader) {
+    // ---------------- TMA producer (one elected thread) ----------------
+    if (elect_one()) {
       for (int part = 0; part < C::NPART; ++part) {
         tma_prefetch_desc(&maps.q[part]);
         tma_prefetch_desc(&maps.k[part]);
         tma_prefetch_desc(&maps.v[part]);
         tma_prefetch_desc(&maps.dO[part]);
       }
-      mbar_expect_tx(bar(C::B_KV), 2 * C::OPND);
-      for (int part = 0; part < C::NPART; ++part)
-        for (int p = 0; p < C::DPANELS; ++p) {
-          tma_load_4d(sbase + C::OFF_K + part * C::TILE + p * C::PANEL, &maps.k[part], bar(C::B_KV), p * 64,
-                      kvh, j * 128, b);
-          tma_load_4d(sbase + C::OFF_V + part * C::TILE + p * C::PANEL, &maps.v[part], bar(C::B_KV), p * 64,
-                      kvh, j * 128, b);
-        }
-    }
-    int it = 0;
-    for (; it < n_it; ++it) {
-      const int s = it % C::NQS;
-      if (it >= C::NQS && !mbar_wait_warp(bar(C::B_QE + s), ((it / C::NQS) - 1) & 1, w)) break;
-      const int h = kvh * a.group + it / n_i;
-      const int i = j + it % n_i;
-      const uint32_t st = stage(s);
-      if (leader) {
-        mbar_expect_tx(bar(C::B_QF + s), 2 * C::OPND + 1024);
+      bool ok = true;
+      int gi = 0, n = 0;
+      BwdItem itm{};
+      for (; ok && bwd_item(a, n, itm); ++n) {
+        // K_j, V_j of the item into K/V buffer n % KVB.
+        const int x = n % C::KVB;
+        if (n >= C::KVB && !mbar_wait(bar(C::B_KVE + x), ((n / C::KVB) - 1) & 1, w)) break;
+        mbar_expect_tx(bar(C::B_KVF + x), 2 * C::OPND);
         for (int part = 0; part < C::NPART; ++part)
           for (int p = 0; p < C::DPANELS; ++p) {
-            tma_load_4d(st + part * C::TILE + p * C::PANEL, &maps.q[part], bar(C::B_QF + s), p * 64, h,
-                        i * 128, b);
-            tma_load_4d(st + C::OPND + part * C::TILE + p * C::PANEL, &maps.dO[part], bar(C::B_QF + s),
-                        p * 64, h, i * 128, b);
+            tma_load_4d(sbase + C::OFF_K + x * 2 * C::OPND + part * C::TILE + p * C::PANEL, &maps.k[part],
+                        bar(C::B_KVF + x), p * 64, itm.kvh, itm.j * 128, itm.b);
+            tma_load_4d(sbase + C::OFF_V + x * 2 * C::OPND + part * C::TILE + p * C::PANEL, &maps.v[part],
+                        bar(C::B_KVF + x), p * 64, itm.kvh, itm.j * 128, itm.b);
           }
-        const size_t ro = (static_cast<size_t>(b) * a.Hq + h) * a.Tpad + static_cast<size_t>(i) * 128;
-        bulk_load(st + 2 * C::OPND, a.lse2 + ro, 512, bar(C::B_QF + s));
-        bulk_load(st + 2 * C::OPND + 512, a.dvec + ro, 512, bar(C::B_QF + s));
+        for (int it = 0; it < itm.n_it; ++it, ++gi) {
+          const int s = gi % C::NQS;
+          if (gi >= C::NQS && !mbar_wait(bar(C::B_QE + s), ((gi / C::NQS) - 1) & 1, w)) {
+            ok = false;
+            break;
+          }
+          const int h = itm.kvh * a.group + it / itm.n_i;
+          const int i = itm.j + it % itm.n_i;
+          const uint32_t st = stage(s);
+          mbar_expect_tx(bar(C::B_QF + s), 2 * C::OPND + 1024);
+          for (int part = 0; part < C::NPART; ++part)
+            for (int p = 0; p < C::DPANELS; ++p) {
+              tma_load_4d(st + part * C::TILE + p * C::PANEL, &maps.q[part], bar(C::B_QF + s), p * 64, h, i * 128,
+                          itm.b);
+              tma_load_4d(st + C::OPND + part * C::TILE + p * C::PANEL, &maps.dO[part], bar(C::B_QF + s), p * 64,
+                          h, i * 128, itm.b);
+            }
+          const size_t ro = (static_cast<size_t>(itm.b) * a.Hq + h) * a.Tpad + static_cast<size_t>(i) * 128;
+          bulk_load(st + 2 * C::OPND, a.lse2 + ro, 512, bar(C::B_QF + s));
+          bulk_load(st + 2 * C::OPND + 512, a.dvec + ro, 512, bar(C::B_QF + s));
+        }
       }
-    }
-    if (leader) {
-      mbar_drain(bar(C::B_KV), 0, a.timeout_ns);
-      for (int s = 0; s < C::NQS && s < it; ++s) {
-        const int last = s + ((it - 1 - s) / C::NQS) * C::NQS;
+      // Exit path: every load issued has landed before shared memory is
+      // released. n K/V loads were issued, minus one if the loop left before
+      // the load of item n - 1 (only when a wait gave up).
+      const int nkv = n;
+      for (int x = 0; x < C::KVB && x < nkv; ++x) {
+        const int last = x + ((nkv - 1 - x) / C::KVB) * C::KVB;
+        mbar_drain(bar(C::B_KVF + x), (last / C::KVB) & 1, a.timeout_ns);
+      }
+      for (int s = 0; s < C::NQS && s < gi; ++s) {
+        const int last = s + ((gi - 1 - s) / C::NQS) * C::NQS;
         mbar_drain(bar(C::B_QF + s), (last / C::NQS) & 1, a.timeout_ns);
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
-    // ---------------- tcgen05 MMA issuer (whole warp; one elected lane issues) ----------------
-    const bool leader = elect_one();
-    const uint32_t kb = sbase + C::OFF_K, vb = sbase + C::OFF_V;
-    const uint32_t pb = sbase + C::OFF_P, dsb = sbase + C::OFF_DS;
-    // S^T = K Q^T (M = keys, N = queries, K = head dim) into TMEM_S
-    auto issue_s = [&](int it2) {
-      const uint32_t qb = stage(it2 % C::NQS);
-#pragma unroll
-      for (int t = 0; t < C::NPROD; ++t)
-#pragma unroll
-        for (int k = 0; k < DHB / 16; ++k) {
-          const uint32_t off = (k / 4) * C::PANEL + (k % 4) * 32;
-          const uint64_t ad = make_sdesc(kb + C::pa(t) * C::TILE + off, 16, 1024);
-          const uint64_t bd = make_sdesc(qb + C::pb(t) * C::TILE + off, 16, 1024);
-          if (leader) mma_ss<false>(tmem + C::TM_S, ad, bd, C::IDESC_T, (t > 0 || k > 0) ? 1u : 0u);
-        }
-      if (leader) tc_commit(bar(C::B_SR));
-    };
-    // dP^T = V dO^T into TMEM_DP
-    auto issue_dp = [&](int it2) {
-      const uint32_t dob = stage(it2 % C::NQS) + C::OPND;
-#pragma unroll
-      for (int t = 0; t < C::NPROD; ++t)
-#pragma unroll
-        for (int k = 0; k < DHB / 16; ++k) {
-          const uint32_t off = (k / 4) * C::PANEL + (k % 4) * 32;
-          const uint64_t ad = make_sdesc(vb + C::pa(t) * C::TILE + off, 16, 1024);
-          const uint64_t bd = make_sdesc(dob + C::pb(t) * C::TILE + off, 16, 1024);
-          if (leader) mma_ss<false>(tmem + C::TM_DP, ad, bd, C::IDESC_T, (t > 0 || k > 0) ? 1u : 0u);
-        }
-      if (leader) tc_commit(bar(C::B_DPR));
-    };
-    bool ok = mbar_wait_warp(bar(C::B_KV), 0, w) && mbar_wait_warp(bar(C::B_QF), 0, w);
-    if (ok) {
-      tc_fence_after();
-      issue_s(0);
-      issue_dp(0);
-    }
-    for (int it = 0; ok && it < n_it; ++it) {
-      const int s = it % C::NQS;
-      const uint32_t qb = stage(s), dob = stage(s) + C::OPND;
-      // dV += P^T dO, one query half per warpgroup as soon as it is written
-      // (M = keys, N = head dim, K = queries 64g .. 64g+63).
-#pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        if (!mbar_wait_warp(bar(C::B_PR + g), it & 1, w)) { ok = false; break; }
-        tc_fence_after();
+    // ---------------- tcgen05 MMA issuer (one elected thread) ----------------
+    if (elect_one()) {
+      const uint32_t dsb = sbase + C::OFF_DS;
+      const uint32_t pb = sbase + C::OFF_P;
+      // S^T = K Q^T (M = keys, N = queries, K = head dim) into TMEM_S, for
+      // iteration gi2 whose item uses K/V buffer x2.
+      auto issue_s = [&](int gi2, int x2) {
+        const uint32_t qb = stage(gi2 % C::NQS);
+        const uint32_t kb = sbase + C::OFF_K + x2 * 2 * C::OPND;
 #pragma unroll
         for (int t = 0; t < C::NPROD; ++t)
 #pragma unroll
-          for (int k = 4 * g; k < 4 * g + 4; ++k) {
-            const uint32_t aoff = (k / 4) * C::PANEL + (k % 4) * 32;
-            const uint64_t ad = make_sdesc(pb + C::pa(t) * C::PT_HALF + aoff, 16, 1024);
-            const uint64_t bd = make_sdesc(dob + C::pb(t) * C::TILE + k * 16 * 128, C::PANEL, 1024);
-            if (leader)
-              mma_ss<false>(tmem + C::TM_DV, ad, bd, C::IDESC_KV, (it > 0 || g > 0 || t > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < DHB / 16; ++k) {
+            const uint32_t off = (k / 4) * C::PANEL + (k % 4) * 32;
+            mma_ss<false>(tmem + C::TM_S, make_sdesc(kb + C::pa(t) * C::TILE + off, 16, 1024),
+                          make_sdesc(qb + C::pb(t) * C::TILE + off, 16, 1024), C::IDESC_T, (t > 0 || k > 0) ? 1u : 0u);
           }
-        if constexpr (C::SHARE) {
-          if (leader) tc_commit(bar(C::B_DVD + g));
-        }
-      }
-      if (!ok) break;
-      const bool more = it + 1 < n_it;
-      if constexpr (C::PREFETCH) {
-        // Next iteration's S^T and dP^T while dK and dQ of this one are pending.
-        if (more) {
-          if (!mbar_wait_warp(bar(C::B_QF + (it + 1) % C::NQS), ((it + 1) / C::NQS) & 1, w) ||
-              !mbar_wait_warp(bar(C::B_SDPF), it & 1, w)) { ok = false; break; }
-          tc_fence_after();
-          issue_s(it + 1);
-          issue_dp(it + 1);
-        }
-      }
-      // dK += dS^T Q, one query half at a time (M = keys, N = head dim).
-#pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        if (!mbar_wait_warp(bar(C::B_DSR + g), it & 1, w)) { ok = false; break; }
-        tc_fence_after();
+        tc_commit(bar(C::B_SR));
+      };
+      // dP^T = V dO^T into TMEM_DP
+      auto issue_dp = [&](int gi2, int x2) {
+        const uint32_t dob = stage(gi2 % C::NQS) + C::OPND;
+        const uint32_t vb = sbase + C::OFF_V + x2 * 2 * C::OPND;
 #pragma unroll
         for (int t = 0; t < C::NPROD; ++t)
 #pragma unroll
-          for (int k = 4 * g; k < 4 * g + 4; ++k) {
-            const uint32_t aoff = (k / 4) * C::PANEL + (k % 4) * 32;
-            const uint64_t ad = make_sdesc(dsb + C::pa(t) * C::PT_HALF + aoff, 16, 1024);
-            const uint64_t bd = make_sdesc(qb + C::pb(t) * C::TILE + k * 16 * 128, C::PANEL, 1024);
-            if (leader)
-              mma_ss<false>(tmem + C::TM_DK, ad, bd, C::IDESC_KV, (it > 0 || g > 0 || t > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < DHB / 16; ++k) {
+            const uint32_t off = (k / 4) * C::PANEL + (k % 4) * 32;
+            mma_ss<false>(tmem + C::TM_DP, make_sdesc(vb + C::pa(t) * C::TILE + off, 16, 1024),
+                          make_sdesc(dob + C::pb(t) * C::TILE + off, 16, 1024), C::IDESC_T,
+                          (t > 0 || k > 0) ? 1u : 0u);
           }
+        tc_commit(bar(C::B_DPR));
+      };
+      BwdItem itm{};
+      int n = 0, gi = 0;
+      bool ok = bwd_item(a, 0, itm);
+      if (ok) ok = mbar_wait(bar(C::B_KVF), 0, w) && mbar_wait(bar(C::B_QF), 0, w);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_dp(0, 0);
       }
-      if (!ok) break;
-      // The Q/dO stage is no longer read (dQ reads dS^T and K): release it now.
-      if (leader) tc_commit(bar(C::B_QE + s));
-      // dQ partial = dS K (M = queries, N = head dim, K = keys): the previous
-      // partial must have been drained, and (aliased columns) dP^T fully read.
-      if (it > 0 && !mbar_wait_warp(bar(C::B_ITF), (it - 1) & 1, w)) { ok = false; break; }
-      if constexpr (!C::PREFETCH) {
-        if (!mbar_wait_warp(bar(C::B_SDPF), it & 1, w)) { ok = false; break; }
-      }
-      tc_fence_after();
-#pragma unroll
-      for (int t = 0; t < C::NPROD; ++t)
-#pragma unroll
-        for (int k = 0; k < 128 / 16; ++k) {
-          const uint64_t ad = make_sdesc(dsb + C::pa(t) * C::PT_HALF + k * 16 * 128, C::PANEL, 1024);
-          const uint64_t bd = make_sdesc(kb + C::pb(t) * C::TILE + k * 16 * 128, C::PANEL, 1024);
-          if (leader) mma_ss<false>(tmem + C::TM_DQ, ad, bd, C::IDESC_Q, (t > 0 || k > 0) ? 1u : 0u);
+      while (ok) {
+        const int x = n % C::KVB;
+        const uint32_t kb = sbase + C::OFF_K + x * 2 * C::OPND;
+        // The epilogue of the previous item must have read dK and dV before
+        // this item's first products overwrite them.
+        if (n >= 1 && !mbar_wait(bar(C::B_KVFREE), (n - 1) & 1, w)) {
+          ok = false;
+          break;
         }
-      if (leader) tc_commit(bar(C::B_DQF));
-      if constexpr (!C::PREFETCH) {
-        if (more) {
-          // With aliased dQ columns, dP^T(it+1) may only be written once dQ(it)
-          // has been drained.
-          if (!mbar_wait_warp(bar(C::B_QF + (it + 1) % C::NQS), ((it + 1) / C::NQS) & 1, w)) { ok = false; break; }
-          if (C::DQ_ALIAS && !mbar_wait_warp(bar(C::B_ITF), it & 1, w)) { ok = false; break; }
+        BwdItem nxt{};
+        const bool has_next = bwd_item(a, n + 1, nxt);
+        for (int it = 0; ok && it < itm.n_it; ++it, ++gi) {
+          const int s = gi % C::NQS;
+          const uint32_t qb = stage(s), dob = stage(s) + C::OPND;
+          // The next iteration: in this item, or the first of the next item.
+          const bool more_here = it + 1 < itm.n_it;
+          const bool more = more_here || (C::KVB > 1 && has_next);
+          if constexpr (C::PREFETCH) {
+            // The next iteration's S^T and dP^T go first: they need only this
+            // iteration's S^T / dP^T to have been read (and the next Q/dO
+            // stage), so the compute warps find them ready when they finish
+            // this iteration.
+            if (more) {
+              const int x2 = more_here ? x : (n + 1) % C::KVB;
+              if (!mbar_wait(bar(C::B_QF + (gi + 1) % C::NQS), ((gi + 1) / C::NQS) & 1, w) ||
+                  (!more_here && !mbar_wait(bar(C::B_KVF + x2), ((n + 1) / C::KVB) & 1, w)) ||
+                  !mbar_wait(bar(C::B_SDPF), gi & 1, w)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_s(gi + 1, x2);
+              issue_dp(gi + 1, x2);
+            }
+          }
+          // dV += P^T dO, one query half per warpgroup as soon as it is written
+          // (M = keys, N = head dim, K = queries 64g .. 64g+63).
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            if (!mbar_wait(bar(C::B_PR + g), gi & 1, w)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int t = 0; t < C::NPROD; ++t)
+#pragma unroll
+              for (int k = 4 * g; k < 4 * g + 4; ++k) {
+                const uint32_t acc = (it > 0 || g > 0 || t > 0 || k > 0) ? 1u : 0u;
+                const uint64_t bd = make_sdesc(dob + C::pb(t) * C::TILE + k * 16 * 128, C::PANEL, 1024);
+                if constexpr (C::PTB) {
+                  mma_ts(tmem + C::TM_DV, tmem + C::TM_P + 8 * k, bd, C::IDESC_KV, acc);
+                } else {
+                  const uint32_t aoff = (k / 4) * C::PANEL + (k % 4) * 32;
+                  mma_ss<false>(tmem + C::TM_DV, make_sdesc(pb + C::pa(t) * C::PT_HALF + aoff, 16, 1024), bd,
+                                C::IDESC_KV, acc);
+                }
+              }
+            // P^T half g is free again once this product is done (it no longer
+            // precedes the next S^T / dP^T in issue order).
+            if constexpr (C::SHARE || C::PTB) tc_commit(bar(C::B_DVD + g));
+          }
+          if (!ok) break;
+          // dK += dS^T Q, one query half at a time (M = keys, N = head dim).
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            if (!mbar_wait(bar(C::B_DSR + g), gi & 1, w)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int t = 0; t < C::NPROD; ++t)
+#pragma unroll
+              for (int k = 4 * g; k < 4 * g + 4; ++k) {
+                const uint32_t aoff = (k / 4) * C::PANEL + (k % 4) * 32;
+                mma_ss<false>(tmem + C::TM_DK, make_sdesc(dsb + C::pa(t) * C::PT_HALF + aoff, 16, 1024),
+                              make_sdesc(qb + C::pb(t) * C::TILE + k * 16 * 128, C::PANEL, 1024), C::IDESC_KV,
+                              (it > 0 || g > 0 || t > 0 || k > 0) ? 1u : 0u);
+              }
+          }
+          if (!ok) break;
+          // The Q/dO stage is no longer read (dQ reads dS^T and K): release it now.
+          tc_commit(bar(C::B_QE + s));
+          // dQ partial = dS K (M = queries, N = head dim, K = keys): the previous
+          // partial must have been drained, and (aliased columns) dP^T fully read.
+          if (gi > 0 && !mbar_wait(bar(C::B_ITF), (gi - 1) & 1, w)) {
+            ok = false;
+            break;
+          }
+          if constexpr (!C::PREFETCH) {
+            if (!mbar_wait(bar(C::B_SDPF), gi & 1, w)) {
+              ok = false;
+              break;
+            }
+          }
           tc_fence_after();
-          issue_s(it + 1);
-          issue_dp(it + 1);
+#pragma unroll
+          for (int t = 0; t < C::NPROD; ++t)
+#pragma unroll
+            for (int k = 0; k < 128 / 16; ++k)
+              mma_ss<false>(tmem + C::TM_DQ, make_sdesc(dsb + C::pa(t) * C::PT_HALF + k * 16 * 128, C::PANEL, 1024),
+                            make_sdesc(kb + C::pb(t) * C::TILE + k * 16 * 128, C::PANEL, 1024), C::IDESC_Q,
+                            (t > 0 || k > 0) ? 1u : 0u);
+          tc_commit(bar(C::B_DQF));
+          if (!more_here) tc_commit(bar(C::B_KVE + x));  // the item's last read of K and V
+          if constexpr (!C::PREFETCH) {
+            if (more_here) {
+              // With aliased dQ columns, dP^T(gi+1) may only be written once
+              // dQ(gi) has been drained.
+              if (!mbar_wait(bar(C::B_QF + (gi + 1) % C::NQS), ((gi + 1) / C::NQS) & 1, w) ||
+                  (C::DQ_ALIAS && !mbar_wait(bar(C::B_ITF), gi & 1, w))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_s(gi + 1, x);
+              issue_dp(gi + 1, x);
+            }
+          }
         }
+        if (!ok || !has_next || C::KVB == 1) break;
+        itm = nxt;
+        ++n;
       }
-    }
-    if (leader) {
+      // Exit path: all issued MMAs finish before TMEM is released.
       tc_commit(bar(C::B_FIN));
       mbar_drain(bar(C::B_FIN), 0, a.timeout_ns);
     }
+    __syncwarp();
   } else {
     // ---------------- compute warpgroups ----------------
     // Warpgroup g owns query columns 64g .. 64g+63 of every S^T / dP^T tile
@@ -477,38 +580,37 @@ __global__ void __launch_bounds__(320, 1)
     const float sl2 = a.scale_log2;
     constexpr int W = DHB / 2;  // 32 or 64 head columns drained per warpgroup
     bool ok = true;
-    const int t = threadIdx.x - 64 - 128 * g;  // 0..127 within the warpgroup
-    // dQ(it2) partial -> fp32 accumulator, rows of query tile i2 of head h2.
-    auto drain_dq = [&](int it2) -> bool {
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(C::B_DQF), it2 & 1, w))) return false;
+    // dQ(gi2) partial -> fp32 accumulator, rows of query tile i2 of head h2.
+    auto drain_dq = [&](int gi2, int b2, int h2, int i2) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(C::B_DQF), gi2 & 1, w))) return false;
       tc_fence_after();
-      const int h2 = kvh * a.group + it2 / n_i;
-      const int i2 = j + it2 % n_i;
       uint32_t r[W];
       if constexpr (W == 64) tmem_ld64(tl + C::TM_DQ + g * W, r);
       else tmem_ld32(tl + C::TM_DQ + g * W, r);
       tc_fence_before();
       mbar_arrive(bar(C::B_ITF));
       if constexpr (C::TMA_DQ) {
-        // Stage the fp32 [128 x 32] half in 128-byte-swizzled rows of this
-        // warpgroup's staging panel, then one thread adds the whole box to
-        // global memory. The panel is rewritten only after the previous
-        // reduction (one iteration earlier) has finished reading it.
+        // Each warp stages its 32 rows of the fp32 [128 x 32] half in
+        // 128-byte-swizzled rows (a 4 KB slice of the warpgroup's staging
+        // panel), then its lane 0 adds the [32 x 32] box to global memory. The
+        // slice is rewritten only after that lane's previous reduction (one
+        // iteration earlier) has finished reading it; only warp-level
+        // synchronisation is involved.
         const uint32_t panel = sbase + C::OFF_DQS + g * C::PANEL;
-        if (t == 0) bulk_wait_read0();
-        named_bar(2 + g, 128);
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           st_shared_v4(panel + rl * 128 + ((c ^ (rl & 7)) << 4), r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
         fence_async_smem();
-        named_bar(2 + g, 128);
-        if (t == 0 && g * W < a.Dh) {  // a half past the head width has nothing to add
-          tma_reduce_add_4d(&maps.dq, panel, g * W, h2, i2 * 128, b);
+        __syncwarp();
+        if (lane == 0 && g * W < a.Dh) {  // a half past the head width has nothing to add
+          tma_reduce_add_4d(&maps.dq, panel + quarter * 4096, g * W, h2, i2 * 128 + quarter * 32, b2);
           bulk_commit();
         }
       } else {
         const int qrow = i2 * 128 + rl;
-        float* dst = a.dq_acc + ((static_cast<size_t>(b) * a.T + qrow) * a.Hq + h2) * a.Dh + g * W;
+        float* dst = a.dq_acc + ((static_cast<size_t>(b2) * a.T + qrow) * a.Hq + h2) * a.Dh + g * W;
         const int ncol = a.Dh - g * W;
         if (qrow < a.T && ncol > 0) {
 #pragma unroll
@@ -520,134 +622,172 @@ __global__ void __launch_bounds__(320, 1)
       }
       return true;
     };
-    for (int it = 0; it < n_it; ++it) {
-      const int s = it % C::NQS;
-      const int i = j + it % n_i;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SR), it & 1, w) &&
-                                       mbar_wait(bar(C::B_QF + s), (it / C::NQS) & 1, w));
+    int gi = 0;
+    BwdItem itm{};
+    for (int n = 0; ok && bwd_item(a, n, itm); ++n) {
+      const int j = itm.j;
+      for (int it = 0; it < itm.n_it; ++it, ++gi) {
+        const int s = gi % C::NQS;
+        const int h = itm.kvh * a.group + it / itm.n_i;
+        const int i = j + it % itm.n_i;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SR), gi & 1, w) &&
+                                         mbar_wait(bar(C::B_QF + s), (gi / C::NQS) & 1, w));
+        if (!ok) break;
+        const float* lse2s = reinterpret_cast<const float*>(smem + (stage(s) - sbase) + 2 * C::OPND) + 64 * g;
+        const float* dvs = lse2s + 128;
+        float p[64];
+        uint32_t dpr[64];  // prefetch schedule: dP^T half, loaded together with S^T
+        if constexpr (C::PREFETCH) {
+          // S^T(gi) and dP^T(gi) are issued together: one TMEM round trip for both.
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DPR), gi & 1, w));
+          if (!ok) break;
+          tc_fence_after();
+          uint32_t r[64];
+          tmem_ld64x2(tl + C::TM_S + 64 * g, tl + C::TM_DP + 64 * g, r, dpr);
+          tc_fence_before();
+          mbar_arrive(bar(C::B_SDPF));
+#pragma unroll
+          for (int q = 0; q < 64; ++q) p[q] = __uint_as_float(r[q]);
+        } else {
+          tc_fence_after();
+          uint32_t r[64];
+          tmem_ld64(tl + C::TM_S + 64 * g, r);
+#pragma unroll
+          for (int q = 0; q < 64; ++q) p[q] = __uint_as_float(r[q]);
+        }
+        // P^T = 2^(S^T * scale * log2 e - LSE2); key rl is after query 64g + c on
+        // the diagonal tile: dropped.
+        const bool diag = (i == j);
+        const int lim = rl - 64 * g;
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(lse2s + c);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float e = ex2(fmaf(p[c + u], sl2, -lv[u]));
+            p[c + u] = (diag && c + u < lim) ? 0.f : e;
+          }
+        }
+        if constexpr (C::PTB) {
+          // P^T half g in TMEM was last read by dV(gi - 1).
+          if (gi > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DVD + g), (gi - 1) & 1, w));
+            if (!ok) break;
+            tc_fence_after();
+          }
+          // P^T row -> TMEM: queries (2c, 2c + 1) of this half in column 32 g + c.
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) pk[c] = pack_bf16(p[32 * hh + 2 * c], p[32 * hh + 2 * c + 1]);
+            tmem_st16(tl + C::TM_P + 32 * g + 16 * hh, pk);
+          }
+        } else {
+          store_half_row_bf16<HL>(sbase + C::OFF_P + g * C::PANEL, rl, p, C::PT_HALF);
+          fence_async_smem();
+        }
+        tc_fence_before();
+        mbar_arrive(bar(C::B_PR + g));
+        // dS^T = P^T * (dP^T - D)
+        if constexpr (!C::PREFETCH) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DPR), gi & 1, w));
+          if (!ok) break;
+          tc_fence_after();
+          tmem_ld64(tl + C::TM_DP + 64 * g, dpr);
+          tc_fence_before();
+          mbar_arrive(bar(C::B_SDPF));
+        }
+#pragma unroll
+        for (int q = 0; q < 64; q += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(dvs + q);
+          p[q + 0] *= __uint_as_float(dpr[q + 0]) - d4.x;
+          p[q + 1] *= __uint_as_float(dpr[q + 1]) - d4.y;
+          p[q + 2] *= __uint_as_float(dpr[q + 2]) - d4.z;
+          p[q + 3] *= __uint_as_float(dpr[q + 3]) - d4.w;
+        }
+        if constexpr (C::PREFETCH) {
+          // The dS^T buffer is free once dK(gi-1) and dQ(gi-1) are done.
+          if (gi > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DQF), (gi - 1) & 1, w));
+            if (!ok) break;
+          }
+        }
+        if constexpr (C::SHARE) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DVD + g), gi & 1, w));
+          if (!ok) break;
+        }
+        store_half_row_bf16<HL>(sbase + C::OFF_DS + g * C::PANEL, rl, p, C::PT_HALF);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_DSR + g));
+        // dQ of the previous iteration of this item (prefetch schedule), or of
+        // this one (dP^T of the next iteration may reuse dQ's columns), goes to
+        // the accumulator.
+        if constexpr (C::PREFETCH) {
+          if (it > 0) {
+            const int itp = it - 1;
+            ok = drain_dq(gi - 1, itm.b, itm.kvh * a.group + itp / itm.n_i, j + itp % itm.n_i);
+            if (!ok) break;
+          }
+        } else {
+          ok = drain_dq(gi, itm.b, h, i);
+          if (!ok) break;
+        }
+      }
       if (!ok) break;
-      const float* lse2s = reinterpret_cast<const float*>(smem + (stage(s) - sbase) + 2 * C::OPND) + 64 * g;
-      const float* dvs = lse2s + 128;
-      float p[64];
-      uint32_t dpr[64];  // prefetch schedule: dP^T half, loaded together with S^T
       if constexpr (C::PREFETCH) {
-        // S^T(it) and dP^T(it) are issued together: one TMEM round trip for both.
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DPR), it & 1, w));
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t r[64];
-        tmem_ld64x2(tl + C::TM_S + 64 * g, tl + C::TM_DP + 64 * g, r, dpr);
-        tc_fence_before();
-        mbar_arrive(bar(C::B_SDPF));
-#pragma unroll
-        for (int q = 0; q < 64; ++q) p[q] = __uint_as_float(r[q]);
-      } else {
-        tc_fence_after();
-        uint32_t r[64];
-        tmem_ld64(tl + C::TM_S + 64 * g, r);
-#pragma unroll
-        for (int q = 0; q < 64; ++q) p[q] = __uint_as_float(r[q]);
-      }
-      // P^T = 2^(S^T * scale * log2 e - LSE2); key rl is after query 64g + c on
-      // the diagonal tile: dropped.
-      const bool diag = (i == j);
-      const int lim = rl - 64 * g;
-#pragma unroll
-      for (int c = 0; c < 64; c += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(lse2s + c);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float e = ex2(fmaf(p[c + u], sl2, -lv[u]));
-          p[c + u] = (diag && c + u < lim) ? 0.f : e;
-        }
-      }
-      store_half_row_bf16<HL>(sbase + C::OFF_P + g * C::PANEL, rl, p, C::PT_HALF);
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(C::B_PR + g));
-      // dS^T = P^T * (dP^T - D)
-      if constexpr (!C::PREFETCH) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DPR), it & 1, w));
-        if (!ok) break;
-        tc_fence_after();
-        tmem_ld64(tl + C::TM_DP + 64 * g, dpr);
-        tc_fence_before();
-        mbar_arrive(bar(C::B_SDPF));
-      }
-#pragma unroll
-      for (int q = 0; q < 64; q += 4) {
-        const float4 d4 = *reinterpret_cast<const float4*>(dvs + q);
-        p[q + 0] *= __uint_as_float(dpr[q + 0]) - d4.x;
-        p[q + 1] *= __uint_as_float(dpr[q + 1]) - d4.y;
-        p[q + 2] *= __uint_as_float(dpr[q + 2]) - d4.z;
-        p[q + 3] *= __uint_as_float(dpr[q + 3]) - d4.w;
-      }
-      if constexpr (C::PREFETCH) {
-        // The dS^T buffer is free once dK(it-1) and dQ(it-1) are done.
-        if (it > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DQF), (it - 1) & 1, w));
-          if (!ok) break;
-        }
-      }
-      if constexpr (C::SHARE) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DVD + g), it & 1, w));
+        const int itp = itm.n_it - 1;
+        ok = drain_dq(gi - 1, itm.b, itm.kvh * a.group + itp / itm.n_i, j + itp % itm.n_i);
         if (!ok) break;
       }
-      store_half_row_bf16<HL>(sbase + C::OFF_DS + g * C::PANEL, rl, p, C::PT_HALF);
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(C::B_DSR + g));
-      // dQ of the previous iteration (prefetch schedule), or of this one (dP^T
-      // of the next iteration may reuse dQ's columns), goes to the accumulator.
-      if constexpr (C::PREFETCH) {
-        if (it > 0) {
-          ok = drain_dq(it - 1);
-          if (!ok) break;
-        }
-      } else {
-        ok = drain_dq(it);
-        if (!ok) break;
-      }
-    }
-    if (C::PREFETCH && ok) ok = drain_dq(n_it - 1);
-    if constexpr (C::TMA_DQ) {
-      if (t == 0) bulk_wait0();  // every bulk reduction of this CTA has landed
-    }
-    if (ok) {
-      // The last dQ commit covered every MMA, including the final dK/dV updates.
+      // ---- epilogue of the item: the last dQ commit covered every MMA of it,
+      // including the final dK / dV updates.
       const int key = j * 128 + rl;
       const bool valid = key < a.T;
-      const size_t row_off = ((static_cast<size_t>(b) * a.T + key) * a.Hkv + kvh) * a.Dh + g * W;
+      const size_t row_off = ((static_cast<size_t>(itm.b) * a.T + key) * a.Hkv + itm.kvh) * a.Dh + g * W;
       const int ncol = a.Dh - g * W;
+      uint32_t rv[W], rk[W];
+      if constexpr (W == 64) {
+        tmem_ld64(tl + C::TM_DV + g * W, rv);
+        tmem_ld64(tl + C::TM_DK + g * W, rk);
+      } else {
+        tmem_ld32(tl + C::TM_DV + g * W, rv);
+        tmem_ld32(tl + C::TM_DK + g * W, rk);
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::B_KVFREE));  // the next item's products may overwrite dK, dV
+      if (valid && ncol > 0) {
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col0 = (which == 0 ? C::TM_DV : C::TM_DK) + g * W;
-        const float mul = which == 0 ? 1.f : a.scale;
-        void* base = which == 0 ? a.dv : a.dk;
-        uint32_t r[W];
-        if constexpr (W == 64) tmem_ld64(tl + col0, r);
-        else tmem_ld32(tl + col0, r);
-        if (!valid || ncol <= 0) continue;
-        if constexpr (HL) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(base) + row_off);
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t* r = which == 0 ? rv : rk;
+          const float mul = which == 0 ? 1.f : a.scale;
+          void* base = which == 0 ? a.dv : a.dk;
+          if constexpr (HL) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(base) + row_off);
 #pragma unroll
-          for (int u = 0; u < W / 4; ++u)
-            if (4 * u < ncol)
-              dst[u] = make_float4(__uint_as_float(r[4 * u]) * mul, __uint_as_float(r[4 * u + 1]) * mul,
-                                   __uint_as_float(r[4 * u + 2]) * mul, __uint_as_float(r[4 * u + 3]) * mul);
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + row_off);
+            for (int u = 0; u < W / 4; ++u)
+              if (4 * u < ncol)
+                dst[u] = make_float4(__uint_as_float(r[4 * u]) * mul, __uint_as_float(r[4 * u + 1]) * mul,
+                                     __uint_as_float(r[4 * u + 2]) * mul, __uint_as_float(r[4 * u + 3]) * mul);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + row_off);
 #pragma unroll
-          for (int u = 0; u < W / 8; ++u)
-            if (8 * u < ncol)
-              dst[u] = make_uint4(
-                  pack_bf16(__uint_as_float(r[8 * u]) * mul, __uint_as_float(r[8 * u + 1]) * mul),
-                  pack_bf16(__uint_as_float(r[8 * u + 2]) * mul, __uint_as_float(r[8 * u + 3]) * mul),
-                  pack_bf16(__uint_as_float(r[8 * u + 4]) * mul, __uint_as_float(r[8 * u + 5]) * mul),
-                  pack_bf16(__uint_as_float(r[8 * u + 6]) * mul, __uint_as_float(r[8 * u + 7]) * mul));
+            for (int u = 0; u < W / 8; ++u)
+              if (8 * u < ncol)
+                dst[u] = make_uint4(
+                    pack_bf16(__uint_as_float(r[8 * u]) * mul, __uint_as_float(r[8 * u + 1]) * mul),
+                    pack_bf16(__uint_as_float(r[8 * u + 2]) * mul, __uint_as_float(r[8 * u + 3]) * mul),
+                    pack_bf16(__uint_as_float(r[8 * u + 4]) * mul, __uint_as_float(r[8 * u + 5]) * mul),
+                    pack_bf16(__uint_as_float(r[8 * u + 6]) * mul, __uint_as_float(r[8 * u + 7]) * mul));
+          }
         }
       }
+    }
+    if constexpr (C::TMA_DQ) {
+      if (lane == 0) bulk_wait0();  // every bulk reduction this warp issued has landed
+      __syncwarp();
     }
   }
 

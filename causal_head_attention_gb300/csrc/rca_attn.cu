@@ -80,8 +80,9 @@ EncodeFn get_encode() {
 // panel of the head dimension, 128-byte swizzle. Positions past T and head
 // columns past Dh read as zero.
 rca_status make_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t H, int64_t Dh,
-                    bool f32, const char* name) {
-  // (f32 selects fp32 elements with 32-element panels; bf16 uses 64-element panels)
+                    bool f32, const char* name, unsigned box_rows = 128) {
+  // (f32 selects fp32 elements with 32-element panels; bf16 uses 64-element panels;
+  // a box covers box_rows positions of one head)
   EncodeFn enc = get_encode();
   if (!enc) return fail(RCA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorName(g_encode_err));
   const uint64_t es = f32 ? 4 : 2;
@@ -89,7 +90,7 @@ rca_status make_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64
                         static_cast<cuuint64_t>(B)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(Dh * es), static_cast<cuuint64_t>(H * Dh * es),
                            static_cast<cuuint64_t>(T * H * Dh * es)};
-  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / es), 1, 128, 1};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / es), 1, box_rows, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                    const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -332,7 +333,8 @@ rca_status launch_bwd_main(const void* q, const void* k, const void* v, const vo
     maps.v[1] = maps.v[0];
     maps.dO[1] = maps.dO[0];
   }
-  RCA_CHECK(make_map(&maps.dq, w + L.dq_off, B, T, Hq, Dh, true, "dq accumulator"));
+  // dQ partials are added by each warp for its 32 query rows.
+  RCA_CHECK(make_map(&maps.dq, w + L.dq_off, B, T, Hq, Dh, true, "dq accumulator", 32));
   int* status = status_override;
   if (!status) RCA_CHECK(status_word(&status));
   auto kern = rca::attn_bwd_main_kernel<HL, DHB>;
@@ -352,8 +354,16 @@ rca_status launch_bwd_main(const void* q, const void* k, const void* v, const vo
   a.Tpad = int(L.Tpad);
   a.scale = float(1.0 / std::sqrt(double(Dh)));
   a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(Dh)));
-  const unsigned grid = unsigned(int64_t(a.n_t) * B * Hkv);
-  kern<<<grid, C::NTHREADS, C::SMEM_BYTES, st>>>(maps, a);
+  a.n_items = int(int64_t(a.n_t) * B * Hkv);
+  // Persistent launch (one CTA per SM walking several work items) where the
+  // kernel prefetches across items; otherwise one CTA per work item.
+  int grid = a.n_items;
+  if (C::PTB) {
+    int sms = 0;
+    RCA_CHECK(sm_count(&sms));
+    if (grid > sms) grid = sms;
+  }
+  kern<<<unsigned(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(maps, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch attn_bwd_main_kernel");
   return RCA_OK;
