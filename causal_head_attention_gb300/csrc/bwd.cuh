@@ -199,7 +199,13 @@ struct BwdCfg {
   static constexpr uint32_t IDESC_T = make_idesc(false, 128, 128, false, false);   // S^T, dP^T
   static constexpr uint32_t IDESC_KV = make_idesc(false, 128, DHB, false, true);   // dV, dK
   static constexpr uint32_t IDESC_Q = make_idesc(false, 128, DHB, true, true);     // dQ
-  static constexpr int NTHREADS = 320;
+  // Warpgroups (4 warps each): 0 dQ drain, 1 and 2 compute, 3 = TMA producer
+  // (warp 12), MMA issuer (warp 13) and two idle warps. Registers are split
+  // per warpgroup from the 128 per thread the CTA is launched with.
+  static constexpr int NTHREADS = 512;
+  static constexpr int LAUNCH_REGS = 128;
+  static constexpr int REG_DQ = 64, REG_CTL = 96, REG_CMP = 176;
+  static_assert(128 * REG_DQ + 256 * REG_CMP + 128 * REG_CTL <= NTHREADS * LAUNCH_REGS, "register split");
   // barriers
   static constexpr int B_KVF = 0;            // [KVB] K/V tiles of a work item landed
   static constexpr int B_KVE = B_KVF + KVB;  // [KVB] K/V buffer free (last dQ of its item done)
@@ -284,7 +290,7 @@ __device__ __forceinline__ void store_half_row_bf16(uint32_t panel, int rl, cons
 }
 
 template <bool HL, int DHB>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(512, 1)
     attn_bwd_main_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   using C = BwdCfg<HL, DHB>;
   extern __shared__ uint8_t smem_raw[];
@@ -316,13 +322,13 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(bar(C::B_DSR + g), 128);
     }
     mbar_init(bar(C::B_DQF), 1);
-    mbar_init(bar(C::B_ITF), 256);
+    mbar_init(bar(C::B_ITF), 128);  // the dQ drain warpgroup
     mbar_init(bar(C::B_KVFREE), 256);
     mbar_init(bar(C::B_FIN), 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
-  if (warp == 1) {
+  if (warp == 13) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -331,11 +337,27 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl w{a.status, abort_flag, a.timeout_ns};
+  // Every role ends in end_role(): the TMEM owner (warp 13) waits until all
+  // 512 threads have finished with TMEM and releases it; the others only
+  // arrive. No code follows the role branches (each warpgroup runs with its
+  // own register budget).
+  auto end_role = [&]() {
+    tc_fence_before();
+    if (warp == 13) {
+      named_bar(1, C::NTHREADS);
+      tc_fence_after();
+      tmem_dealloc(tmem, C::TMEM_COLS);
+    } else {
+      named_bar_arrive(1, C::NTHREADS);
+    }
+  };
 
   // Every role walks the same sequence of work items; iterations are numbered
   // gi = 0, 1, ... across all of this CTA's items, and the Q/dO ring position
   // and every per-iteration barrier phase is a function of gi.
-  if (warp == 0) {
+  if (warp >= 12) {
+   reg_dealloc<C::REG_CTL>();
+   if (warp == 12) {
     // ---------------- TMA producer (one elected thread) ----------------
     if (elect_one()) {
       for (int part = 0; part < C::NPART; ++part) {
@@ -395,7 +417,7 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+   } else if (warp == 13) {
     // ---------------- tcgen05 MMA issuer (one elected thread) ----------------
     if (elect_one()) {
       const uint32_t dsb = sbase + C::OFF_DS;
@@ -569,67 +591,100 @@ __global__ void __launch_bounds__(320, 1)
       mbar_drain(bar(C::B_FIN), 0, a.timeout_ns);
     }
     __syncwarp();
-  } else {
-    // ---------------- compute warpgroups ----------------
-    // Warpgroup g owns query columns 64g .. 64g+63 of every S^T / dP^T tile
-    // and drains head columns [g W, g W + W) of dQ, dK and dV.
-    const int g = (warp - 2) >> 2;
-    const int quarter = warp & 3;
-    const int rl = quarter * 32 + lane;  // key row for P^T/dS^T, query row for dQ
+   }
+   end_role();  // warps 14 and 15 have no role
+  } else if (warp < 4) {
+    reg_dealloc<C::REG_DQ>();
+    // ---------------- dQ drain warpgroup ----------------
+    // Warp q reads TMEM lanes 32 q .. 32 q + 31 (query rows) of every dQ
+    // partial, 32 head columns at a time, and adds them to the fp32
+    // accumulator: bf16 storage with a 64-column head stages each 32 x 32
+    // block in a 128-byte-swizzled slice of shared memory and adds it with a
+    // bulk tensor reduction issued by the warp's lane 0 (the slice is rewritten
+    // only after that lane's previous reductions have read it); otherwise
+    // every lane adds its row with vector reductions.
+    const int quarter = warp;
+    const int rl = quarter * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const float sl2 = a.scale_log2;
-    constexpr int W = DHB / 2;  // 32 or 64 head columns drained per warpgroup
     bool ok = true;
-    // dQ(gi2) partial -> fp32 accumulator, rows of query tile i2 of head h2.
-    auto drain_dq = [&](int gi2, int b2, int h2, int i2) -> bool {
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(C::B_DQF), gi2 & 1, w))) return false;
-      tc_fence_after();
-      uint32_t r[W];
-      if constexpr (W == 64) tmem_ld64(tl + C::TM_DQ + g * W, r);
-      else tmem_ld32(tl + C::TM_DQ + g * W, r);
-      tc_fence_before();
-      mbar_arrive(bar(C::B_ITF));
-      if constexpr (C::TMA_DQ) {
-        // Each warp stages its 32 rows of the fp32 [128 x 32] half in
-        // 128-byte-swizzled rows (a 4 KB slice of the warpgroup's staging
-        // panel), then its lane 0 adds the [32 x 32] box to global memory. The
-        // slice is rewritten only after that lane's previous reduction (one
-        // iteration earlier) has finished reading it; only warp-level
-        // synchronisation is involved.
-        const uint32_t panel = sbase + C::OFF_DQS + g * C::PANEL;
-        if (lane == 0) bulk_wait_read0();
-        __syncwarp();
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_shared_v4(panel + rl * 128 + ((c ^ (rl & 7)) << 4), r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0 && g * W < a.Dh) {  // a half past the head width has nothing to add
-          tma_reduce_add_4d(&maps.dq, panel + quarter * 4096, g * W, h2, i2 * 128 + quarter * 32, b2);
-          bulk_commit();
+    int gi = 0;
+    BwdItem itm{};
+    for (int n = 0; ok && bwd_item(a, n, itm); ++n) {
+      for (int it = 0; it < itm.n_it; ++it, ++gi) {
+        const int h = itm.kvh * a.group + it / itm.n_i;
+        const int i = itm.j + it % itm.n_i;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DQF), gi & 1, w));
+        if (!ok) break;
+        tc_fence_after();
+        if constexpr (C::TMA_DQ) {
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
         }
-      } else {
-        const int qrow = i2 * 128 + rl;
-        float* dst = a.dq_acc + ((static_cast<size_t>(b2) * a.T + qrow) * a.Hq + h2) * a.Dh + g * W;
-        const int ncol = a.Dh - g * W;
-        if (qrow < a.T && ncol > 0) {
 #pragma unroll
-          for (int u = 0; u < W / 4; ++u)
-            if (4 * u < ncol)
-              red_add_v4(dst + 4 * u, __uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
-                         __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+        for (int c = 0; c < DHB / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tl + C::TM_DQ + 32 * c, r);
+          if (c == DHB / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(bar(C::B_ITF));  // dQ(gi) read: its columns may be overwritten
+          }
+          if constexpr (C::TMA_DQ) {
+            const uint32_t panel = sbase + C::OFF_DQS + c * C::PANEL;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              st_shared_v4(panel + rl * 128 + ((k ^ (rl & 7)) << 4), r[4 * k], r[4 * k + 1], r[4 * k + 2],
+                           r[4 * k + 3]);
+          } else {
+            const int qrow = i * 128 + rl;
+            const int ncol = a.Dh - 32 * c;
+            if (qrow < a.T && ncol > 0) {
+              float* dst = a.dq_acc + ((static_cast<size_t>(itm.b) * a.T + qrow) * a.Hq + h) * a.Dh + 32 * c;
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                if (4 * u < ncol)
+                  red_add_v4(dst + 4 * u, __uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                             __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+            }
+          }
+        }
+        if constexpr (C::TMA_DQ) {
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int c = 0; c < DHB / 32; ++c)
+              if (32 * c < a.Dh)  // a block past the head width has nothing to add
+                tma_reduce_add_4d(&maps.dq, sbase + C::OFF_DQS + c * C::PANEL + quarter * 4096, 32 * c, h,
+                                  i * 128 + quarter * 32, itm.b);
+            bulk_commit();
+          }
         }
       }
-      return true;
-    };
+    }
+    if constexpr (C::TMA_DQ) {
+      if (lane == 0) bulk_wait0();  // every bulk reduction this warp issued has landed
+      __syncwarp();
+    }
+    end_role();
+  } else {
+    reg_alloc<C::REG_CMP>();
+    // ---------------- compute warpgroups ----------------
+    // Warpgroup g owns query columns 64g .. 64g+63 of every S^T / dP^T tile
+    // and writes head columns [g W, g W + W) of dK and dV.
+    const int g = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int rl = quarter * 32 + lane;  // key row of P^T / dS^T
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float sl2 = a.scale_log2;
+    constexpr int W = DHB / 2;  // 32 or 64 head columns per warpgroup
+    bool ok = true;
     int gi = 0;
     BwdItem itm{};
     for (int n = 0; ok && bwd_item(a, n, itm); ++n) {
       const int j = itm.j;
       for (int it = 0; it < itm.n_it; ++it, ++gi) {
         const int s = gi % C::NQS;
-        const int h = itm.kvh * a.group + it / itm.n_i;
-        const int i = j + it % itm.n_i;
+        const int i = j + it % itm.n_i;  // query tile
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SR), gi & 1, w) &&
                                          mbar_wait(bar(C::B_QF + s), (gi / C::NQS) & 1, w));
         if (!ok) break;
@@ -707,12 +762,10 @@ __global__ void __launch_bounds__(320, 1)
           p[q + 2] *= __uint_as_float(dpr[q + 2]) - d4.z;
           p[q + 3] *= __uint_as_float(dpr[q + 3]) - d4.w;
         }
-        if constexpr (C::PREFETCH) {
-          // The dS^T buffer is free once dK(gi-1) and dQ(gi-1) are done.
-          if (gi > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DQF), (gi - 1) & 1, w));
-            if (!ok) break;
-          }
+        // The dS^T buffer is free once dK(gi-1) and dQ(gi-1) are done.
+        if (gi > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DQF), (gi - 1) & 1, w));
+          if (!ok) break;
         }
         if constexpr (C::SHARE) {
           ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DVD + g), gi & 1, w));
@@ -722,28 +775,13 @@ __global__ void __launch_bounds__(320, 1)
         fence_async_smem();
         tc_fence_before();
         mbar_arrive(bar(C::B_DSR + g));
-        // dQ of the previous iteration of this item (prefetch schedule), or of
-        // this one (dP^T of the next iteration may reuse dQ's columns), goes to
-        // the accumulator.
-        if constexpr (C::PREFETCH) {
-          if (it > 0) {
-            const int itp = it - 1;
-            ok = drain_dq(gi - 1, itm.b, itm.kvh * a.group + itp / itm.n_i, j + itp % itm.n_i);
-            if (!ok) break;
-          }
-        } else {
-          ok = drain_dq(gi, itm.b, h, i);
-          if (!ok) break;
-        }
       }
       if (!ok) break;
-      if constexpr (C::PREFETCH) {
-        const int itp = itm.n_it - 1;
-        ok = drain_dq(gi - 1, itm.b, itm.kvh * a.group + itp / itm.n_i, j + itp % itm.n_i);
-        if (!ok) break;
-      }
-      // ---- epilogue of the item: the last dQ commit covered every MMA of it,
+      // ---- epilogue of the item: the last dQ commit covers every MMA of it,
       // including the final dK / dV updates.
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DQF), (gi - 1) & 1, w));
+      if (!ok) break;
+      tc_fence_after();
       const int key = j * 128 + rl;
       const bool valid = key < a.T;
       const size_t row_off = ((static_cast<size_t>(itm.b) * a.T + key) * a.Hkv + itm.kvh) * a.Dh + g * W;
@@ -785,17 +823,7 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
     }
-    if constexpr (C::TMA_DQ) {
-      if (lane == 0) bulk_wait0();  // every bulk reduction this warp issued has landed
-      __syncwarp();
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+    end_role();
   }
 }
 

@@ -340,6 +340,19 @@ rca_status launch_bwd_main(const void* q, const void* k, const void* v, const vo
   auto kern = rca::attn_bwd_main_kernel<HL, DHB>;
   cudaError_t e = ensure_smem(kern, C::SMEM_BYTES, smem_set);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
+  // The kernel splits its registers between warpgroups (setmaxnreg) out of the
+  // per-thread count it is launched with; a different count would make the
+  // split wait forever, so it is checked before the first launch.
+  static std::atomic<int> launch_regs{0};
+  if (launch_regs.load(std::memory_order_acquire) == 0) {
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(bwd)");
+    launch_regs.store(fa.numRegs, std::memory_order_release);
+  }
+  if (launch_regs.load(std::memory_order_acquire) != C::LAUNCH_REGS)
+    return fail(RCA_ERR_UNSUPPORTED, "backward kernel built with %d registers per thread, its warpgroup split needs %d",
+                launch_regs.load(), C::LAUNCH_REGS);
   rca::BwdArgs a{};
   a.dk = dk;
   a.dv = dv;

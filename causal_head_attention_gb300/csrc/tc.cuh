@@ -411,6 +411,17 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
 __device__ __forceinline__ void named_bar(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// Per-warpgroup register budget (executed by every thread of a warpgroup).
+// Raises draw only on registers released by other warpgroups of the same CTA,
+// so the shares must sum to at most the CTA's launch allocation.
+template <int N>
+__device__ __forceinline__ void reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
 // Arrive on a named barrier without waiting for it.
 __device__ __forceinline__ void named_bar_arrive(int id, int count) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
