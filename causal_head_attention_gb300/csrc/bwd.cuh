@@ -160,10 +160,10 @@ struct BwdCfg {
   static constexpr int SMEM_LIMIT = 232448;
   static constexpr int BAR_BYTES = 1024;
   static constexpr int STAGE_BYTES = 2 * OPND + 1024;   // Q, dO, LSE2[128], D[128]
-  // bf16 storage with a 64-column head: dQ halves are staged as fp32 for bulk
-  // tensor reductions in a buffer of their own (two 16 KB panels).
+  // bf16 storage with a 64-column head: dQ is staged as fp32, 32 columns at a
+  // time, for bulk tensor reductions in a 16 KB panel of its own.
   static constexpr bool TMA_DQ = !HL && DHB == 64;
-  static constexpr int DQS_BYTES = TMA_DQ ? 2 * PANEL : 0;
+  static constexpr int DQS_BYTES = TMA_DQ ? PANEL : 0;
   static constexpr int AVAIL = SMEM_LIMIT - 1024 - BAR_BYTES - KVB * 2 * OPND - DQS_BYTES;
   static constexpr int NQS_SEP = (AVAIL - P_SMEM - P_BYTES) / STAGE_BYTES;
   static constexpr int NQS_SHR = (AVAIL - P_BYTES) / STAGE_BYTES;
@@ -599,10 +599,10 @@ __global__ void __launch_bounds__(512, 1)
     // Warp q reads TMEM lanes 32 q .. 32 q + 31 (query rows) of every dQ
     // partial, 32 head columns at a time, and adds them to the fp32
     // accumulator: bf16 storage with a 64-column head stages each 32 x 32
-    // block in a 128-byte-swizzled slice of shared memory and adds it with a
-    // bulk tensor reduction issued by the warp's lane 0 (the slice is rewritten
-    // only after that lane's previous reductions have read it); otherwise
-    // every lane adds its row with vector reductions.
+    // block in the warp's 4 KB, 128-byte-swizzled slice of the staging panel
+    // and adds it with a bulk tensor reduction issued by the warp's lane 0
+    // (the slice is rewritten only after that lane's previous reduction has
+    // read it); otherwise every lane adds its row with vector reductions.
     const int quarter = warp;
     const int rl = quarter * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -616,10 +616,6 @@ __global__ void __launch_bounds__(512, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DQF), gi & 1, w));
         if (!ok) break;
         tc_fence_after();
-        if constexpr (C::TMA_DQ) {
-          if (lane == 0) bulk_wait_read0();
-          __syncwarp();
-        }
 #pragma unroll
         for (int c = 0; c < DHB / 32; ++c) {
           uint32_t r[32];
@@ -629,11 +625,20 @@ __global__ void __launch_bounds__(512, 1)
             mbar_arrive(bar(C::B_ITF));  // dQ(gi) read: its columns may be overwritten
           }
           if constexpr (C::TMA_DQ) {
-            const uint32_t panel = sbase + C::OFF_DQS + c * C::PANEL;
+            const uint32_t panel = sbase + C::OFF_DQS;
+            if (lane == 0) bulk_wait_read0();  // the previous block has been read from the slice
+            __syncwarp();
 #pragma unroll
             for (int k = 0; k < 8; ++k)
               st_shared_v4(panel + rl * 128 + ((k ^ (rl & 7)) << 4), r[4 * k], r[4 * k + 1], r[4 * k + 2],
                            r[4 * k + 3]);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (32 * c < a.Dh)  // a block past the head width has nothing to add
+                tma_reduce_add_4d(&maps.dq, panel + quarter * 4096, 32 * c, h, i * 128 + quarter * 32, itm.b);
+              bulk_commit();
+            }
           } else {
             const int qrow = i * 128 + rl;
             const int ncol = a.Dh - 32 * c;
@@ -645,18 +650,6 @@ __global__ void __launch_bounds__(512, 1)
                   red_add_v4(dst + 4 * u, __uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
                              __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
             }
-          }
-        }
-        if constexpr (C::TMA_DQ) {
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-#pragma unroll
-            for (int c = 0; c < DHB / 32; ++c)
-              if (32 * c < a.Dh)  // a block past the head width has nothing to add
-                tma_reduce_add_4d(&maps.dq, sbase + C::OFF_DQS + c * C::PANEL + quarter * 4096, 32 * c, h,
-                                  i * 128 + quarter * 32, itm.b);
-            bulk_commit();
           }
         }
       }
