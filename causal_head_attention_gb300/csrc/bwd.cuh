@@ -45,23 +45,25 @@ struct PreArgs {
 };
 
 // A group of LPR consecutive lanes handles one (b, t, h) row of Dh elements,
-// each lane 16 bytes, so every load instruction is fully coalesced.
-template <bool F32>
+// each lane 16 bytes, so every load instruction is fully coalesced. IT is the
+// index type of the row decomposition: 32-bit whenever every thread index
+// fits (the divisions are then far cheaper), 64-bit otherwise.
+template <bool F32, typename IT>
 __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const PreArgs a) {
   constexpr int ES = F32 ? 4 : 2;
   constexpr int EPL = 16 / ES;  // elements per lane
-  const int lpr = a.Dh / EPL;   // lanes per row: power of two in [2, 32]
-  const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long rows = static_cast<long long>(a.B) * a.Tpad * a.Hq;
-  const long long row = gid / lpr;
+  const unsigned lpr = static_cast<unsigned>(a.Dh / EPL);  // lanes per row: power of two in [2, 32]
+  const IT gid = static_cast<IT>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const IT rows = static_cast<IT>(a.B) * a.Tpad * a.Hq;
+  const IT row = gid / lpr;
   const int part = static_cast<int>(gid % lpr);
   const bool in = row < rows;
   int b = 0, t = 0, h = 0;
   if (in) {
-    h = static_cast<int>(row % a.Hq);
-    const long long bt = row / a.Hq;
-    t = static_cast<int>(bt % a.Tpad);
-    b = static_cast<int>(bt / a.Tpad);
+    h = static_cast<int>(row % static_cast<IT>(a.Hq));
+    const IT bt = row / static_cast<IT>(a.Hq);
+    t = static_cast<int>(bt % static_cast<IT>(a.Tpad));
+    b = static_cast<int>(bt / static_cast<IT>(a.Tpad));
   }
   const bool live = in && t < a.T;
   float acc = 0.f;
@@ -98,18 +100,29 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const PreArgs 
 // ----------------------------------------------------------------------------
 // dQ convert
 // ----------------------------------------------------------------------------
+// Grid-stride over float4 groups, four loads in flight per thread per pass.
 template <bool F32>
 __global__ void __launch_bounds__(256)
     attn_bwd_dq_convert_kernel(const float* __restrict__ acc, void* __restrict__ dq, long long n4,
                                float scale) {
+  constexpr int U = 4;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
-    const float4 v = reinterpret_cast<const float4*>(acc)[i];
-    if constexpr (F32) {
-      reinterpret_cast<float4*>(dq)[i] = make_float4(v.x * scale, v.y * scale, v.z * scale, v.w * scale);
-    } else {
-      reinterpret_cast<uint2*>(dq)[i] = make_uint2(pack_bf16(v.x * scale, v.y * scale),
-                                                   pack_bf16(v.z * scale, v.w * scale));
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += U * stride) {
+    float4 v[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k)
+      if (i + k * stride < n4) v[k] = reinterpret_cast<const float4*>(acc)[i + k * stride];
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const long long j = i + k * stride;
+      if (j >= n4) continue;
+      if constexpr (F32) {
+        reinterpret_cast<float4*>(dq)[j] =
+            make_float4(v[k].x * scale, v[k].y * scale, v[k].z * scale, v[k].w * scale);
+      } else {
+        reinterpret_cast<uint2*>(dq)[j] = make_uint2(pack_bf16(v[k].x * scale, v[k].y * scale),
+                                                     pack_bf16(v[k].z * scale, v[k].w * scale));
+      }
     }
   }
 }

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -417,10 +418,14 @@ rca_status do_preprocess(const void* out, const float* lse, const void* dout, in
   const int64_t lpr = Dh / (dt == RCA_BF16 ? 8 : 4);
   const int64_t threads = B * L.Tpad * Hq * lpr;
   const unsigned grid = unsigned((threads + 255) / 256);
-  if (dt == RCA_BF16)
-    rca::attn_bwd_preprocess_kernel<false><<<grid, 256, 0, st>>>(a);
-  else
-    rca::attn_bwd_preprocess_kernel<true><<<grid, 256, 0, st>>>(a);
+  const bool narrow = (int64_t(grid) * 256) < (int64_t(1) << 31);  // 32-bit thread indices suffice
+  if (dt == RCA_BF16) {
+    if (narrow) rca::attn_bwd_preprocess_kernel<false, uint32_t><<<grid, 256, 0, st>>>(a);
+    else rca::attn_bwd_preprocess_kernel<false, unsigned long long><<<grid, 256, 0, st>>>(a);
+  } else {
+    if (narrow) rca::attn_bwd_preprocess_kernel<true, uint32_t><<<grid, 256, 0, st>>>(a);
+    else rca::attn_bwd_preprocess_kernel<true, unsigned long long><<<grid, 256, 0, st>>>(a);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch attn_bwd_preprocess_kernel");
   return RCA_OK;
@@ -430,10 +435,9 @@ rca_status do_convert(void* dq, int64_t B, int64_t Hq, int64_t T, int64_t Dh, rc
                       const WsLayout& L, cudaStream_t st) {
   const float* acc = reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws) + L.dq_off);
   const long long n4 = (long long)(B * T * Hq * Dh / 4);
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  long long want = (n4 + 255) / 256;
+  int sms = 0;
+  RCA_CHECK(sm_count(&sms));
+  long long want = (n4 + 1023) / 1024;  // four float4 groups per thread
   const long long cap = (long long)sms * 8;
   const unsigned grid = unsigned(want < cap ? (want > 0 ? want : 1) : cap);
   const float scale = float(1.0 / std::sqrt(double(Dh)));
