@@ -11,12 +11,17 @@
 // Work items are (batch, head, 128-row query tile); key tiles 0..qt are
 // visited, tile qt being the diagonal one.
 //
-// CTA layout (352 threads):
-//   warp 0      TMA producer: per work item the Q tile, then K_t / V_t into
-//               NSK / NSV-stage rings
-//   warp 1      TMEM owner + single-thread issuer of S_t = Q K_t^T
-//   warps 2..9  two softmax warpgroups (thread i of a warpgroup owns query row i)
-//   warp 10     single-thread issuer of the P V products
+// CTA layout (512 threads, four warpgroups with their own register budgets):
+//   warp 0        TMA producer: per work item the Q tile, then K_t / V_t into
+//                 NSK / NSV-stage rings
+//   warp 1        single-thread issuer of S_t = Q K_t^T
+//   warp 2        single-thread issuer of the P V products
+//   warp 3        TMEM owner
+//   warps 4..11   two softmax warpgroups (thread i of a warpgroup owns query row i)
+//   warps 12..15  epilogue warpgroup (persistent mode): per work item it merges
+//                 the two softmax warpgroups' statistics and partials and
+//                 stores O and LSE, while the softmax warpgroups already work
+//                 on the next item
 // Two issuers on different SM sub-partitions keep the tensor pipe fed: each
 // has half the instructions, and neither waits for the other's events.
 //
@@ -54,8 +59,14 @@ namespace rca {
 
 template <bool TF32, int DHP>
 struct FwdCfg {
-  // warp 0 TMA, warp 1 S = Q K^T issuer, warps 2..9 softmax, warp 10 P V issuer
-  static constexpr int NTHREADS = 352;
+  // Warpgroups (4 warps each): 0 = TMA producer (warp 0), S = Q K^T issuer
+  // (warp 1), P V issuer (warp 2), TMEM owner (warp 3); 1 and 2 = softmax;
+  // 3 = epilogue (persistent mode; idle otherwise). Registers are split per
+  // warpgroup from the 128 per thread the CTA is launched with.
+  static constexpr int NTHREADS = 512;
+  static constexpr int LAUNCH_REGS = 128;
+  static constexpr int REG_CTL = 96, REG_SM = 168, REG_EPI = 80;
+  static_assert(128 * REG_CTL + 256 * REG_SM + 128 * REG_EPI <= NTHREADS * LAUNCH_REGS, "register split");
   // bf16 storage: the two softmax warpgroups alternate whole key tiles
   // ("ping-pong"); fp32 storage: they split every key tile in halves.
   static constexpr bool PP = !TF32;
@@ -63,6 +74,9 @@ struct FwdCfg {
   // from TMEM), so it costs no shared-memory bandwidth, which on this part is
   // shared by TMA writes, register stores and the tensor core's operand reads.
   static constexpr bool PT = PP && DHP <= 64;
+  // Persistent CTAs hand each work item's merge and output to the epilogue
+  // warpgroup, so the softmax warpgroups go straight on to the next item.
+  static constexpr bool EPI_WG = PT;
   static constexpr int ES = TF32 ? 4 : 2;     // storage bytes per element
   static constexpr int PE = 128 / ES;         // elements per 128-byte swizzle row
   static constexpr int BM = 128, BN = 128;    // query rows, keys per tile
@@ -131,9 +145,13 @@ struct FwdCfg {
   static constexpr int B_PF = B_SFREE + 2;
   static constexpr int B_OD = B_PF + 4;     // [2 halves][2 parities] P V half done
   static constexpr int B_ITEMD = B_OD + 4;  // every P V product of a work item done
-  static constexpr int B_OFREE = B_ITEMD + 1;  // O partials read by the epilogue (256 arrivals)
-  static constexpr int B_STAT = B_OFREE + 1;   // merge statistics written (256 arrivals)
-  static constexpr int B_FIN = B_STAT + 1;   // [2] exit: S issuer's / P V issuer's MMAs done
+  static constexpr int B_OFREE = B_ITEMD + 1;  // O partials read by the epilogue
+  // [2 item parities] merge statistics written (256 softmax arrivals) / read by
+  // the epilogue warpgroup (128 arrivals). One barrier per parity: on short
+  // items a side may run a whole item ahead of the other.
+  static constexpr int B_STAT = B_OFREE + 1;
+  static constexpr int B_STATFREE = B_STAT + 2;
+  static constexpr int B_FIN = B_STATFREE + 2;   // [2] exit: S issuer's / P V issuer's MMAs done
   static constexpr int NBAR = B_FIN + 2;
   static_assert(8 * NBAR + 8 <= 512, "barrier area");
 };
@@ -203,7 +221,7 @@ __device__ __forceinline__ void split_v_half(uint32_t vsrc, uint32_t vhi, uint32
 }
 
 template <bool TF32, int DHP>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(512, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
   using C = FwdCfg<TF32, DHP>;
@@ -239,14 +257,17 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(bar(C::B_OD + i), 1);
     }
     mbar_init(bar(C::B_ITEMD), 1);
-    mbar_init(bar(C::B_OFREE), 256);
-    mbar_init(bar(C::B_STAT), 256);
+    mbar_init(bar(C::B_OFREE), C::EPI_WG ? 128 : 256);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(C::B_STAT + i), 256);
+      mbar_init(bar(C::B_STATFREE + i), 128);
+    }
     mbar_init(bar(C::B_FIN), 1);
     mbar_init(bar(C::B_FIN + 1), 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
-  if (warp == 1) {
+  if (warp == 3) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -255,11 +276,27 @@ __global__ void __launch_bounds__(352, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl w{a.status, abort_flag, a.timeout_ns};
+  // Every role ends in end_role(): the TMEM owner (warp 3) waits until all
+  // 512 threads have finished with TMEM and releases it; the others only
+  // arrive. No code follows the role branches (each warpgroup runs with its
+  // own register budget).
+  auto end_role = [&]() {
+    tc_fence_before();
+    if (warp == 3) {
+      named_bar(1, C::NTHREADS);
+      tc_fence_after();
+      tmem_dealloc(tmem, C::TMEM_COLS);
+    } else {
+      named_bar_arrive(1, C::NTHREADS);
+    }
+  };
 
   // Every role walks the same sequence of work items; key tiles are numbered
   // t = 0, 1, ... across all of this CTA's items, and every ring position and
   // barrier phase below is a function of t (or of the item number n).
-  if (warp == 0) {
+  if (warp < 4) {
+   reg_dealloc<C::REG_CTL>();
+   if (warp == 0) {
     // ---------------- TMA producer (one elected thread) ----------------
     if (elect_one()) {
       tma_prefetch_desc(&tmQ);
@@ -330,7 +367,7 @@ __global__ void __launch_bounds__(352, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+   } else if (warp == 1) {
     // ---------------- S = Q K^T issuer (one elected thread) ----------------
     // Shared-memory descriptors are built once and advanced by constant
     // offsets (the address field holds address / 16; every address here stays
@@ -374,7 +411,7 @@ __global__ void __launch_bounds__(352, 1)
       mbar_drain(bar(C::B_FIN), 0, a.timeout_ns);
     }
     __syncwarp();
-  } else if (warp == 10) {
+   } else if (warp == 2) {
     // ---------------- P V issuer (one elected thread) ----------------
     if (elect_one()) {
       bool ok = true;
@@ -447,10 +484,13 @@ __global__ void __launch_bounds__(352, 1)
       mbar_drain(bar(C::B_FIN + 1), 0, a.timeout_ns);
     }
     __syncwarp();
-  } else {
+   }
+   end_role();  // warp 3: TMEM owner
+  } else if (warp < 12) {
+    reg_alloc<C::REG_SM>();
     // ---------------- softmax warpgroups ----------------
-    const int g = (warp - 2) >> 2;              // warpgroup
-    const int tq = threadIdx.x - 64 - 128 * g;  // 0..127 within the warpgroup
+    const int g = (warp - 4) >> 2;               // warpgroup
+    const int tq = threadIdx.x - 128 - 128 * g;  // 0..127 within the warpgroup
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -677,17 +717,31 @@ __global__ void __launch_bounds__(352, 1)
         }
       }
       if (!ok) break;
-      // ---- epilogue of work item n ----
+      if constexpr (C::EPI_WG) {
+        // Publish this warpgroup's statistics of item n (set n % 2, free once
+        // the epilogue has read those of item n - 2) and go on to the next item.
+        if (n >= 2) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_STATFREE + (n & 1)), ((n - 2) >> 1) & 1, w));
+          if (!ok) break;
+        }
+        float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT) + (n & 1) * 512;
+        stat[g * 128 + row] = m;
+        stat[256 + g * 128 + row] = l;
+        mbar_arrive(bar(C::B_STAT + (n & 1)));
+        tb += it.nkv;
+        continue;
+      }
+      // ---- epilogue of work item n (one item per CTA) ----
       // Every product of the item (both warpgroups') is complete before the
       // partials are read.
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ITEMD), n & 1, w));
       if (!ok) break;
       // Merge the two warpgroups' statistics through shared memory.
-      float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT) + (C::PT ? (n & 1) * 512 : 0);
+      float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT);
       stat[g * 128 + row] = m;
       stat[256 + g * 128 + row] = l;
       mbar_arrive(bar(C::B_STAT));
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_STAT), n & 1, w));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_STAT), 0, w));
       if (!ok) break;
       tc_fence_after();
       const float m0 = stat[row], m1 = stat[128 + row];
@@ -759,13 +813,80 @@ __global__ void __launch_bounds__(352, 1)
         a.lse[(static_cast<size_t>(it.b) * a.Hq + it.h) * a.T + q_idx] = (mt + __log2f(lt)) * 0.69314718055994531f;
       tb += it.nkv;
     }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+    end_role();
+  } else {
+    reg_dealloc<C::REG_EPI>();
+    if constexpr (C::EPI_WG) {
+      // ---------------- epilogue warpgroup ----------------
+      // Per work item: merge the softmax warpgroups' statistics, wait for the
+      // item's last product, read both O partials (32 head columns at a time),
+      // release them for the next item and store the output rows and LSE.
+      // Warp q owns TMEM lanes (query rows) 32 q .. 32 q + 31.
+      const int quarter = warp & 3;
+      const int row = quarter * 32 + lane;
+      const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+      bool ok = true;
+      int tb = 0;
+      FwdItem it{};
+      for (int n = 0; ok && fwd_item(a, n, it); ++n) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_STAT + (n & 1)), (n >> 1) & 1, w));
+        if (!ok) break;
+        const float* stat = reinterpret_cast<const float*>(smem + C::OFF_STAT) + (n & 1) * 512;
+        const float m0 = stat[row], m1 = stat[128 + row];
+        const float l0 = stat[256 + row], l1 = stat[384 + row];
+        mbar_arrive(bar(C::B_STATFREE + (n & 1)));
+        const float mt = fmaxf(m0, m1);
+        const float f0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - mt);
+        const float f1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - mt);
+        const float lt = l0 * f0 + l1 * f1;
+        const float c0 = f0 / lt, c1 = f1 / lt;
+        // A warpgroup that had no key tile in this item (a single-tile item)
+        // holds a stale partial: it is not read.
+        const bool use0 = it.nkv >= 2 || (tb & 1) == 0;
+        const bool use1 = it.nkv >= 2 || (tb & 1) == 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ITEMD), n & 1, w));
+        if (!ok) break;
+        tc_fence_after();
+        const int q_idx = it.qt * C::BM + row;
+        const bool valid = q_idx < a.T;
+        const size_t row_off = ((static_cast<size_t>(it.b) * a.T + q_idx) * a.Hq + it.h) * a.Dh;
+#pragma unroll
+        for (int c = 0; c < DHP / 32; ++c) {
+          float o[32];
+          uint32_t r[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0.f;
+          if (use0) {
+            tmem_ld32(tl + C::TMEM_O + 32 * c, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]) * c0;
+          }
+          if (use1) {
+            tmem_ld32(tl + C::TMEM_O + C::DHB + 32 * c, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = fmaf(__uint_as_float(r[i]), c1, o[i]);
+          }
+          if (c == DHP / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(bar(C::B_OFREE));  // both partials read: the next item's products may start
+          }
+          const int nc = a.Dh - 32 * c;  // valid columns in this block
+          if (valid && nc > 0) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + row_off + 32 * c);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (8 * u < nc)
+                dst[u] = make_uint4(pack_bf16(o[8 * u], o[8 * u + 1]), pack_bf16(o[8 * u + 2], o[8 * u + 3]),
+                                    pack_bf16(o[8 * u + 4], o[8 * u + 5]), pack_bf16(o[8 * u + 6], o[8 * u + 7]));
+          }
+        }
+        if (valid)
+          a.lse[(static_cast<size_t>(it.b) * a.Hq + it.h) * a.T + q_idx] =
+              (mt + __log2f(lt)) * 0.69314718055994531f;
+        tb += it.nkv;
+      }
+    }
+    end_role();
   }
 }
 

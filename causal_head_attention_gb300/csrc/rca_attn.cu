@@ -253,6 +253,18 @@ rca_status launch_fwd(const void* q, const void* k, const void* v, int64_t B, in
   auto kern = rca::attn_fwd_kernel<TF32, DHP>;
   cudaError_t e = ensure_smem(kern, C::SMEM_BYTES, smem_set);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fwd)");
+  // Warpgroup register split (setmaxnreg) out of the launch count: checked
+  // before the first launch, as in the backward.
+  static std::atomic<int> launch_regs{0};
+  if (launch_regs.load(std::memory_order_acquire) == 0) {
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(fwd)");
+    launch_regs.store(fa.numRegs, std::memory_order_release);
+  }
+  if (launch_regs.load(std::memory_order_acquire) != C::LAUNCH_REGS)
+    return fail(RCA_ERR_UNSUPPORTED, "forward kernel built with %d registers per thread, its warpgroup split needs %d",
+                launch_regs.load(), C::LAUNCH_REGS);
   rca::FwdArgs a{};
   a.out = out;
   a.lse = lse;
