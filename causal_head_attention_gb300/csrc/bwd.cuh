@@ -232,8 +232,9 @@ struct BwdCfg {
   static constexpr int B_DSR = B_DVD + 2;   // [2] dS^T half g written
   static constexpr int B_DQF = B_DSR + 2;   // dQ(it) in TMEM (all MMAs of it done)
   static constexpr int B_ITF = B_DQF + 1;   // dQ(it) drained by both warpgroups
-  static constexpr int B_KVFREE = B_ITF + 1;  // dK, dV of a work item read by the epilogue (256)
-  static constexpr int B_FIN = B_KVFREE + 1;
+  static constexpr int B_KVFREE = B_ITF + 1;  // dK, dV of a work item read (drain warpgroup)
+  static constexpr int B_KVD = B_KVFREE + 1;   // dK, dV of a work item final (its last dK done)
+  static constexpr int B_FIN = B_KVD + 1;
   static constexpr int NBAR = B_FIN + 1;
   // parts multiplied for one product: (hi,hi) [, (hi,lo), (lo,hi)]
   static constexpr int NPROD = HL ? 3 : 1;
@@ -336,7 +337,8 @@ __global__ void __launch_bounds__(512, 1)
     }
     mbar_init(bar(C::B_DQF), 1);
     mbar_init(bar(C::B_ITF), 128);  // the dQ drain warpgroup
-    mbar_init(bar(C::B_KVFREE), 256);
+    mbar_init(bar(C::B_KVFREE), 128);  // the dQ drain warpgroup writes dK, dV
+    mbar_init(bar(C::B_KVD), 1);
     mbar_init(bar(C::B_FIN), 1);
     *abort_flag = 0;
     mbar_init_fence();
@@ -477,12 +479,6 @@ __global__ void __launch_bounds__(512, 1)
       while (ok) {
         const int x = n % C::KVB;
         const uint32_t kb = sbase + C::OFF_K + x * 2 * C::OPND;
-        // The epilogue of the previous item must have read dK and dV before
-        // this item's first products overwrite them.
-        if (n >= 1 && !mbar_wait(bar(C::B_KVFREE), (n - 1) & 1, w)) {
-          ok = false;
-          break;
-        }
         BwdItem nxt{};
         const bool has_next = bwd_item(a, n + 1, nxt);
         for (int it = 0; ok && it < itm.n_it; ++it, ++gi) {
@@ -508,6 +504,13 @@ __global__ void __launch_bounds__(512, 1)
               issue_s(gi + 1, x2);
               issue_dp(gi + 1, x2);
             }
+          }
+          // The previous item's dK and dV must have been read before this
+          // item's first products overwrite them (waited here, after the
+          // prefetch above, so that S^T / dP^T never wait for it).
+          if (it == 0 && n >= 1 && !mbar_wait(bar(C::B_KVFREE), (n - 1) & 1, w)) {
+            ok = false;
+            break;
           }
           // dV += P^T dO, one query half per warpgroup as soon as it is written
           // (M = keys, N = head dim, K = queries 64g .. 64g+63).
@@ -558,6 +561,7 @@ __global__ void __launch_bounds__(512, 1)
           if (!ok) break;
           // The Q/dO stage is no longer read (dQ reads dS^T and K): release it now.
           tc_commit(bar(C::B_QE + s));
+          if (!more_here) tc_commit(bar(C::B_KVD));  // the item's dK and dV are final
           // dQ partial = dS K (M = queries, N = head dim, K = keys): the previous
           // partial must have been drained, and (aliased columns) dP^T fully read.
           if (gi > 0 && !mbar_wait(bar(C::B_ITF), (gi - 1) & 1, w)) {
@@ -609,6 +613,8 @@ __global__ void __launch_bounds__(512, 1)
   } else if (warp < 4) {
     reg_dealloc<C::REG_DQ>();
     // ---------------- dQ drain warpgroup ----------------
+    // It also writes each work item's dK and dV once the item's last product
+    // is done, so the compute warpgroups go straight on to the next item.
     // Warp q reads TMEM lanes 32 q .. 32 q + 31 (query rows) of every dQ
     // partial, 32 head columns at a time, and adds them to the fp32
     // accumulator: bf16 storage with a 64-column head stages each 32 x 32
@@ -624,6 +630,51 @@ __global__ void __launch_bounds__(512, 1)
     BwdItem itm{};
     for (int n = 0; ok && bwd_item(a, n, itm); ++n) {
       for (int it = 0; it < itm.n_it; ++it, ++gi) {
+        if (it == itm.n_it - 1) {
+          // ---- dK, dV of the item, written as soon as its last dK product is
+          // done (before its last dQ is drained). Key row rl of the key tile,
+          // 32 head columns at a time; dK carries the softmax scale.
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_KVD), n & 1, w));
+          if (!ok) break;
+          tc_fence_after();
+          const int key = itm.j * 128 + rl;
+          const bool valid = key < a.T;
+          const size_t row_off = ((static_cast<size_t>(itm.b) * a.T + key) * a.Hkv + itm.kvh) * a.Dh;
+#pragma unroll
+          for (int which = 0; which < 2; ++which) {
+#pragma unroll
+            for (int c = 0; c < DHB / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(tl + (which == 0 ? C::TM_DV : C::TM_DK) + 32 * c, r);
+              if (which == 1 && c == DHB / 32 - 1) {
+                tc_fence_before();
+                mbar_arrive(bar(C::B_KVFREE));  // the next item's products may overwrite dK, dV
+              }
+              const float mul = which == 0 ? 1.f : a.scale;
+              const int ncol = a.Dh - 32 * c;
+              if (!valid || ncol <= 0) continue;
+              void* base = which == 0 ? a.dv : a.dk;
+              if constexpr (HL) {
+                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(base) + row_off + 32 * c);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                  if (4 * u < ncol)
+                    dst[u] = make_float4(__uint_as_float(r[4 * u]) * mul, __uint_as_float(r[4 * u + 1]) * mul,
+                                         __uint_as_float(r[4 * u + 2]) * mul, __uint_as_float(r[4 * u + 3]) * mul);
+              } else {
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + row_off + 32 * c);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                  if (8 * u < ncol)
+                    dst[u] = make_uint4(
+                        pack_bf16(__uint_as_float(r[8 * u]) * mul, __uint_as_float(r[8 * u + 1]) * mul),
+                        pack_bf16(__uint_as_float(r[8 * u + 2]) * mul, __uint_as_float(r[8 * u + 3]) * mul),
+                        pack_bf16(__uint_as_float(r[8 * u + 4]) * mul, __uint_as_float(r[8 * u + 5]) * mul),
+                        pack_bf16(__uint_as_float(r[8 * u + 6]) * mul, __uint_as_float(r[8 * u + 7]) * mul));
+              }
+            }
+          }
+        }
         const int h = itm.kvh * a.group + it / itm.n_i;
         const int i = itm.j + it % itm.n_i;
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DQF), gi & 1, w));
@@ -675,14 +726,12 @@ __global__ void __launch_bounds__(512, 1)
   } else {
     reg_alloc<C::REG_CMP>();
     // ---------------- compute warpgroups ----------------
-    // Warpgroup g owns query columns 64g .. 64g+63 of every S^T / dP^T tile
-    // and writes head columns [g W, g W + W) of dK and dV.
+    // Warpgroup g owns query columns 64g .. 64g+63 of every S^T / dP^T tile.
     const int g = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int rl = quarter * 32 + lane;  // key row of P^T / dS^T
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = a.scale_log2;
-    constexpr int W = DHB / 2;  // 32 or 64 head columns per warpgroup
     bool ok = true;
     int gi = 0;
     BwdItem itm{};
@@ -783,51 +832,6 @@ __global__ void __launch_bounds__(512, 1)
         mbar_arrive(bar(C::B_DSR + g));
       }
       if (!ok) break;
-      // ---- epilogue of the item: the last dQ commit covers every MMA of it,
-      // including the final dK / dV updates.
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DQF), (gi - 1) & 1, w));
-      if (!ok) break;
-      tc_fence_after();
-      const int key = j * 128 + rl;
-      const bool valid = key < a.T;
-      const size_t row_off = ((static_cast<size_t>(itm.b) * a.T + key) * a.Hkv + itm.kvh) * a.Dh + g * W;
-      const int ncol = a.Dh - g * W;
-      uint32_t rv[W], rk[W];
-      if constexpr (W == 64) {
-        tmem_ld64(tl + C::TM_DV + g * W, rv);
-        tmem_ld64(tl + C::TM_DK + g * W, rk);
-      } else {
-        tmem_ld32(tl + C::TM_DV + g * W, rv);
-        tmem_ld32(tl + C::TM_DK + g * W, rk);
-      }
-      tc_fence_before();
-      mbar_arrive(bar(C::B_KVFREE));  // the next item's products may overwrite dK, dV
-      if (valid && ncol > 0) {
-#pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          const uint32_t* r = which == 0 ? rv : rk;
-          const float mul = which == 0 ? 1.f : a.scale;
-          void* base = which == 0 ? a.dv : a.dk;
-          if constexpr (HL) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(base) + row_off);
-#pragma unroll
-            for (int u = 0; u < W / 4; ++u)
-              if (4 * u < ncol)
-                dst[u] = make_float4(__uint_as_float(r[4 * u]) * mul, __uint_as_float(r[4 * u + 1]) * mul,
-                                     __uint_as_float(r[4 * u + 2]) * mul, __uint_as_float(r[4 * u + 3]) * mul);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + row_off);
-#pragma unroll
-            for (int u = 0; u < W / 8; ++u)
-              if (8 * u < ncol)
-                dst[u] = make_uint4(
-                    pack_bf16(__uint_as_float(r[8 * u]) * mul, __uint_as_float(r[8 * u + 1]) * mul),
-                    pack_bf16(__uint_as_float(r[8 * u + 2]) * mul, __uint_as_float(r[8 * u + 3]) * mul),
-                    pack_bf16(__uint_as_float(r[8 * u + 4]) * mul, __uint_as_float(r[8 * u + 5]) * mul),
-                    pack_bf16(__uint_as_float(r[8 * u + 6]) * mul, __uint_as_float(r[8 * u + 7]) * mul));
-          }
-        }
-      }
     }
     end_role();
   }
