@@ -11,7 +11,7 @@
 // "config.py"): dK and dV sum over the query heads that share a KV head.
 //
 // Three kernels:
-//   attn_bwd_preprocess_kernel  D, LSE in base 2 (padded rows: D = 0, LSE = +inf),
+//   attn_bwd_preprocess_kernel  -D and -LSE in base 2 (padded rows: 0 and -inf),
 //                               zeroes the fp32 dQ accumulator. HBM-bound.
 //   attn_bwd_main_kernel        work item = (batch, KV head, 128-key tile j); loops
 //                               over every query head of the group and every query
@@ -39,8 +39,8 @@ struct PreArgs {
   const float* lse;
   const void* dout;
   float* dq_acc;  // [B, T, Hq, Dh]
-  float* lse2;    // [B, Hq, Tpad]
-  float* dvec;    // [B, Hq, Tpad]
+  float* lse2;    // [B, Hq, Tpad]  -LSE * log2(e); -inf on padded rows
+  float* dvec;    // [B, Hq, Tpad]  -D; 0 on padded rows
   int B, Hq, T, Dh, Tpad;
 };
 
@@ -91,9 +91,9 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const PreArgs 
   for (int o = lpr >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, lpr);
   if (in && part == 0) {
     const size_t so = (static_cast<size_t>(b) * a.Hq + h) * a.Tpad + t;
-    a.dvec[so] = live ? acc : 0.f;
-    a.lse2[so] = live ? a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.T + t] * 1.4426950408889634f
-                      : INFINITY;
+    a.dvec[so] = live ? -acc : 0.f;
+    a.lse2[so] = live ? -(a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.T + t] * 1.4426950408889634f)
+                      : -INFINITY;
   }
 }
 
@@ -731,7 +731,7 @@ __global__ void __launch_bounds__(512, 1)
     const int quarter = warp & 3;
     const int rl = quarter * 32 + lane;  // key row of P^T / dS^T
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const float sl2 = a.scale_log2;
+    const uint64_t sl2x2 = f2pack(a.scale_log2, a.scale_log2);
     bool ok = true;
     int gi = 0;
     BwdItem itm{};
@@ -765,19 +765,25 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int q = 0; q < 64; ++q) p[q] = __uint_as_float(r[q]);
         }
-        // P^T = 2^(S^T * scale * log2 e - LSE2); key rl is after query 64g + c on
-        // the diagonal tile: dropped.
-        const bool diag = (i == j);
-        const int lim = rl - 64 * g;
+        // P^T = 2^(S^T * scale * log2 e - LSE * log2 e) (the stage holds the
+        // negated base-2 LSE), two columns per packed FMA; key rl is after query
+        // 64g + c on the diagonal tile: dropped.
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(lse2s + c);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          float x0, x1, x2, x3;
+          f2unpack(ffma2(f2pack(p[c], p[c + 1]), sl2x2, f2pack(l4.x, l4.y)), x0, x1);
+          f2unpack(ffma2(f2pack(p[c + 2], p[c + 3]), sl2x2, f2pack(l4.z, l4.w)), x2, x3);
+          p[c] = ex2(x0);
+          p[c + 1] = ex2(x1);
+          p[c + 2] = ex2(x2);
+          p[c + 3] = ex2(x3);
+        }
+        if (i == j) {  // diagonal tile (uniform across the CTA)
+          const int lim = rl - 64 * g;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float e = ex2(fmaf(p[c + u], sl2, -lv[u]));
-            p[c + u] = (diag && c + u < lim) ? 0.f : e;
-          }
+          for (int c = 0; c < 64; ++c)
+            if (c < lim) p[c] = 0.f;
         }
         if constexpr (C::PTB) {
           // P^T half g in TMEM was last read by dV(gi - 1).
@@ -809,13 +815,21 @@ __global__ void __launch_bounds__(512, 1)
           tc_fence_before();
           mbar_arrive(bar(C::B_SDPF));
         }
+        // (the stage holds -D), two columns per packed add and multiply
 #pragma unroll
         for (int q = 0; q < 64; q += 4) {
           const float4 d4 = *reinterpret_cast<const float4*>(dvs + q);
-          p[q + 0] *= __uint_as_float(dpr[q + 0]) - d4.x;
-          p[q + 1] *= __uint_as_float(dpr[q + 1]) - d4.y;
-          p[q + 2] *= __uint_as_float(dpr[q + 2]) - d4.z;
-          p[q + 3] *= __uint_as_float(dpr[q + 3]) - d4.w;
+          float y0, y1, y2, y3;
+          f2unpack(fmul2(f2pack(p[q], p[q + 1]),
+                         fadd2(f2pack(__uint_as_float(dpr[q]), __uint_as_float(dpr[q + 1])), f2pack(d4.x, d4.y))),
+                   y0, y1);
+          f2unpack(fmul2(f2pack(p[q + 2], p[q + 3]),
+                         fadd2(f2pack(__uint_as_float(dpr[q + 2]), __uint_as_float(dpr[q + 3])), f2pack(d4.z, d4.w))),
+                   y2, y3);
+          p[q] = y0;
+          p[q + 1] = y1;
+          p[q + 2] = y2;
+          p[q + 3] = y3;
         }
         // The dS^T buffer is free once dK(gi-1) and dQ(gi-1) are done.
         if (gi > 0) {

@@ -121,7 +121,7 @@ rca_status rca_attn_bwd(const void* q, const void* k, const void* v, const void*
  * The three stages of rca_attn_bwd, exposed so a caller can time or schedule
  * them separately. They must run in this order on one stream with the same
  * arguments and workspace.
- *  preprocess: D = rowsum(dout * out), LSE in base 2, zeroes the dQ accumulator
+ *  preprocess: -D = -rowsum(dout * out), -LSE in base 2, zeroes the dQ accumulator
  *              (memory-bound).
  *  main:       recomputes P from Q, K and LSE; accumulates dK, dV per key tile
  *              (written to dk, dv) and adds dQ partials into the workspace.
