@@ -13,3 +13,4 @@ from .attention import (  # noqa: F401
     head_backward,
     head_forward,
 )
+from .decode import gather_positions, paged_decode  # noqa: F401
