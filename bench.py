@@ -36,7 +36,14 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from causal_head_attention_gb300.inputs import BY_NAME, HEADLINE, make_inputs  # noqa: E402
+from causal_head_attention_gb300.inputs import (  # noqa: E402
+    BY_NAME,
+    DEC_GQA,
+    DEC_MHA,
+    HEADLINE,
+    make_inputs,
+    make_paged_inputs,
+)
 
 L2_BYTES = 129 * 1024 * 1024
 
@@ -398,6 +405,12 @@ def run_gpu(args, w, world, rank, local):
                "sample": f"{n} of {w.B * w.Hkv} (batch, KV-head) groups of the same workload, fwd+bwd, fp64, "
                          f"{dt:.1f} s"}
 
+    decode = None
+    if rank == 0 and not args.no_decode:
+        decode = [bench_decode(dw, dev, stream, args.decode_steps, 5,
+                               0.0 if (args.no_cpu_baseline or world > 1) else args.decode_cpu_budget, P)
+                  for dw in (DEC_MHA, DEC_GQA)]
+
     if rank == 0:
         line = {
             "metric": args.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -416,10 +429,119 @@ def run_gpu(args, w, world, rank, local):
             "e2e": e2e,
             "clocks": clocks,
             "gpu_launches": 4 * args.steps,
+            "paged_decode": decode,
             "src_digest": src_digest(),
         }
         print(json.dumps(line), flush=True)
     return 0
+
+
+def decode_bytes(w, lens) -> int:
+    """Algorithmic HBM bytes of one paged decode call: every cached K and V row
+    once, the query, the page-table entries in use, the lengths, and the output
+    and LSE written once."""
+    es = 2 if w.dtype == "bf16" else 4
+    n = [int(x) for x in lens]
+    kv = sum(n) * w.Hkv * w.Dh * 2 * es
+    table = sum(-(-x // w.page_size) for x in n) * 4
+    return kv + 2 * w.B * w.Hq * w.Dh * es + w.B * w.Hq * 4 + table + w.B * 4
+
+
+def bench_decode(w, dev, stream, steps, warmup, cpu_budget, P):
+    """Paged decode on one workload: CUDA-event time per call (decode kernel plus
+    the combine kernel) over `steps` calls that alternate between two copies of
+    the pools (each larger than L2)."""
+    import causal_head_attention_gb300 as rca
+
+    q0, kp0, vp0, table0, lens0 = make_paged_inputs(w)
+    q, table, lens = (x.to(dev) for x in (q0, table0, lens0))
+    pools = [(kp0.to(dev), vp0.to(dev))]
+    pools.append(tuple(x.clone() for x in pools[0]))
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    n_ws = rca.rca_paged_decode_workspace_size(w.B, w.Hq, w.Hkv, w.Dh, w.page_size, w.max_pages, q.dtype)
+    ws = torch.empty(n_ws, dtype=torch.uint8, device=dev)
+
+    def call(i):
+        kp, vp = pools[i % 2]
+        rca.rca_paged_decode(q, kp, vp, table, lens, out, lse, ws, stream)
+
+    for i in range(warmup):
+        call(i)
+    torch.cuda.synchronize(dev)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    evs[0].record(stream)
+    for i in range(steps):
+        call(i)
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    rca.rca_stream_status(stream)
+    per = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(steps))
+    ms = sum(per) / steps
+    nbytes = decode_bytes(w, lens0)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+
+    # End to end: query, table and lengths from pinned host memory (the cache
+    # stays resident, as a serving cache does), output and LSE back to the host.
+    hq, ht, hl = (x.pin_memory() for x in (q0, table0, lens0))
+    ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_call(i):
+        q.copy_(hq, non_blocking=True)
+        table.copy_(ht, non_blocking=True)
+        lens.copy_(hl, non_blocking=True)
+        call(i)
+        ho.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    for i in range(2):
+        e2e_call(i)
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(steps):
+        e2e_call(i)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    rca.rca_stream_status(stream)
+    e_ms = a.elapsed_time(b) / steps
+
+    cpu = None
+    if cpu_budget > 0:
+        import numpy as np
+
+        import oracle
+
+        order = np.argsort(-lens0.numpy())  # longest requests first, then as many as the budget allows
+        q64, k64, v64 = (x.double().numpy() for x in (q0, kp0, vp0))
+        t0 = time.perf_counter()
+        done_bytes, nreq = 0, 0
+        for bi in order:
+            one = slice(int(bi), int(bi) + 1)
+            oracle.paged_decode(q64[one], k64, v64, table0.numpy()[one], lens0.numpy()[one])
+            done_bytes += int(lens0[bi]) * w.Hkv * w.Dh * 2 * (2 if w.dtype == "bf16" else 4)
+            nreq += 1
+            if time.perf_counter() - t0 > cpu_budget:
+                break
+        dt = time.perf_counter() - t0
+        cpu = {"value": done_bytes / dt / 1e9, "unit": "GB/s of K/V", "cores": 1, "kind": "oracle",
+               "sample": f"{nreq} of {w.B} requests (longest first), fp64, {dt:.1f} s"}
+
+    return {
+        "workload": w.describe(), "name": w.name, "metric": "paged decode K/V streaming GB/s",
+        "us_per_call": ms * 1e3, "us_min": per[0] * 1e3,
+        "calls_per_s": 1e3 / ms, "tokens_per_s": w.B * 1e3 / ms,
+        "roofline": {"kernel": "decode (+ combine)", "bound": "hbm", "achieved": gbs, "peak": P["hbm_gbs"],
+                     "unit": "GB/s", "frac": gbs / P["hbm_gbs"], "bytes_per_call": nbytes,
+                     "traffic": ncu_traffic("decode", w.name)},
+        "e2e": {"us_per_call": e_ms * 1e3, "h2d_bytes_per_call": sum(x.numel() * x.element_size() for x in (hq, ht, hl)),
+                "d2h_bytes_per_call": ho.numel() * ho.element_size() + hlse.numel() * 4},
+        "l2": "2 rotating pool copies, each larger than L2",
+        "cpu_baseline": cpu,
+        "gpu_launches": 2 * steps,
+    }
 
 
 def main():
@@ -434,6 +556,9 @@ def main():
                     help="warm-up runs at least this long (clock samples under load)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the paged decode measurement")
+    ap.add_argument("--decode-steps", type=int, default=50)
+    ap.add_argument("--decode-cpu-budget", type=float, default=3.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     args.metric = "causal attn fwd+bwd TFLOP/s at B4 H16 T2048 Dh64 BF16; % of GB300 tensor peak"

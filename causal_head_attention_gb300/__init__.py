@@ -1,4 +1,5 @@
-"""GB300 (sm_103a) causal multi-head attention: forward and its VJP.
+"""GB300 (sm_103a) causal multi-head attention: forward and its VJP, and paged
+decode attention (one query token per request over a paged K/V cache).
 
 The computation lives in librca_attn.so (hand-written CUDA, C ABI in
 include/rca_attn.h). This package only allocates outputs with torch and
@@ -19,6 +20,8 @@ from ._native import (  # noqa: F401  (C-ABI names)
     rca_attn_bwd_workspace_size,
     rca_attn_fwd,
     rca_last_error,
+    rca_paged_decode,
+    rca_paged_decode_workspace_size,
     rca_selftest_device_timeout,
     rca_set_wait_timeout_ns,
     rca_stream_status,
@@ -38,6 +41,9 @@ __all__ = [
     "rca_attn_bwd_main",
     "rca_attn_bwd_dq_convert",
     "rca_attn_bwd_noalloc",
+    "paged_decode",
+    "rca_paged_decode",
+    "rca_paged_decode_workspace_size",
     "rca_stream_status",
     "rca_last_error",
     "rca_set_wait_timeout_ns",
@@ -75,6 +81,23 @@ def attention_backward(q, k, v, out, lse, dout, workspace=None, stream=None):
     ws = workspace if workspace is not None else workspace_for(q, k)
     rca_attn_bwd(q, k, v, out, lse, dout.contiguous(), dq, dk, dv, ws, stream)
     return dq, dk, dv
+
+
+def paged_decode(q, k_pool, v_pool, page_table, seq_lens, workspace=None, stream=None):
+    """One decode step: q [B,Hq,Dh] over pools [P,Hkv,page_size,Dh] through
+    page_table [B,max_pages] (int32) for seq_lens [B] (int32) cached positions.
+    Returns (out [B,Hq,Dh] in q's dtype, lse [B,Hq] float32). Inference only."""
+    import torch
+
+    B, Hq, Dh = q.shape
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = rca_paged_decode_workspace_size(B, Hq, k_pool.shape[1], Dh, k_pool.shape[2], page_table.shape[1],
+                                            q.dtype)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    rca_paged_decode(q, k_pool, v_pool, page_table, seq_lens, out, lse, workspace, stream)
+    return out, lse
 
 
 def _autograd_cls():

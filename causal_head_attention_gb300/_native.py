@@ -18,6 +18,7 @@ RCA_ERR_INVALID_ARGUMENT = 1
 RCA_ERR_UNSUPPORTED = 2
 RCA_ERR_CUDA = 3
 RCA_ERR_DEVICE_TIMEOUT = 4
+RCA_ERR_DEVICE_INVALID_INPUT = 5
 RCA_F32_TF32 = 0
 RCA_BF16 = 1
 
@@ -27,6 +28,7 @@ STATUS_NAMES = {
     2: "RCA_ERR_UNSUPPORTED",
     3: "RCA_ERR_CUDA",
     4: "RCA_ERR_DEVICE_TIMEOUT",
+    5: "RCA_ERR_DEVICE_INVALID_INPUT",
 }
 
 # Every symbol include/rca_attn.h declares, with its ctypes signature.
@@ -47,6 +49,9 @@ _SIG = {
                                                ctypes.c_size_t, _P]),
     "rca_attn_bwd_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                             ctypes.c_int, _P]),
+    "rca_paged_decode_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I, ctypes.c_int]),
+    "rca_paged_decode": (ctypes.c_int, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.c_int,
+                                        _P, ctypes.c_size_t, _P]),
     "rca_selftest_device_timeout": (ctypes.c_int, [_P]),
     "rca_stream_status": (ctypes.c_int, [_P]),
     "rca_set_wait_timeout_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
@@ -189,6 +194,37 @@ def rca_attn_bwd_noalloc(q, k, v, out, lse, dout, dq, dk, dv, stream=None):
     B, Hq, Hkv, T, Dh = _shape(q, k)
     _check(lib().rca_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
                                       _ptr(dk), _ptr(dv), B, Hq, Hkv, T, Dh, _dtype_code(q), _stream(stream)))
+
+
+def rca_paged_decode_workspace_size(B, Hq, Hkv, Dh, page_size, max_pages, dt) -> int:
+    """dt: RCA_BF16 / RCA_F32_TF32, or a torch dtype."""
+    if not isinstance(dt, int):
+        torch = _torch()
+        dt = RCA_BF16 if dt == torch.bfloat16 else RCA_F32_TF32
+    return lib().rca_paged_decode_workspace_size(B, Hq, Hkv, Dh, page_size, max_pages, dt)
+
+
+def rca_paged_decode(q, k_pool, v_pool, page_table, seq_lens, out, lse, workspace, stream=None):
+    """q, out [B,Hq,Dh]; k_pool, v_pool [P,Hkv,page_size,Dh]; page_table [B,max_pages]
+    int32; seq_lens [B] int32; lse [B,Hq] float32; workspace a device buffer of at
+    least rca_paged_decode_workspace_size(...) bytes."""
+    torch = _torch()
+    if q.dim() != 3 or k_pool.dim() != 4 or page_table.dim() != 2:
+        raise ValueError("q must be [B,Hq,Dh], the pools [P,Hkv,page_size,Dh], page_table [B,max_pages]")
+    if page_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("page_table and seq_lens must be int32")
+    B, Hq, Dh = q.shape
+    P, Hkv, page_size, _ = k_pool.shape
+    if (tuple(v_pool.shape) != tuple(k_pool.shape) or k_pool.shape[3] != Dh or tuple(out.shape) != (B, Hq, Dh)
+            or tuple(lse.shape) != (B, Hq) or tuple(seq_lens.shape) != (B,) or page_table.shape[0] != B):
+        raise ValueError("inconsistent shapes: q, out [B,Hq,Dh]; k_pool, v_pool [P,Hkv,page_size,Dh]; "
+                         "page_table [B,max_pages]; seq_lens [B]; lse [B,Hq]")
+    if k_pool.dtype != q.dtype or v_pool.dtype != q.dtype or out.dtype != q.dtype or lse.dtype != torch.float32:
+        raise TypeError("q, k_pool, v_pool and out share the storage dtype; lse is float32")
+    _check(lib().rca_paged_decode(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(seq_lens), B, Hq,
+                                  Hkv, Dh, page_size, page_table.shape[1], P, _ptr(out), _ptr(lse),
+                                  _dtype_code(q), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream)))
 
 
 def rca_selftest_device_timeout(stream=None):

@@ -38,19 +38,35 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(s) <= t for s in sources())
 
 
+UNITS = ("rca_attn.cu", "decode.cu")  # translation units, compiled in parallel
+
+
+def _run(cmd, verbose):
+    if verbose:
+        print(" ".join(cmd), file=sys.stderr)
+    return subprocess.run(cmd, capture_output=True, text=True)
+
+
 def build(force: bool = False, verbose: bool = False, extra: tuple = ()) -> str:
     if not force and up_to_date():
         return LIB
-    cmd = [
-        nvcc_path(), ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-        f"-I{INCLUDE}", "-o", LIB + ".tmp", os.path.join(CSRC, "rca_attn.cu"), *extra,
-    ]
-    if verbose:
-        print(" ".join(cmd), file=sys.stderr)
-    r = subprocess.run(cmd, capture_output=True, text=True)
+    from concurrent.futures import ThreadPoolExecutor
+
+    nvcc = nvcc_path()
+    common = [nvcc, ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}", *extra]
+    objs = [os.path.join(PKG, u[:-3] + ".o") for u in UNITS]
+    cmds = [common + ["-c", "-o", o, os.path.join(CSRC, u)] for u, o in zip(UNITS, objs)]
+    with ThreadPoolExecutor(len(cmds)) as ex:
+        results = list(ex.map(lambda c: _run(c, verbose), cmds))
+    for r in results:
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed ({r.returncode}):\n{r.stdout}\n{r.stderr}")
+    r = _run([nvcc, ARCH, "-shared", "-o", LIB + ".tmp", *objs], verbose)
     if r.returncode != 0:
-        raise RuntimeError(f"nvcc failed ({r.returncode}):\n{r.stdout}\n{r.stderr}")
+        raise RuntimeError(f"nvcc link failed ({r.returncode}):\n{r.stdout}\n{r.stderr}")
     os.replace(LIB + ".tmp", LIB)
+    for o in objs:
+        os.remove(o)
     return LIB
 
 

@@ -13,6 +13,7 @@
 
 #include "rca_attn.h"
 #include "bwd.cuh"
+#include "decode.h"
 #include "fwd.cuh"
 
 namespace rca {
@@ -221,6 +222,53 @@ rca_status check_ws(const void* ws, size_t bytes, const WsLayout& L) {
   if (bytes < L.total)
     return fail(RCA_ERR_INVALID_ARGUMENT, "workspace too small: %zu bytes given, %zu needed", bytes, L.total);
   return RCA_OK;
+}
+
+rca_status check_decode_shape(int64_t B, int64_t Hq, int64_t Hkv, int64_t Dh, int64_t page_size,
+                              int64_t max_pages, int64_t num_pages, rca_dtype dt) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || max_pages < 1 || num_pages < 1)
+    return fail(RCA_ERR_INVALID_ARGUMENT,
+                "B, Hq, Hkv, max_pages and num_pages must be >= 1 (got B=%lld Hq=%lld Hkv=%lld max_pages=%lld "
+                "num_pages=%lld)",
+                (long long)B, (long long)Hq, (long long)Hkv, (long long)max_pages, (long long)num_pages);
+  if (Hq % Hkv != 0)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "grouped-query attention needs Hq %% Hkv == 0 (Hq=%lld Hkv=%lld)",
+                (long long)Hq, (long long)Hkv);
+  if (dt != RCA_BF16 && dt != RCA_F32_TF32) return fail(RCA_ERR_INVALID_ARGUMENT, "unknown dtype %d", (int)dt);
+  if (Dh != 16 && Dh != 32 && Dh != 64 && Dh != 128)
+    return fail(RCA_ERR_UNSUPPORTED, "head width Dh=%lld is not supported (supported: 16, 32, 64, 128)",
+                (long long)Dh);
+  if (page_size < 1 || page_size > 65536 || (page_size & (page_size - 1)) != 0)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "page_size must be a power of two in [1, 65536] (got %lld)",
+                (long long)page_size);
+  if (B > rca::kDecodeMaxBatch)
+    return fail(RCA_ERR_UNSUPPORTED, "paged decode takes at most %lld requests per call (got B=%lld)",
+                (long long)rca::kDecodeMaxBatch, (long long)B);
+  if (max_pages > (int64_t(1) << 30) / page_size)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "max_pages * page_size must be <= 2^30");
+  if (num_pages > 0x7fffffffLL || Hq > 65536 ||
+      B * rca::decode_max_chunks(page_size, max_pages) * Hq > 0x7fffffffLL)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "paged decode problem too large");
+  return RCA_OK;
+}
+
+struct DecodeWs {
+  size_t ml_off, acc_off, total;
+};
+
+// Per (request, query head, chunk): (max, sum) and the unnormalised output row.
+// Used only when a request can span more than one chunk; never less than 256
+// bytes so that a valid size is never 0.
+DecodeWs decode_ws_layout(int64_t B, int64_t Hq, int64_t Dh, int64_t page_size, int64_t max_pages) {
+  DecodeWs w{};
+  w.total = 256;
+  const int64_t maxch = rca::decode_max_chunks(page_size, max_pages);
+  if (maxch <= 1) return w;
+  const size_t rows = size_t(B) * Hq * maxch;
+  w.ml_off = 0;
+  w.acc_off = round256(rows * 2 * 4);
+  w.total = w.acc_off + round256(rows * Dh * 4);
+  return w;
 }
 
 #define RCA_CHECK(x)              \
@@ -560,6 +608,69 @@ rca_status rca_attn_bwd(const void* q, const void* k, const void* v, const void*
   RCA_GUARD_END
 }
 
+size_t rca_paged_decode_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t Dh, int64_t page_size,
+                                       int64_t max_pages, rca_dtype dt) {
+  try {
+    if (check_decode_shape(B, Hq, Hkv, Dh, page_size, max_pages, 1, dt) != RCA_OK) return 0;
+    return decode_ws_layout(B, Hq, Dh, page_size, max_pages).total;
+  } catch (...) {
+    return 0;
+  }
+}
+
+rca_status rca_paged_decode(const void* q, const void* k_pool, const void* v_pool, const int32_t* page_table,
+                            const int32_t* seq_lens, int64_t B, int64_t Hq, int64_t Hkv, int64_t Dh,
+                            int64_t page_size, int64_t max_pages, int64_t num_pages, void* out, float* lse,
+                            rca_dtype dt, void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  RCA_GUARD_BEGIN
+  g_err.clear();
+  if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !out || !lse)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_paged_decode: null pointer");
+  RCA_CHECK(check_decode_shape(B, Hq, Hkv, Dh, page_size, max_pages, num_pages, dt));
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_paged_decode: q, k_pool and v_pool must be 16-byte aligned");
+  const auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  const uintptr_t out_mis = reinterpret_cast<uintptr_t>(out) & (dt == RCA_F32_TF32 ? 3u : 1u);
+  if (!a4(page_table) || !a4(seq_lens) || !a4(lse) || out_mis)
+    return fail(RCA_ERR_INVALID_ARGUMENT,
+                "rca_paged_decode: page_table, seq_lens and lse must be 4-byte aligned, out aligned to its element");
+  const DecodeWs L = decode_ws_layout(B, Hq, Dh, page_size, max_pages);
+  if (!workspace) return fail(RCA_ERR_INVALID_ARGUMENT, "rca_paged_decode: workspace is null");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_paged_decode: workspace must be 256-byte aligned");
+  if (workspace_bytes < L.total)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_paged_decode: workspace too small: %zu bytes given, %zu needed",
+                workspace_bytes, L.total);
+  int* status = nullptr;
+  RCA_CHECK(status_word(&status));
+  int sms = 0;
+  RCA_CHECK(sm_count(&sms));
+  rca::DecodeParams p{};
+  p.q = q;
+  p.k_pool = k_pool;
+  p.v_pool = v_pool;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.lse = lse;
+  p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.ml_off);
+  p.part_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.acc_off);
+  p.status = status;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Dh = Dh;
+  p.page_size = page_size;
+  p.max_pages = max_pages;
+  p.num_pages = num_pages;
+  p.bf16 = dt == RCA_BF16;
+  p.sms = sms;
+  cudaError_t e = rca::launch_paged_decode(p, static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launch paged decode");
+  return RCA_OK;
+  RCA_GUARD_END
+}
+
 rca_status rca_selftest_device_timeout(void* cuda_stream) {
   RCA_GUARD_BEGIN
   g_err.clear();
@@ -587,6 +698,10 @@ rca_status rca_stream_status(void* cuda_stream) {
   if (h != 0) {
     cudaMemset(status, 0, sizeof(int));
     cudaDeviceSynchronize();
+    if (h == rca::kStatusBadInput)
+      return fail(RCA_ERR_DEVICE_INVALID_INPUT,
+                  "a kernel read an invalid device-side input (a page ID outside [0, num_pages) or a "
+                  "length outside [1, max_pages * page_size]); the affected results are invalid");
     return fail(RCA_ERR_DEVICE_TIMEOUT, "a device-side wait exceeded its time limit (status %d); outputs are invalid", h);
   }
   return RCA_OK;

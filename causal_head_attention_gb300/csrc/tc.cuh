@@ -11,6 +11,8 @@ namespace rca {
 
 // Status values written by kernels into the library's device status word.
 constexpr int kStatusTimeout = 4;
+// A kernel read an invalid device-side input (a page ID or a length).
+constexpr int kStatusBadInput = 5;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -71,14 +71,15 @@ typedef enum {
   RCA_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad size, Hq % Hkv != 0, misalignment, small workspace */
   RCA_ERR_UNSUPPORTED = 2,      /* valid request this build does not implement (e.g. Dh = 96) */
   RCA_ERR_CUDA = 3,             /* a CUDA runtime/driver call failed; message holds the CUDA error text */
-  RCA_ERR_DEVICE_TIMEOUT = 4    /* a device-side wait exceeded its time limit; outputs are invalid */
+  RCA_ERR_DEVICE_TIMEOUT = 4,   /* a device-side wait exceeded its time limit; outputs are invalid */
+  RCA_ERR_DEVICE_INVALID_INPUT = 5 /* a kernel read an invalid device-side input (page ID, length) */
 } rca_status;
 
 /* Storage dtype of q/k/v/out/dout/dq/dk/dv; selects the tensor-core operand type. */
 typedef enum { RCA_F32_TF32 = 0, RCA_BF16 = 1 } rca_dtype;
 
-/* ABI version: upper 16 bits major, lower 16 bits minor (0x00010000 = 1.0). */
-#define RCA_ABI_VERSION 0x00010000u
+/* ABI version: upper 16 bits major, lower 16 bits minor (0x00010001 = 1.1). */
+#define RCA_ABI_VERSION 0x00010001u
 uint32_t rca_abi_version(void);
 
 /* Message of the last failed call on this thread ("" if none). The pointer is
@@ -167,9 +168,65 @@ rca_status rca_attn_bwd_noalloc(const void* q, const void* k, const void* v, con
                                 rca_dtype dt, void* cuda_stream);
 
 /*
+ * Paged decode attention ("Execution Backends and the Python ABI",
+ * docs/internals/backends_and_python.html, section "Incremental attention"):
+ * one new query token per request attends over every position the request has
+ * cached, each key and value fetched through the request's page table. Query
+ * and output are [H, d_h] per request; the key and value pools are
+ * [physical_page, H, page_offset, d_h]; a request-local table maps logical page
+ * j (positions j*page_size .. j*page_size + page_size - 1) to a physical page
+ * ID. The operation is inference-only: it has no backward.
+ *
+ * Per request b (length L = seq_lens[b]) and query head h, with KV head
+ * kv = h / (Hq/Hkv) and K[t] = k_pool[page_table[b][t / page_size], kv,
+ * t % page_size, :] (likewise V):
+ *   s_t    = scale * q[b,h,:] . K[t],   t = 0 .. L-1,  scale = 1/sqrt(Dh)
+ *   lse[b,h] = ln sum_t exp(s_t)                       (natural log, fp32)
+ *   out[b,h,:] = sum_t exp(s_t - lse[b,h]) V[t]
+ * The new token's own key and value must already be in the cache (position
+ * L-1), so every request attends to at least one position.
+ *
+ * Layouts (contiguous, row-major):
+ *   q, out            : [B, Hq, Dh]                          storage dtype
+ *   k_pool, v_pool    : [num_pages, Hkv, page_size, Dh]      storage dtype
+ *   page_table        : [B, max_pages] int32 physical page IDs (entries past a
+ *                       request's last page are never read)
+ *   seq_lens          : [B] int32
+ *   lse               : [B, Hq] float32
+ * RCA_BF16: bfloat16 storage; RCA_F32_TF32: float32 storage. Both compute in
+ * fp32 on the CUDA cores (no tensor-core rounding). Dh in {16, 32, 64, 128};
+ * page_size a power of two in [1, 65536]; 1 <= B <= 8192;
+ * max_pages * page_size <= 2^30. q, k_pool and v_pool 16-byte aligned,
+ * page_table, seq_lens and lse 4-byte aligned.
+ *
+ * Device-side inputs (page_table, seq_lens) are checked by the kernels as they
+ * read them: a page ID outside [0, num_pages) is never dereferenced and a length
+ * outside [1, max_pages * page_size] makes that request's out and lse NaN; both
+ * record RCA_ERR_DEVICE_INVALID_INPUT for rca_stream_status(). Other requests'
+ * results are unaffected by a bad length; a bad page ID leaves its request's
+ * results invalid.
+ *
+ * workspace: caller-owned device memory of at least
+ * rca_paged_decode_workspace_size(...) bytes (>= 256 for valid sizes, 0 for
+ * invalid ones), 256-byte aligned: fp32 partial results of requests longer than
+ * 256 positions; contents on entry do not matter. All pointers are device
+ * pointers owned by the caller; the call validates its host arguments (nothing
+ * is enqueued on failure) and then only enqueues work on cuda_stream.
+ */
+size_t rca_paged_decode_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t Dh,
+                                       int64_t page_size, int64_t max_pages, rca_dtype dt);
+rca_status rca_paged_decode(const void* q, const void* k_pool, const void* v_pool,
+                            const int32_t* page_table, const int32_t* seq_lens,
+                            int64_t B, int64_t Hq, int64_t Hkv, int64_t Dh,
+                            int64_t page_size, int64_t max_pages, int64_t num_pages,
+                            void* out, float* lse, rca_dtype dt,
+                            void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/*
  * Synchronises cuda_stream, then reports (and clears) an asynchronous CUDA
- * error or a device-side timeout recorded by a kernel of this library on the
- * current device. RCA_OK if neither happened.
+ * error, a device-side timeout (RCA_ERR_DEVICE_TIMEOUT) or an invalid
+ * device-side input (RCA_ERR_DEVICE_INVALID_INPUT) recorded by a kernel of this
+ * library on the current device. RCA_OK if none happened.
  */
 rca_status rca_stream_status(void* cuda_stream);
 

@@ -109,3 +109,45 @@ def test_error_text_is_per_thread(lib):
 def test_timeout_setter(lib):
     old = lib.rca_set_wait_timeout_ns(5)
     assert lib.rca_set_wait_timeout_ns(old) == 1000000
+
+
+def decode(lib, q=FAKE, B=2, Hq=4, Hkv=2, Dh=64, page_size=16, max_pages=8, num_pages=20, dt=1, out=FAKE,
+           lse=FAKE, ws=ctypes.c_void_p(1 << 20), ws_bytes=1 << 30, table=FAKE):
+    return lib.rca_paged_decode(q, FAKE, FAKE, table, FAKE, B, Hq, Hkv, Dh, page_size, max_pages, num_pages,
+                                out, lse, dt, ws, ws_bytes, NULL)
+
+
+@pytest.mark.parametrize(
+    "kw,status,needle",
+    [
+        (dict(q=NULL), 1, "null"),
+        (dict(table=NULL), 1, "null"),
+        (dict(B=0), 1, ">= 1"),
+        (dict(num_pages=0), 1, ">= 1"),
+        (dict(Hq=3, Hkv=2), 1, "Hq % Hkv"),
+        (dict(Dh=96), 2, "Dh=96"),
+        (dict(page_size=12), 1, "power of two"),
+        (dict(page_size=1 << 17), 1, "power of two"),
+        (dict(B=8193), 2, "at most"),
+        (dict(max_pages=1 << 27), 1, "2^30"),
+        (dict(dt=7), 1, "dtype"),
+        (dict(q=ctypes.c_void_p(4104)), 1, "16-byte"),
+        (dict(lse=ctypes.c_void_p(4098)), 1, "4-byte"),
+        (dict(ws=NULL), 1, "workspace is null"),
+        (dict(ws=ctypes.c_void_p(4096 + 128)), 1, "256-byte"),
+        (dict(ws_bytes=64), 1, "too small"),
+    ],
+)
+def test_decode_validation(lib, kw, status, needle):
+    assert decode(lib, **kw) == status
+    assert needle in lib.rca_last_error().decode()
+
+
+def test_decode_workspace_size(lib):
+    # one chunk of 256 positions per request at most: no partials, minimum size
+    assert lib.rca_paged_decode_workspace_size(4, 8, 8, 64, 16, 16, 1) == 256
+    # B * Hq * chunks rows of (max, sum) and Dh floats
+    n = lib.rca_paged_decode_workspace_size(64, 16, 16, 64, 16, 128, 1)
+    assert n >= 64 * 16 * 8 * (64 + 2) * 4
+    assert lib.rca_paged_decode_workspace_size(4, 8, 8, 96, 16, 16, 1) == 0
+    assert lib.rca_paged_decode_workspace_size(4, 8, 8, 64, 12, 16, 1) == 0
