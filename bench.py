@@ -62,10 +62,23 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def src_digest() -> str:
+# Source files each profiled kernel is built from (its device code, the shared
+# device helpers and its host launcher).
+KERNEL_SOURCES = {
+    "fwd": ("fwd.cuh", "tc.cuh", "rca_attn.cu"),
+    "bwd_main": ("bwd.cuh", "tc.cuh", "rca_attn.cu"),
+    "bwd_preprocess": ("bwd.cuh", "tc.cuh", "rca_attn.cu"),
+    "bwd_dq_convert": ("bwd.cuh", "tc.cuh", "rca_attn.cu"),
+    "decode": ("decode.cu", "decode.h", "tc.cuh"),
+}
+
+
+def src_digest(kernel: str | None = None) -> str:
+    """Digest of the kernel sources (all of csrc/, or those `kernel` is built from)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "causal_head_attention_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    names = sorted(os.listdir(csrc)) if kernel is None else sorted(KERNEL_SOURCES[kernel])
+    for f in names:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode())
             h.update(fh.read())
@@ -74,14 +87,14 @@ def src_digest() -> str:
 
 def ncu_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
+    the current sources of that kernel; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(workload, {}).get(kernel)
-    if not e or e.get("src_digest") != src_digest():
+    if not e or e.get("src_digest") != src_digest(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 

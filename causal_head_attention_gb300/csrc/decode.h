@@ -11,7 +11,10 @@ namespace rca {
 // request of length L yields ceil(L / kDecodeChunk) items per KV head group;
 // requests with one item write their output directly, longer ones leave one
 // partial (max, sum, unnormalised output) per item for the combine kernel.
-constexpr int kDecodeChunk = 256;
+#ifndef DEC_CHUNK
+#define DEC_CHUNK 256
+#endif
+constexpr int kDecodeChunk = DEC_CHUNK;
 
 // Largest request count the decode kernel accepts: each CTA keeps the prefix
 // sums of the per-request item counts in shared memory (4 bytes a request).
@@ -31,6 +34,7 @@ struct DecodeParams {
   int64_t B, Hq, Hkv, Dh, page_size, max_pages, num_pages;
   bool bf16;
   int sms;
+  unsigned long long timeout_ns;  // device-side wait limit
 };
 
 inline int64_t decode_max_chunks(int64_t page_size, int64_t max_pages) {

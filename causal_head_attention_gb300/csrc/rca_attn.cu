@@ -665,6 +665,7 @@ rca_status rca_paged_decode(const void* q, const void* k_pool, const void* v_poo
   p.num_pages = num_pages;
   p.bf16 = dt == RCA_BF16;
   p.sms = sms;
+  p.timeout_ns = g_timeout_ns.load();
   cudaError_t e = rca::launch_paged_decode(p, static_cast<cudaStream_t>(cuda_stream));
   if (e != cudaSuccess) return cuda_fail(e, "launch paged decode");
   return RCA_OK;
