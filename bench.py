@@ -418,6 +418,10 @@ def run_gpu(args, w, world, rank, local):
                "sample": f"{n} of {w.B * w.Hkv} (batch, KV-head) groups of the same workload, fwd+bwd, fp64, "
                          f"{dt:.1f} s"}
 
+    mat = None
+    if rank == 0 and not args.no_materialized and w.B * w.Hq * w.T * w.T * 4 <= 2 ** 31:
+        mat = bench_materialized(w, dev, stream, max(3, args.steps // 5), 2, P)
+
     decode = None
     if rank == 0 and not args.no_decode:
         decode = [bench_decode(dw, dev, stream, args.decode_steps, 5,
@@ -443,10 +447,73 @@ def run_gpu(args, w, world, rank, local):
             "clocks": clocks,
             "gpu_launches": 4 * args.steps,
             "paged_decode": decode,
+            "materialized": mat,
             "src_digest": src_digest(),
         }
         print(json.dumps(line), flush=True)
     return 0
+
+
+def bench_materialized(w, dev, stream, steps, warmup, P):
+    """Materialized path on one workload: CUDA-event time of rca_attn_materialized_fwd
+    and _bwd (probabilities kept, dprobs = None), and of the fused causal softmax
+    and its VJP alone on [B*Hq, T, T] fp32 rows (HBM-bound; bytes below)."""
+    import causal_head_attention_gb300 as rca
+
+    q0, k0, v0, do0 = make_inputs(w)
+    q, k, v, do = (x.to(dev) for x in (q0, k0, v0, do0))
+    out = torch.empty_like(q)
+    E, T = w.B * w.Hq, w.T
+    probs = torch.empty((w.B, w.Hq, T, T), dtype=torch.float32, device=dev)
+    lse = torch.empty((w.B, w.Hq, T), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(rca.rca_attn_materialized_workspace_size(w.B, w.Hq, w.Hkv, T, w.Dh, q.dtype),
+                     dtype=torch.uint8, device=dev)
+
+    def timed(fn, n):
+        for i in range(warmup):
+            fn(i)
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(n):
+            fn(i)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        rca.rca_stream_status(stream)
+        return a.elapsed_time(b) / n
+
+    fwd_ms = timed(lambda i: rca.rca_attn_materialized_fwd(q, k, v, out, probs, lse, ws, stream), steps)
+    bwd_ms = timed(lambda i: rca.rca_attn_materialized_bwd(q, k, v, probs, do, None, dq, dk, dv, ws, stream), steps)
+    # The softmax and its VJP alone, on two row buffers each larger than L2.
+    scale = 1.0 / (w.Dh ** 0.5)
+    s = [torch.randn((E, T, T), device=dev) for _ in range(2)]
+    g = [torch.randn((E, T, T), device=dev) for _ in range(2)]
+    lse2 = torch.empty((E, T), device=dev)
+    sm_ms = timed(lambda i: rca.rca_causal_softmax(s[i % 2], lse2, scale, stream), steps)
+    smb_ms = timed(lambda i: rca.rca_causal_softmax_bwd(s[i % 2], g[i % 2], None, scale, stream), steps)
+    tri = E * T * (T + 1) // 2 * 4  # bytes of the kept (lower) half of the rows
+    full = E * T * T * 4
+    sm_bytes = tri + full + E * T * 4       # read the kept entries, write whole rows and LSE
+    smb_bytes = 2 * tri + full              # read P and dP where kept, write whole rows
+    gemm_flops = 2.0 * E * T * T * w.Dh * (2 + 4)  # full-square products: 2 forward, 4 backward
+
+    def roof(nbytes, ms):
+        a = nbytes / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": a, "peak": P["hbm_gbs"], "unit": "GB/s", "frac": a / P["hbm_gbs"],
+                "bytes_per_launch": nbytes, "us": ms * 1e3}
+
+    return {
+        "workload": w.describe(), "name": w.name, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+        "probs_bytes": full,
+        "gemm_tflops_incl_softmax": gemm_flops / ((fwd_ms + bwd_ms) * 1e-3) / 1e12,
+        "causal_softmax": roof(sm_bytes, sm_ms), "causal_softmax_bwd": roof(smb_bytes, smb_ms),
+        "note": "GEMMs in cuBLAS (full T x T squares, masked half included); the softmax kernels are this library's",
+        "gpu_launches": {"own_kernels_per_fwd": 4 if w.dtype == "bf16" else 2,
+                         "own_kernels_per_bwd": 8 if w.dtype == "bf16" else 4,
+                         "cublas_gemms_per_fwd": 2, "cublas_gemms_per_bwd": 4},
+    }
 
 
 def decode_bytes(w, lens) -> int:
@@ -570,6 +637,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the paged decode measurement")
+    ap.add_argument("--no-materialized", action="store_true", help="skip the materialized-path measurement")
     ap.add_argument("--decode-steps", type=int, default=50)
     ap.add_argument("--decode-cpu-budget", type=float, default=3.0)
     args = ap.parse_args()

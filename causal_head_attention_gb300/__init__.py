@@ -19,6 +19,11 @@ from ._native import (  # noqa: F401  (C-ABI names)
     rca_attn_bwd_preprocess,
     rca_attn_bwd_workspace_size,
     rca_attn_fwd,
+    rca_attn_materialized_bwd,
+    rca_attn_materialized_fwd,
+    rca_attn_materialized_workspace_size,
+    rca_causal_softmax,
+    rca_causal_softmax_bwd,
     rca_last_error,
     rca_paged_decode,
     rca_paged_decode_workspace_size,
@@ -41,6 +46,13 @@ __all__ = [
     "rca_attn_bwd_main",
     "rca_attn_bwd_dq_convert",
     "rca_attn_bwd_noalloc",
+    "materialized_forward",
+    "materialized_backward",
+    "rca_attn_materialized_fwd",
+    "rca_attn_materialized_bwd",
+    "rca_attn_materialized_workspace_size",
+    "rca_causal_softmax",
+    "rca_causal_softmax_bwd",
     "paged_decode",
     "rca_paged_decode",
     "rca_paged_decode_workspace_size",
@@ -80,6 +92,40 @@ def attention_backward(q, k, v, out, lse, dout, workspace=None, stream=None):
     dv = torch.empty_like(v)
     ws = workspace if workspace is not None else workspace_for(q, k)
     rca_attn_bwd(q, k, v, out, lse, dout.contiguous(), dq, dk, dv, ws, stream)
+    return dq, dk, dv
+
+
+def materialized_workspace_for(q, k):
+    import torch
+
+    B, T, Hq, Dh = q.shape
+    n = rca_attn_materialized_workspace_size(B, Hq, k.shape[2], T, Dh, q.dtype)
+    return torch.empty(n, dtype=torch.uint8, device=q.device)
+
+
+def materialized_forward(q, k, v, workspace=None, stream=None):
+    """Materialized path / probability-returning diagnostic. Returns (out
+    [B,T,Hq,Dh] in q's dtype, probs [B,Hq,T,T] float32, lse [B,Hq,T] float32)."""
+    import torch
+
+    B, T, Hq, Dh = q.shape
+    out = torch.empty_like(q)
+    probs = torch.empty((B, Hq, T, T), dtype=torch.float32, device=q.device)
+    lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    ws = workspace if workspace is not None else materialized_workspace_for(q, k)
+    rca_attn_materialized_fwd(q, k, v, out, probs, lse, ws, stream)
+    return out, probs, lse
+
+
+def materialized_backward(q, k, v, probs, dout, dprobs=None, workspace=None, stream=None):
+    """VJP of (out, probs) from the stored probabilities. Returns (dq, dk, dv)."""
+    import torch
+
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    ws = workspace if workspace is not None else materialized_workspace_for(q, k)
+    rca_attn_materialized_bwd(q, k, v, probs, dout.contiguous(), dprobs, dq, dk, dv, ws, stream)
     return dq, dk, dv
 
 

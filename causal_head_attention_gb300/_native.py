@@ -52,6 +52,13 @@ _SIG = {
     "rca_paged_decode_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I, ctypes.c_int]),
     "rca_paged_decode": (ctypes.c_int, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.c_int,
                                         _P, ctypes.c_size_t, _P]),
+    "rca_attn_materialized_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I, _I, ctypes.c_int]),
+    "rca_attn_materialized_fwd": (ctypes.c_int, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, ctypes.c_int, _P,
+                                                 ctypes.c_size_t, _P]),
+    "rca_attn_materialized_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                                 ctypes.c_int, _P, ctypes.c_size_t, _P]),
+    "rca_causal_softmax": (ctypes.c_int, [_P, _P, _I, _I, ctypes.c_float, _P]),
+    "rca_causal_softmax_bwd": (ctypes.c_int, [_P, _P, _P, _I, _I, ctypes.c_float, _P]),
     "rca_selftest_device_timeout": (ctypes.c_int, [_P]),
     "rca_stream_status": (ctypes.c_int, [_P]),
     "rca_set_wait_timeout_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
@@ -225,6 +232,54 @@ def rca_paged_decode(q, k_pool, v_pool, page_table, seq_lens, out, lse, workspac
                                   Hkv, Dh, page_size, page_table.shape[1], P, _ptr(out), _ptr(lse),
                                   _dtype_code(q), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                   _stream(stream)))
+
+
+def rca_attn_materialized_workspace_size(B, Hq, Hkv, T, Dh, dt) -> int:
+    """dt: RCA_BF16 / RCA_F32_TF32, or a torch dtype."""
+    if not isinstance(dt, int):
+        torch = _torch()
+        dt = RCA_BF16 if dt == torch.bfloat16 else RCA_F32_TF32
+    return lib().rca_attn_materialized_workspace_size(B, Hq, Hkv, T, Dh, dt)
+
+
+def _check_probs(probs, B, Hq, T, name="probs"):
+    torch = _torch()
+    if probs.dtype != torch.float32 or tuple(probs.shape) != (B, Hq, T, T):
+        raise ValueError(f"{name} must be float32 [B,Hq,T,T] = {(B, Hq, T, T)}")
+
+
+def rca_attn_materialized_fwd(q, k, v, out, probs, lse, workspace, stream=None):
+    B, Hq, Hkv, T, Dh = _shape(q, k)
+    _check_probs(probs, B, Hq, T)
+    _check(lib().rca_attn_materialized_fwd(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, T, Dh, _ptr(out), _ptr(probs),
+                                           _ptr(lse), _dtype_code(q), _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def rca_attn_materialized_bwd(q, k, v, probs, dout, dprobs, dq, dk, dv, workspace, stream=None):
+    B, Hq, Hkv, T, Dh = _shape(q, k)
+    _check_probs(probs, B, Hq, T)
+    if dprobs is not None:
+        _check_probs(dprobs, B, Hq, T, "dprobs")
+    _check(lib().rca_attn_materialized_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(probs), _ptr(dout), _ptr(dprobs),
+                                           _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, T, Dh, _dtype_code(q),
+                                           _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                           _stream(stream)))
+
+
+def rca_causal_softmax(scores, lse, scale, stream=None):
+    """In place on scores [N,T,T] float32 (any leading dims); lse [N,T] float32."""
+    T = scores.shape[-1]
+    N = scores.numel() // (T * T)
+    _check(lib().rca_causal_softmax(_ptr(scores), _ptr(lse), N, T, float(scale), _stream(stream)))
+
+
+def rca_causal_softmax_bwd(probs, grad, grad_extra, scale, stream=None):
+    """In place on grad [N,T,T] float32; grad_extra may be None."""
+    T = probs.shape[-1]
+    N = probs.numel() // (T * T)
+    _check(lib().rca_causal_softmax_bwd(_ptr(probs), _ptr(grad), _ptr(grad_extra), N, T, float(scale),
+                                        _stream(stream)))
 
 
 def rca_selftest_device_timeout(stream=None):

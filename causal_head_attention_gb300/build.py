@@ -38,7 +38,7 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(s) <= t for s in sources())
 
 
-UNITS = ("rca_attn.cu", "decode.cu")  # translation units, compiled in parallel
+UNITS = ("rca_attn.cu", "decode.cu", "materialized.cu")  # translation units, compiled in parallel
 
 
 def _run(cmd, verbose):
@@ -61,7 +61,7 @@ def build(force: bool = False, verbose: bool = False, extra: tuple = ()) -> str:
     for r in results:
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed ({r.returncode}):\n{r.stdout}\n{r.stderr}")
-    r = _run([nvcc, ARCH, "-shared", "-o", LIB + ".tmp", *objs], verbose)
+    r = _run([nvcc, ARCH, "-shared", "-o", LIB + ".tmp", *objs, "-lcublas"], verbose)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed ({r.returncode}):\n{r.stdout}\n{r.stderr}")
     os.replace(LIB + ".tmp", LIB)

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -15,6 +16,7 @@
 #include "bwd.cuh"
 #include "decode.h"
 #include "fwd.cuh"
+#include "materialized.h"
 
 namespace rca {
 // Failure-detection self-test: one warp waits, with the same time-bounded wait
@@ -668,6 +670,160 @@ rca_status rca_paged_decode(const void* q, const void* k_pool, const void* v_poo
   p.timeout_ns = g_timeout_ns.load();
   cudaError_t e = rca::launch_paged_decode(p, static_cast<cudaStream_t>(cuda_stream));
   if (e != cudaSuccess) return cuda_fail(e, "launch paged decode");
+  return RCA_OK;
+  RCA_GUARD_END
+}
+
+// ---------------------------------------------------------------------------
+// Materialized path (probabilities returned and kept for the VJP)
+// ---------------------------------------------------------------------------
+static rca_status check_mat_shape(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt) {
+  if (B < 1 || Hq < 1 || Hkv < 1)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "B, Hq and Hkv must be >= 1 (got B=%lld Hq=%lld Hkv=%lld)",
+                (long long)B, (long long)Hq, (long long)Hkv);
+  if (T < 1)
+    return fail(RCA_ERR_INVALID_ARGUMENT,
+                "T must be >= 1 (got %lld): an empty causal row is a fully masked softmax slice", (long long)T);
+  if (Hq % Hkv != 0)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "grouped-query attention needs Hq %% Hkv == 0 (Hq=%lld Hkv=%lld)",
+                (long long)Hq, (long long)Hkv);
+  if (dt != RCA_BF16 && dt != RCA_F32_TF32) return fail(RCA_ERR_INVALID_ARGUMENT, "unknown dtype %d", (int)dt);
+  if (Dh != 16 && Dh != 32 && Dh != 64 && Dh != 128)
+    return fail(RCA_ERR_UNSUPPORTED, "head width Dh=%lld is not supported (supported: 16, 32, 64, 128)",
+                (long long)Dh);
+  if (T > 65536 || B * Hq > 0x7fffffffLL || double(B) * Hq * T * T > double(int64_t(1) << 37))
+    return fail(RCA_ERR_INVALID_ARGUMENT,
+                "materialized attention too large: the probabilities [B,Hq,T,T] need %.1f GB (B=%lld Hq=%lld T=%lld)",
+                4.0 * double(B) * Hq * T * T / 1e9, (long long)B, (long long)Hq, (long long)T);
+  return RCA_OK;
+}
+
+size_t rca_attn_materialized_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
+                                            rca_dtype dt) {
+  try {
+    if (check_mat_shape(B, Hq, Hkv, T, Dh, dt) != RCA_OK) return 0;
+    return rca::materialized_workspace_size(B, Hq, Hkv, T, Dh, dt == RCA_BF16);
+  } catch (...) {
+    return 0;
+  }
+}
+
+static rca_status check_mat_ws(const void* ws, size_t bytes, int64_t B, int64_t Hq, int64_t Hkv, int64_t T,
+                               int64_t Dh, rca_dtype dt) {
+  const size_t need = rca::materialized_workspace_size(B, Hq, Hkv, T, Dh, dt == RCA_BF16);
+  if (!ws) return fail(RCA_ERR_INVALID_ARGUMENT, "workspace is null");
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return fail(RCA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
+  if (bytes < need)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "workspace too small: %zu bytes given, %zu needed", bytes, need);
+  return RCA_OK;
+}
+
+rca_status rca_attn_materialized_fwd(const void* q, const void* k, const void* v, int64_t B, int64_t Hq,
+                                     int64_t Hkv, int64_t T, int64_t Dh, void* out, float* probs, float* lse,
+                                     rca_dtype dt, void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  RCA_GUARD_BEGIN
+  g_err.clear();
+  if (!q || !k || !v || !out || !probs || !lse)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_materialized_fwd: null pointer");
+  RCA_CHECK(check_mat_shape(B, Hq, Hkv, T, Dh, dt));
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(probs) || !aligned16(lse))
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_materialized_fwd: tensors must be 16-byte aligned");
+  RCA_CHECK(check_mat_ws(workspace, workspace_bytes, B, Hq, Hkv, T, Dh, dt));
+  rca::MatParams p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.probs = probs;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.T = T;
+  p.Dh = Dh;
+  p.bf16 = dt == RCA_BF16;
+  p.workspace = workspace;
+  p.workspace_bytes = workspace_bytes;
+  std::string err;
+  if (!rca::materialized_fwd(p, static_cast<cudaStream_t>(cuda_stream), err))
+    return fail(RCA_ERR_CUDA, "rca_attn_materialized_fwd: %s", err.c_str());
+  return RCA_OK;
+  RCA_GUARD_END
+}
+
+rca_status rca_attn_materialized_bwd(const void* q, const void* k, const void* v, const float* probs,
+                                     const void* dout, const float* dprobs, void* dq, void* dk, void* dv, int64_t B,
+                                     int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt, void* workspace,
+                                     size_t workspace_bytes, void* cuda_stream) {
+  RCA_GUARD_BEGIN
+  g_err.clear();
+  if (!q || !k || !v || !probs || !dout || !dq || !dk || !dv)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_materialized_bwd: null pointer");
+  RCA_CHECK(check_mat_shape(B, Hq, Hkv, T, Dh, dt));
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(probs) || !aligned16(dout) ||
+      (dprobs && !aligned16(dprobs)) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_materialized_bwd: tensors must be 16-byte aligned");
+  RCA_CHECK(check_mat_ws(workspace, workspace_bytes, B, Hq, Hkv, T, Dh, dt));
+  rca::MatParams p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.probs = const_cast<float*>(probs);
+  p.dout = dout;
+  p.dprobs = dprobs;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.T = T;
+  p.Dh = Dh;
+  p.bf16 = dt == RCA_BF16;
+  p.workspace = workspace;
+  p.workspace_bytes = workspace_bytes;
+  std::string err;
+  if (!rca::materialized_bwd(p, static_cast<cudaStream_t>(cuda_stream), err))
+    return fail(RCA_ERR_CUDA, "rca_attn_materialized_bwd: %s", err.c_str());
+  return RCA_OK;
+  RCA_GUARD_END
+}
+
+static rca_status check_softmax_args(int64_t N, int64_t T, float scale) {
+  if (N < 1 || T < 1)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "N and T must be >= 1 (got N=%lld T=%lld)", (long long)N, (long long)T);
+  if (T > 65536 || double(N) * T * T > double(int64_t(1) << 37))
+    return fail(RCA_ERR_INVALID_ARGUMENT, "causal softmax too large (N=%lld T=%lld)", (long long)N, (long long)T);
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "scale must be finite");
+  return RCA_OK;
+}
+
+rca_status rca_causal_softmax(float* scores, float* lse, int64_t N, int64_t T, float scale, void* cuda_stream) {
+  RCA_GUARD_BEGIN
+  g_err.clear();
+  if (!scores || !lse) return fail(RCA_ERR_INVALID_ARGUMENT, "rca_causal_softmax: null pointer");
+  RCA_CHECK(check_softmax_args(N, T, scale));
+  if (!aligned16(scores) || !aligned16(lse))
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_causal_softmax: tensors must be 16-byte aligned");
+  std::string err;
+  if (!rca::causal_softmax_fwd(scores, lse, N, T, scale, static_cast<cudaStream_t>(cuda_stream), err))
+    return fail(RCA_ERR_CUDA, "rca_causal_softmax: %s", err.c_str());
+  return RCA_OK;
+  RCA_GUARD_END
+}
+
+rca_status rca_causal_softmax_bwd(const float* probs, float* grad, const float* grad_extra, int64_t N, int64_t T,
+                                  float scale, void* cuda_stream) {
+  RCA_GUARD_BEGIN
+  g_err.clear();
+  if (!probs || !grad) return fail(RCA_ERR_INVALID_ARGUMENT, "rca_causal_softmax_bwd: null pointer");
+  RCA_CHECK(check_softmax_args(N, T, scale));
+  if (!aligned16(probs) || !aligned16(grad) || (grad_extra && !aligned16(grad_extra)))
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_causal_softmax_bwd: tensors must be 16-byte aligned");
+  std::string err;
+  if (!rca::causal_softmax_bwd(probs, grad, grad_extra, N, T, scale, static_cast<cudaStream_t>(cuda_stream), err))
+    return fail(RCA_ERR_CUDA, "rca_causal_softmax_bwd: %s", err.c_str());
   return RCA_OK;
   RCA_GUARD_END
 }

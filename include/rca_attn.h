@@ -78,8 +78,8 @@ typedef enum {
 /* Storage dtype of q/k/v/out/dout/dq/dk/dv; selects the tensor-core operand type. */
 typedef enum { RCA_F32_TF32 = 0, RCA_BF16 = 1 } rca_dtype;
 
-/* ABI version: upper 16 bits major, lower 16 bits minor (0x00010001 = 1.1). */
-#define RCA_ABI_VERSION 0x00010001u
+/* ABI version: upper 16 bits major, lower 16 bits minor (0x00010002 = 1.2). */
+#define RCA_ABI_VERSION 0x00010002u
 uint32_t rca_abi_version(void);
 
 /* Message of the last failed call on this thread ("" if none). The pointer is
@@ -166,6 +166,66 @@ rca_status rca_attn_bwd_noalloc(const void* q, const void* k, const void* v, con
                                 const float* lse, const void* dout, void* dq, void* dk, void* dv,
                                 int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
                                 rca_dtype dt, void* cuda_stream);
+
+/*
+ * Materialized causal attention and its probability-returning diagnostic
+ * ("Execution Backends and the Python ABI", docs/internals/backends_and_python.html,
+ * section "What the Metal slice does": the default materialized request
+ * returns probabilities and context and keeps the [batch, heads, time, time]
+ * probabilities for its VJPs; the diagnostic that returns probabilities always
+ * uses it; causal softmax scales, masks and normalises in one operation).
+ *
+ * Forward, per batch b and query head h (KV head kv = h / (Hq/Hkv)):
+ *   S = scale * Q K^T (scale = 1/sqrt(Dh));  probs[b,h,i,j] = exp(S[i,j] - lse[b,h,i])
+ *   for j <= i and 0 for j > i;  out = probs V.
+ * Backward, for upstream gradients dout of out and dprobs of probs (dprobs may
+ * be NULL, meaning zero):
+ *   dP = dout V^T + dprobs;  dS = probs * (dP - rowsum(probs * dP));
+ *   dq = scale dS K;  dk = scale dS^T Q;  dv = probs^T dout  (dk, dv summed over
+ *   the query heads of a KV head). The backward reads the probabilities the
+ *   forward stored; it does not recompute them.
+ *
+ * Layouts: q, out, dout, dq [B,T,Hq,Dh] and k, v, dk, dv [B,T,Hkv,Dh] in the
+ * storage dtype (as rca_attn_fwd); probs, dprobs [B,Hq,T,T] float32 (4*B*Hq*T*T
+ * bytes: 1 GiB for B=4, Hq=16, T=2048); lse [B,Hq,T] float32. Dh in {16, 32, 64,
+ * 128} for both dtypes. The products over Dh use bf16 tensor cores with fp32
+ * accumulation (RCA_BF16) or fp32 (RCA_F32_TF32); those over T are fp32. All
+ * tensors 16-byte aligned. workspace: at least
+ * rca_attn_materialized_workspace_size(...) bytes (the same size serves both
+ * calls), 256-byte aligned, contents on entry irrelevant. Every pointer is a
+ * device pointer owned by the caller; calls validate, then only enqueue work
+ * on cuda_stream (the GEMMs run in cuBLAS on that stream).
+ */
+size_t rca_attn_materialized_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
+                                            rca_dtype dt);
+rca_status rca_attn_materialized_fwd(const void* q, const void* k, const void* v,
+                                     int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
+                                     void* out, float* probs, float* lse, rca_dtype dt,
+                                     void* workspace, size_t workspace_bytes, void* cuda_stream);
+rca_status rca_attn_materialized_bwd(const void* q, const void* k, const void* v, const float* probs,
+                                     const void* dout, const float* dprobs,
+                                     void* dq, void* dk, void* dv,
+                                     int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
+                                     rca_dtype dt, void* workspace, size_t workspace_bytes,
+                                     void* cuda_stream);
+
+/*
+ * The fused causal softmax of the materialized path, and its VJP, on N
+ * independent row-major [T, T] float32 score matrices (one per batch and head),
+ * in place ("Execution Backends and the Python ABI", "What the Metal slice
+ * does": causal softmax combines scaling, masking and normalisation in one
+ * kernel; Neural-network page, "Stable softmax and cross-entropy":
+ * max-subtracted softmax):
+ *   forward   scores[n,i,j] <- exp(scale*scores[n,i,j] - lse[n,i]) for j <= i,
+ *             0 for j > i;  lse[n,i] = ln sum_{j<=i} exp(scale*scores[n,i,j])
+ *   backward  with G = grad + grad_extra (grad_extra may be NULL):
+ *             grad[n,i,j] <- scale * probs[n,i,j] * (G[n,i,j] - sum_k probs[n,i,k] G[n,i,k])
+ *             for j <= i, 0 for j > i (the gradient of the unscaled scores).
+ * Device pointers, 16-byte aligned; lse is [N, T]; 1 <= T <= 65536; scale finite.
+ */
+rca_status rca_causal_softmax(float* scores, float* lse, int64_t N, int64_t T, float scale, void* cuda_stream);
+rca_status rca_causal_softmax_bwd(const float* probs, float* grad, const float* grad_extra, int64_t N, int64_t T,
+                                  float scale, void* cuda_stream);
 
 /*
  * Paged decode attention ("Execution Backends and the Python ABI",

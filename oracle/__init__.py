@@ -14,4 +14,10 @@ from .attention import (  # noqa: F401
     head_forward,
 )
 from .decode import gather_positions, paged_decode  # noqa: F401
-from .materialized import attention_probs, head_backward_probs, materialized_backward  # noqa: F401
+from .materialized import (  # noqa: F401
+    attention_probs,
+    causal_softmax,
+    causal_softmax_vjp,
+    head_backward_probs,
+    materialized_backward,
+)

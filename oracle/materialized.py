@@ -26,11 +26,15 @@ D = rowsum(dO * O), which equals rowsum(P * dO V^T)). Readings: the
 probabilities are float64 here and float32 on the device, [B, Hq, T, T], zero
 above the diagonal; KV head floor(h / g) as in the full-sequence path.
 
+The fused causal softmax itself (scale, mask, normalise) and its VJP with
+respect to the unscaled scores are exposed as causal_softmax and
+causal_softmax_vjp.
+
 Parity status: pinned (see tests/test_oracle_materialized_pins.py): torch's fp64
-softmax of the masked scores, torch autograd through P and O, central finite
-differences of the combined loss, the full-sequence oracle's backward when
-dP_up = 0, and invariance to dP_up above the diagonal and to a constant added
-to it on each row's kept entries.
+softmax of the masked scores and its autograd, torch autograd through P and O,
+central finite differences of the combined loss, the full-sequence oracle's
+backward when dP_up = 0, and invariance to dP_up above the diagonal and to a
+constant added to it on each row's kept entries.
 """
 
 from __future__ import annotations
@@ -38,6 +42,26 @@ from __future__ import annotations
 import numpy as np
 
 from .attention import _check_shapes, contract, default_scale, head_forward
+
+
+def causal_softmax(s, scale: float):
+    """Fused causal softmax of [..., T, T] scores: P = softmax(scale * S) over
+    j <= i (max subtracted), 0 above the diagonal; also LSE [..., T]."""
+    s = np.asarray(s, dtype=np.float64) * scale
+    t = s.shape[-1]
+    keep = np.tril(np.ones((t, t), dtype=bool))
+    s = np.where(keep, s, -np.inf)
+    m = np.max(s, axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    l = np.sum(e, axis=-1, keepdims=True)
+    return e / l, (m + np.log(l))[..., 0]
+
+
+def causal_softmax_vjp(p, g, scale: float):
+    """Gradient of <G, causal_softmax(scale * S)> with respect to S."""
+    p = np.asarray(p, dtype=np.float64)
+    g = np.asarray(g, dtype=np.float64)
+    return scale * p * (g - np.sum(p * g, axis=-1, keepdims=True))
 
 
 def attention_probs(q, k, v, scale: float | None = None):

@@ -151,3 +151,44 @@ def test_decode_workspace_size(lib):
     assert n >= 64 * 16 * 8 * (64 + 2) * 4
     assert lib.rca_paged_decode_workspace_size(4, 8, 8, 96, 16, 16, 1) == 0
     assert lib.rca_paged_decode_workspace_size(4, 8, 8, 64, 12, 16, 1) == 0
+
+
+def mat_fwd(lib, q=FAKE, B=1, Hq=2, Hkv=2, T=8, Dh=64, dt=1, probs=FAKE, ws=ctypes.c_void_p(1 << 20),
+            ws_bytes=1 << 30):
+    return lib.rca_attn_materialized_fwd(q, FAKE, FAKE, B, Hq, Hkv, T, Dh, FAKE, probs, FAKE, dt, ws, ws_bytes,
+                                         NULL)
+
+
+@pytest.mark.parametrize(
+    "kw,status,needle",
+    [
+        (dict(q=NULL), 1, "null"),
+        (dict(probs=NULL), 1, "null"),
+        (dict(T=0), 1, "fully masked"),
+        (dict(Hq=3, Hkv=2), 1, "Hq % Hkv"),
+        (dict(Dh=96), 2, "Dh=96"),
+        (dict(T=70000), 1, "too large"),
+        (dict(B=64, Hq=64, T=16384), 1, "too large"),
+        (dict(probs=ctypes.c_void_p(4100)), 1, "aligned"),
+        (dict(ws=NULL), 1, "workspace is null"),
+        (dict(ws_bytes=100), 1, "too small"),
+    ],
+)
+def test_materialized_validation(lib, kw, status, needle):
+    assert mat_fwd(lib, **kw) == status
+    assert needle in lib.rca_last_error().decode()
+
+
+def test_materialized_bwd_validation(lib):
+    st = lib.rca_attn_materialized_bwd(FAKE, FAKE, FAKE, FAKE, NULL, NULL, FAKE, FAKE, FAKE, 1, 2, 2, 8, 64, 1,
+                                       ctypes.c_void_p(1 << 20), 1 << 30, NULL)
+    assert st == 1 and "null" in lib.rca_last_error().decode()
+
+
+def test_materialized_workspace_size(lib):
+    n = lib.rca_attn_materialized_workspace_size(4, 16, 16, 2048, 64, 1)
+    # dP [B,Hq,T,T] fp32 plus per-head dK, dV and fp32 copies of Q, K, V, dO, O, dQ
+    assert n >= 4 * 16 * 2048 * 2048 * 4 + 2 * 4 * 16 * 2048 * 64 * 4 + 6 * 4 * 2048 * 16 * 64 * 4
+    n32 = lib.rca_attn_materialized_workspace_size(4, 16, 16, 2048, 64, 0)
+    assert 4 * 16 * 2048 * 2048 * 4 < n32 < n
+    assert lib.rca_attn_materialized_workspace_size(4, 16, 16, 2048, 96, 1) == 0

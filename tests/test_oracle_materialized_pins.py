@@ -106,6 +106,24 @@ def test_vjp_invariances():
         assert np.allclose(x, y, rtol=1e-9, atol=1e-11)
 
 
+def test_causal_softmax_matches_torch_and_head_forward():
+    rng = np.random.default_rng(11)
+    s = rng.standard_normal((3, 9, 9)) * 4
+    p, lse = oracle.causal_softmax(s, 0.7)
+    mask = torch.ones(9, 9, dtype=torch.bool).tril()
+    st = torch.tensor(s, dtype=torch.float64, requires_grad=True)
+    tp = torch.softmax((0.7 * st).masked_fill(~mask, float("-inf")), dim=-1)
+    assert np.allclose(p, tp.detach().numpy(), rtol=1e-12, atol=1e-15)
+    assert np.allclose(lse, torch.logsumexp((0.7 * st).masked_fill(~mask, float("-inf")), -1).detach().numpy())
+    g = rng.standard_normal((3, 9, 9))
+    (tp * torch.tensor(g)).sum().backward()
+    assert np.allclose(oracle.causal_softmax_vjp(p, g, 0.7), st.grad.numpy(), rtol=1e-11, atol=1e-13)
+    q, k, v, _, _ = rand(1, 9, 1, 1, 4, seed=12)
+    _, _, ph = oracle.head_forward(q[0, :, 0], k[0, :, 0], v[0, :, 0], 0.5)
+    p2, _ = oracle.causal_softmax(q[0, :, 0] @ k[0, :, 0].T, 0.5)
+    assert np.allclose(p2, ph, rtol=1e-13, atol=1e-15)
+
+
 # ---------------------------------------------------------------------------
 # Planted mistakes
 # ---------------------------------------------------------------------------
