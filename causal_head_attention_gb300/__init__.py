@@ -17,8 +17,10 @@ from ._native import (  # noqa: F401  (C-ABI names)
     rca_attn_bwd_main,
     rca_attn_bwd_noalloc,
     rca_attn_bwd_preprocess,
+    rca_attn_bwd_qkv,
     rca_attn_bwd_workspace_size,
     rca_attn_fwd,
+    rca_attn_fwd_qkv,
     rca_attn_materialized_bwd,
     rca_attn_materialized_fwd,
     rca_attn_materialized_workspace_size,
@@ -46,6 +48,11 @@ __all__ = [
     "rca_attn_bwd_main",
     "rca_attn_bwd_dq_convert",
     "rca_attn_bwd_noalloc",
+    "attention_forward_qkv",
+    "attention_backward_qkv",
+    "causal_attention_qkv",
+    "rca_attn_fwd_qkv",
+    "rca_attn_bwd_qkv",
     "materialized_forward",
     "materialized_backward",
     "rca_attn_materialized_fwd",
@@ -146,6 +153,62 @@ def paged_decode(q, k_pool, v_pool, page_table, seq_lens, workspace=None, stream
     return out, lse
 
 
+def attention_forward_qkv(qkv, Hq, Hkv, stream=None):
+    """Fused layout: qkv [B,T,(Hq+2*Hkv)*Dh] -> (out [B,T,Hq*Dh], lse [B,Hq,T])."""
+    import torch
+
+    B, T, W = qkv.shape
+    Dh = W // (Hq + 2 * Hkv)
+    out = torch.empty((B, T, Hq * Dh), dtype=qkv.dtype, device=qkv.device)
+    lse = torch.empty((B, Hq, T), dtype=torch.float32, device=qkv.device)
+    rca_attn_fwd_qkv(qkv, Hq, Hkv, out, lse, stream)
+    return out, lse
+
+
+def attention_backward_qkv(qkv, Hq, Hkv, out, lse, dout, workspace=None, stream=None):
+    """Returns dqkv [B,T,(Hq+2*Hkv)*Dh] (the gradient of the fused projection output)."""
+    import torch
+
+    B, T, W = qkv.shape
+    Dh = W // (Hq + 2 * Hkv)
+    dqkv = torch.empty_like(qkv)
+    if workspace is None:
+        n = rca_attn_bwd_workspace_size(B, Hq, Hkv, T, Dh, qkv.dtype)
+        workspace = torch.empty(n, dtype=torch.uint8, device=qkv.device)
+    rca_attn_bwd_qkv(qkv, Hq, Hkv, out, lse, dout.contiguous(), dqkv, workspace, stream)
+    return dqkv
+
+
+def _autograd_qkv_cls():
+    import torch
+
+    class CausalAttentionQKV(torch.autograd.Function):
+        """Custom-gradient node over the fused layout: input qkv, output the
+        merged heads; the VJP returns the gradient of qkv in the same layout."""
+
+        @staticmethod
+        def forward(ctx, qkv, Hq, Hkv):
+            out, lse = attention_forward_qkv(qkv, Hq, Hkv)
+            ctx.save_for_backward(qkv, out, lse)
+            ctx.heads = (Hq, Hkv)
+            return out
+
+        @staticmethod
+        def backward(ctx, dout):
+            qkv, out, lse = ctx.saved_tensors
+            return attention_backward_qkv(qkv, *ctx.heads, out, lse, dout), None, None
+
+    return CausalAttentionQKV
+
+
+def causal_attention_qkv(qkv, Hq, Hkv):
+    """Differentiable causal attention on a fused projection output
+    [B,T,(Hq+2*Hkv)*Dh]; returns [B,T,Hq*Dh] for the output projection."""
+    if _Lazy.qkv_cls is None:
+        _Lazy.qkv_cls = _autograd_qkv_cls()
+    return _Lazy.qkv_cls.apply(qkv, Hq, Hkv)
+
+
 def _autograd_cls():
     import torch
 
@@ -168,6 +231,7 @@ def _autograd_cls():
 
 class _Lazy:
     cls = None
+    qkv_cls = None
 
 
 def causal_attention(q, k, v):

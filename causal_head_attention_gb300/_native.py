@@ -59,6 +59,9 @@ _SIG = {
                                                  ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "rca_causal_softmax": (ctypes.c_int, [_P, _P, _I, _I, ctypes.c_float, _P]),
     "rca_causal_softmax_bwd": (ctypes.c_int, [_P, _P, _P, _I, _I, ctypes.c_float, _P]),
+    "rca_attn_fwd_qkv": (ctypes.c_int, [_P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_int, _P]),
+    "rca_attn_bwd_qkv": (ctypes.c_int, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_int, _P, ctypes.c_size_t,
+                                        _P]),
     "rca_selftest_device_timeout": (ctypes.c_int, [_P]),
     "rca_stream_status": (ctypes.c_int, [_P]),
     "rca_set_wait_timeout_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
@@ -280,6 +283,26 @@ def rca_causal_softmax_bwd(probs, grad, grad_extra, scale, stream=None):
     N = probs.numel() // (T * T)
     _check(lib().rca_causal_softmax_bwd(_ptr(probs), _ptr(grad), _ptr(grad_extra), N, T, float(scale),
                                         _stream(stream)))
+
+
+def _qkv_shape(qkv, Hq, Hkv):
+    if qkv.dim() != 3 or qkv.shape[2] % (Hq + 2 * Hkv):
+        raise ValueError("qkv must be [B, T, (Hq + 2*Hkv) * Dh]")
+    B, T, W = qkv.shape
+    return B, T, W // (Hq + 2 * Hkv)
+
+
+def rca_attn_fwd_qkv(qkv, Hq, Hkv, out, lse, stream=None):
+    B, T, Dh = _qkv_shape(qkv, Hq, Hkv)
+    _check(lib().rca_attn_fwd_qkv(_ptr(qkv), B, T, Hq, Hkv, Dh, _ptr(out), _ptr(lse), _dtype_code(qkv),
+                                  _stream(stream)))
+
+
+def rca_attn_bwd_qkv(qkv, Hq, Hkv, out, lse, dout, dqkv, workspace, stream=None):
+    B, T, Dh = _qkv_shape(qkv, Hq, Hkv)
+    _check(lib().rca_attn_bwd_qkv(_ptr(qkv), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dqkv), B, T, Hq, Hkv, Dh,
+                                  _dtype_code(qkv), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream)))
 
 
 def rca_selftest_device_timeout(stream=None):

@@ -101,10 +101,12 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const PreArgs 
 // dQ convert
 // ----------------------------------------------------------------------------
 // Grid-stride over float4 groups, four loads in flight per thread per pass.
-template <bool F32>
+// STRIDED: the output rows (one position, all heads) are dq_row4 groups of 4
+// elements apart instead of row4 (a row of a fused QKV gradient buffer).
+template <bool F32, bool STRIDED>
 __global__ void __launch_bounds__(256)
     attn_bwd_dq_convert_kernel(const float* __restrict__ acc, void* __restrict__ dq, long long n4,
-                               float scale) {
+                               float scale, long long row4, long long dq_row4) {
   constexpr int U = 4;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += U * stride) {
@@ -114,8 +116,9 @@ __global__ void __launch_bounds__(256)
       if (i + k * stride < n4) v[k] = reinterpret_cast<const float4*>(acc)[i + k * stride];
 #pragma unroll
     for (int k = 0; k < U; ++k) {
-      const long long j = i + k * stride;
+      long long j = i + k * stride;
       if (j >= n4) continue;
+      if constexpr (STRIDED) j = (j / row4) * dq_row4 + j % row4;
       if constexpr (F32) {
         reinterpret_cast<float4*>(dq)[j] =
             make_float4(v[k].x * scale, v[k].y * scale, v[k].z * scale, v[k].w * scale);
@@ -130,12 +133,16 @@ __global__ void __launch_bounds__(256)
 // ----------------------------------------------------------------------------
 // fp32 storage mode: bf16 hi/lo split of an operand (x = hi + lo)
 // ----------------------------------------------------------------------------
+// STRIDED: source rows are src_row4 groups of 4 apart (a fused QKV buffer);
+// the copies are contiguous.
+template <bool STRIDED>
 __global__ void __launch_bounds__(256)
     split_hilo_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ hi,
-                      __nv_bfloat16* __restrict__ lo, long long n4) {
+                      __nv_bfloat16* __restrict__ lo, long long n4, long long row4, long long src_row4) {
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
-    const float4 v = reinterpret_cast<const float4*>(src)[i];
+    const long long si = STRIDED ? (i / row4) * src_row4 + i % row4 : i;
+    const float4 v = reinterpret_cast<const float4*>(src)[si];
     uint32_t h0, l0, h1, l1;
     split_bf16x2(v.x, v.y, h0, l0);
     split_bf16x2(v.z, v.w, h1, l1);
@@ -251,6 +258,7 @@ struct BwdMaps {
 struct BwdArgs {
   void* dk;
   void* dv;
+  long long dkv_row;   // elements between consecutive positions of dK, dV (Hkv * Dh if contiguous)
   float* dq_acc;       // [B, T, Hq, Dh]
   const float* lse2;   // [B, Hq, Tpad]
   const float* dvec;   // [B, Hq, Tpad]
@@ -639,7 +647,7 @@ __global__ void __launch_bounds__(512, 1)
           tc_fence_after();
           const int key = itm.j * 128 + rl;
           const bool valid = key < a.T;
-          const size_t row_off = ((static_cast<size_t>(itm.b) * a.T + key) * a.Hkv + itm.kvh) * a.Dh;
+          const size_t row_off = (static_cast<size_t>(itm.b) * a.T + key) * a.dkv_row + static_cast<size_t>(itm.kvh) * a.Dh;
 #pragma unroll
           for (int which = 0; which < 2; ++which) {
 #pragma unroll

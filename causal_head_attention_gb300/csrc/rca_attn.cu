@@ -84,7 +84,10 @@ EncodeFn get_encode() {
 // panel of the head dimension, 128-byte swizzle. Positions past T and head
 // columns past Dh read as zero.
 rca_status make_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t H, int64_t Dh,
-                    bool f32, const char* name, unsigned box_rows = 128) {
+                    bool f32, const char* name, unsigned box_rows = 128, int64_t row_stride = 0) {
+  // (row_stride: elements between consecutive positions of one head; 0 means
+  // H * Dh, a contiguous [B, T, H, Dh] tensor. A fused QKV buffer has a larger one.)
+  if (row_stride == 0) row_stride = H * Dh;
   // (f32 selects fp32 elements with 32-element panels; bf16 uses 64-element panels;
   // a box covers box_rows positions of one head)
   EncodeFn enc = get_encode();
@@ -92,8 +95,8 @@ rca_status make_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64
   const uint64_t es = f32 ? 4 : 2;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(Dh), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T),
                         static_cast<cuuint64_t>(B)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(Dh * es), static_cast<cuuint64_t>(H * Dh * es),
-                           static_cast<cuuint64_t>(T * H * Dh * es)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(Dh * es), static_cast<cuuint64_t>(row_stride * es),
+                           static_cast<cuuint64_t>(T * row_stride * es)};
   cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / es), 1, box_rows, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
@@ -291,13 +294,13 @@ DecodeWs decode_ws_layout(int64_t B, int64_t Hq, int64_t Dh, int64_t page_size, 
 // ---------------------------------------------------------------------------
 template <bool TF32, int DHP>
 rca_status launch_fwd(const void* q, const void* k, const void* v, int64_t B, int64_t Hq, int64_t Hkv,
-                      int64_t T, int64_t Dh, void* out, float* lse, cudaStream_t st) {
+                      int64_t T, int64_t Dh, void* out, float* lse, cudaStream_t st, int64_t qs, int64_t kvs) {
   using C = rca::FwdCfg<TF32, DHP>;
   static std::atomic<unsigned long long> smem_set{0};
   CUtensorMap mq, mk, mv;
-  RCA_CHECK(make_map(&mq, q, B, T, Hq, Dh, TF32, "q"));
-  RCA_CHECK(make_map(&mk, k, B, T, Hkv, Dh, TF32, "k"));
-  RCA_CHECK(make_map(&mv, v, B, T, Hkv, Dh, TF32, "v"));
+  RCA_CHECK(make_map(&mq, q, B, T, Hq, Dh, TF32, "q", 128, qs));
+  RCA_CHECK(make_map(&mk, k, B, T, Hkv, Dh, TF32, "k", 128, kvs));
+  RCA_CHECK(make_map(&mv, v, B, T, Hkv, Dh, TF32, "v", 128, kvs));
   int* status = nullptr;
   RCA_CHECK(status_word(&status));
   auto kern = rca::attn_fwd_kernel<TF32, DHP>;
@@ -340,15 +343,22 @@ rca_status launch_fwd(const void* q, const void* k, const void* v, int64_t B, in
   return RCA_OK;
 }
 
-rca_status launch_split(const void* src, void* hi, void* lo, size_t n, cudaStream_t st) {
+// n elements in rows of row_len (all heads of one position); source rows are
+// src_row apart (== row_len when contiguous).
+rca_status launch_split(const void* src, void* hi, void* lo, size_t n, int64_t row_len, int64_t src_row,
+                        cudaStream_t st) {
   const long long n4 = (long long)(n / 4);
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long want = (n4 + 255) / 256, cap = (long long)sms * 8;
   const unsigned grid = unsigned(want < cap ? (want > 0 ? want : 1) : cap);
-  rca::split_hilo_kernel<<<grid, 256, 0, st>>>(static_cast<const float*>(src), static_cast<__nv_bfloat16*>(hi),
-                                                static_cast<__nv_bfloat16*>(lo), n4);
+  if (src_row == row_len)
+    rca::split_hilo_kernel<false><<<grid, 256, 0, st>>>(static_cast<const float*>(src), static_cast<__nv_bfloat16*>(hi),
+                                                         static_cast<__nv_bfloat16*>(lo), n4, row_len / 4, src_row / 4);
+  else
+    rca::split_hilo_kernel<true><<<grid, 256, 0, st>>>(static_cast<const float*>(src), static_cast<__nv_bfloat16*>(hi),
+                                                        static_cast<__nv_bfloat16*>(lo), n4, row_len / 4, src_row / 4);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch split_hilo_kernel");
   return RCA_OK;
@@ -357,7 +367,8 @@ rca_status launch_split(const void* src, void* hi, void* lo, size_t n, cudaStrea
 template <bool HL, int DHB>
 rca_status launch_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
                            int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, void* ws,
-                           const WsLayout& L, cudaStream_t st, int* status_override = nullptr) {
+                           const WsLayout& L, cudaStream_t st, int* status_override, int64_t qs, int64_t kvs,
+                           int64_t dkvs) {
   using C = rca::BwdCfg<HL, DHB>;
   static std::atomic<unsigned long long> smem_set{0};
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -374,10 +385,10 @@ rca_status launch_bwd_main(const void* q, const void* k, const void* v, const vo
     void* vh = static_cast<uint8_t*>(kh) + 2 * L.kv_part;
     void* vl = static_cast<uint8_t*>(kh) + 3 * L.kv_part;
     const size_t nq = size_t(B) * T * Hq * Dh, nkv = size_t(B) * T * Hkv * Dh;
-    RCA_CHECK(launch_split(q, qh, ql, nq, st));
-    RCA_CHECK(launch_split(dout, dh, dl, nq, st));
-    RCA_CHECK(launch_split(k, kh, kl, nkv, st));
-    RCA_CHECK(launch_split(v, vh, vl, nkv, st));
+    RCA_CHECK(launch_split(q, qh, ql, nq, Hq * Dh, qs, st));
+    RCA_CHECK(launch_split(dout, dh, dl, nq, Hq * Dh, Hq * Dh, st));
+    RCA_CHECK(launch_split(k, kh, kl, nkv, Hkv * Dh, kvs, st));
+    RCA_CHECK(launch_split(v, vh, vl, nkv, Hkv * Dh, kvs, st));
     RCA_CHECK(make_map(&maps.q[0], qh, B, T, Hq, Dh, false, "q hi"));
     RCA_CHECK(make_map(&maps.q[1], ql, B, T, Hq, Dh, false, "q lo"));
     RCA_CHECK(make_map(&maps.dO[0], dh, B, T, Hq, Dh, false, "dout hi"));
@@ -387,9 +398,9 @@ rca_status launch_bwd_main(const void* q, const void* k, const void* v, const vo
     RCA_CHECK(make_map(&maps.v[0], vh, B, T, Hkv, Dh, false, "v hi"));
     RCA_CHECK(make_map(&maps.v[1], vl, B, T, Hkv, Dh, false, "v lo"));
   } else {
-    RCA_CHECK(make_map(&maps.q[0], q, B, T, Hq, Dh, false, "q"));
-    RCA_CHECK(make_map(&maps.k[0], k, B, T, Hkv, Dh, false, "k"));
-    RCA_CHECK(make_map(&maps.v[0], v, B, T, Hkv, Dh, false, "v"));
+    RCA_CHECK(make_map(&maps.q[0], q, B, T, Hq, Dh, false, "q", 128, qs));
+    RCA_CHECK(make_map(&maps.k[0], k, B, T, Hkv, Dh, false, "k", 128, kvs));
+    RCA_CHECK(make_map(&maps.v[0], v, B, T, Hkv, Dh, false, "v", 128, kvs));
     RCA_CHECK(make_map(&maps.dO[0], dout, B, T, Hq, Dh, false, "dout"));
     maps.q[1] = maps.q[0];
     maps.k[1] = maps.k[0];
@@ -419,6 +430,7 @@ rca_status launch_bwd_main(const void* q, const void* k, const void* v, const vo
   rca::BwdArgs a{};
   a.dk = dk;
   a.dv = dv;
+  a.dkv_row = dkvs;
   a.dq_acc = reinterpret_cast<float*>(w + L.dq_off);
   a.lse2 = reinterpret_cast<const float*>(w + L.lse2_off);
   a.dvec = reinterpret_cast<const float*>(w + L.d_off);
@@ -445,25 +457,35 @@ rca_status launch_bwd_main(const void* q, const void* k, const void* v, const vo
   return RCA_OK;
 }
 
+// qs, kvs: elements between consecutive positions of Q and of K, V (0 means
+// contiguous [B, T, H, Dh]); dkvs the same for the dK, dV outputs.
 rca_status do_fwd(const void* q, const void* k, const void* v, int64_t B, int64_t Hq, int64_t Hkv, int64_t T,
-                  int64_t Dh, void* out, float* lse, rca_dtype dt, cudaStream_t st) {
+                  int64_t Dh, void* out, float* lse, rca_dtype dt, cudaStream_t st, int64_t qs = 0,
+                  int64_t kvs = 0) {
   if (dt == RCA_BF16) {
-    if (Dh <= 64) return launch_fwd<false, 64>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st);
-    return launch_fwd<false, 128>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st);
+    if (Dh <= 64) return launch_fwd<false, 64>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs);
+    return launch_fwd<false, 128>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs);
   }
-  if (Dh <= 32) return launch_fwd<true, 32>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st);
-  return launch_fwd<true, 64>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st);
+  if (Dh <= 32) return launch_fwd<true, 32>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs);
+  return launch_fwd<true, 64>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs);
 }
 
 rca_status do_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
                        int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt, void* ws,
-                       const WsLayout& L, cudaStream_t st, int* status_override = nullptr) {
+                       const WsLayout& L, cudaStream_t st, int* status_override = nullptr, int64_t qs = 0,
+                       int64_t kvs = 0, int64_t dkvs = 0) {
+  if (qs == 0) qs = Hq * Dh;
+  if (kvs == 0) kvs = Hkv * Dh;
+  if (dkvs == 0) dkvs = Hkv * Dh;
   if (dt == RCA_BF16) {
     if (Dh <= 64)
-      return launch_bwd_main<false, 64>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st, status_override);
-    return launch_bwd_main<false, 128>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st, status_override);
+      return launch_bwd_main<false, 64>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st, status_override, qs,
+                                        kvs, dkvs);
+    return launch_bwd_main<false, 128>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st, status_override, qs,
+                                       kvs, dkvs);
   }
-  return launch_bwd_main<true, 64>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st, status_override);
+  return launch_bwd_main<true, 64>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st, status_override, qs, kvs,
+                                   dkvs);
 }
 
 rca_status do_preprocess(const void* out, const float* lse, const void* dout, int64_t B, int64_t Hq, int64_t T,
@@ -494,7 +516,8 @@ rca_status do_preprocess(const void* out, const float* lse, const void* dout, in
 }
 
 rca_status do_convert(void* dq, int64_t B, int64_t Hq, int64_t T, int64_t Dh, rca_dtype dt, const void* ws,
-                      const WsLayout& L, cudaStream_t st) {
+                      const WsLayout& L, cudaStream_t st, int64_t dqs = 0) {
+  if (dqs == 0) dqs = Hq * Dh;  // elements between consecutive positions of dq
   const float* acc = reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws) + L.dq_off);
   const long long n4 = (long long)(B * T * Hq * Dh / 4);
   int sms = 0;
@@ -503,10 +526,15 @@ rca_status do_convert(void* dq, int64_t B, int64_t Hq, int64_t T, int64_t Dh, rc
   const long long cap = (long long)sms * 8;
   const unsigned grid = unsigned(want < cap ? (want > 0 ? want : 1) : cap);
   const float scale = float(1.0 / std::sqrt(double(Dh)));
-  if (dt == RCA_BF16)
-    rca::attn_bwd_dq_convert_kernel<false><<<grid, 256, 0, st>>>(acc, dq, n4, scale);
-  else
-    rca::attn_bwd_dq_convert_kernel<true><<<grid, 256, 0, st>>>(acc, dq, n4, scale);
+  const long long row4 = Hq * Dh / 4, dq_row4 = dqs / 4;
+  const bool strided = dqs != Hq * Dh;
+  if (dt == RCA_BF16) {
+    if (strided) rca::attn_bwd_dq_convert_kernel<false, true><<<grid, 256, 0, st>>>(acc, dq, n4, scale, row4, dq_row4);
+    else rca::attn_bwd_dq_convert_kernel<false, false><<<grid, 256, 0, st>>>(acc, dq, n4, scale, row4, dq_row4);
+  } else {
+    if (strided) rca::attn_bwd_dq_convert_kernel<true, true><<<grid, 256, 0, st>>>(acc, dq, n4, scale, row4, dq_row4);
+    else rca::attn_bwd_dq_convert_kernel<true, false><<<grid, 256, 0, st>>>(acc, dq, n4, scale, row4, dq_row4);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch attn_bwd_dq_convert_kernel");
   return RCA_OK;
@@ -825,6 +853,48 @@ rca_status rca_causal_softmax_bwd(const float* probs, float* grad, const float* 
   if (!rca::causal_softmax_bwd(probs, grad, grad_extra, N, T, scale, static_cast<cudaStream_t>(cuda_stream), err))
     return fail(RCA_ERR_CUDA, "rca_causal_softmax_bwd: %s", err.c_str());
   return RCA_OK;
+  RCA_GUARD_END
+}
+
+// ---------------------------------------------------------------------------
+// Fused QKV layout: q, k, v read from one [B, T, (Hq + 2 Hkv) * Dh] projection
+// output, dq, dk, dv written into one buffer of the same shape.
+// ---------------------------------------------------------------------------
+rca_status rca_attn_fwd_qkv(const void* qkv, int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t Dh, void* out,
+                            float* lse, rca_dtype dt, void* cuda_stream) {
+  RCA_GUARD_BEGIN
+  g_err.clear();
+  if (!qkv || !out || !lse) return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_fwd_qkv: null pointer");
+  RCA_CHECK(check_shape(B, Hq, Hkv, T, Dh, dt));
+  if (!aligned16(qkv) || !aligned16(out) || !aligned16(lse))
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_fwd_qkv: qkv, out and lse must be 16-byte aligned");
+  const int64_t es = dt == RCA_BF16 ? 2 : 4, row = (Hq + 2 * Hkv) * Dh;
+  const char* base = static_cast<const char*>(qkv);
+  return do_fwd(base, base + Hq * Dh * es, base + (Hq + Hkv) * Dh * es, B, Hq, Hkv, T, Dh, out, lse, dt,
+                static_cast<cudaStream_t>(cuda_stream), row, row);
+  RCA_GUARD_END
+}
+
+rca_status rca_attn_bwd_qkv(const void* qkv, const void* out, const float* lse, const void* dout, void* dqkv,
+                            int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t Dh, rca_dtype dt,
+                            void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  RCA_GUARD_BEGIN
+  g_err.clear();
+  if (!qkv || !out || !lse || !dout || !dqkv) return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd_qkv: null pointer");
+  RCA_CHECK(check_shape(B, Hq, Hkv, T, Dh, dt));
+  if (!aligned16(qkv) || !aligned16(out) || !aligned16(lse) || !aligned16(dout) || !aligned16(dqkv))
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd_qkv: tensors must be 16-byte aligned");
+  const WsLayout L = ws_layout(B, Hq, Hkv, T, Dh, dt);
+  RCA_CHECK(check_ws(workspace, workspace_bytes, L));
+  const int64_t es = dt == RCA_BF16 ? 2 : 4, row = (Hq + 2 * Hkv) * Dh;
+  const char* base = static_cast<const char*>(qkv);
+  char* dbase = static_cast<char*>(dqkv);
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  RCA_CHECK(do_preprocess(out, lse, dout, B, Hq, T, Dh, dt, workspace, L, st));
+  RCA_CHECK(do_bwd_main(base, base + Hq * Dh * es, base + (Hq + Hkv) * Dh * es, dout, dbase + Hq * Dh * es,
+                        dbase + (Hq + Hkv) * Dh * es, B, Hq, Hkv, T, Dh, dt, workspace, L, st, nullptr, row, row,
+                        row));
+  return do_convert(dbase, B, Hq, T, Dh, dt, workspace, L, st, row);
   RCA_GUARD_END
 }
 

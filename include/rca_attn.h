@@ -78,8 +78,8 @@ typedef enum {
 /* Storage dtype of q/k/v/out/dout/dq/dk/dv; selects the tensor-core operand type. */
 typedef enum { RCA_F32_TF32 = 0, RCA_BF16 = 1 } rca_dtype;
 
-/* ABI version: upper 16 bits major, lower 16 bits minor (0x00010002 = 1.2). */
-#define RCA_ABI_VERSION 0x00010002u
+/* ABI version: upper 16 bits major, lower 16 bits minor (0x00010003 = 1.3). */
+#define RCA_ABI_VERSION 0x00010003u
 uint32_t rca_abi_version(void);
 
 /* Message of the last failed call on this thread ("" if none). The pointer is
@@ -166,6 +166,26 @@ rca_status rca_attn_bwd_noalloc(const void* q, const void* k, const void* v, con
                                 const float* lse, const void* dout, void* dq, void* dk, void* dv,
                                 int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
                                 rca_dtype dt, void* cuda_stream);
+
+/*
+ * Fused QKV layout (an addition around the pages' operation: the pages project
+ * query, key and value with three Linear layers, then split heads, attend,
+ * merge heads and apply the output projection — "Neural network" page, "Where
+ * attention is"). Here q, k and v are read in place from one fused projection
+ * output and the gradients are written in place into one buffer of the same
+ * shape, so neither direction needs a split or a concatenation copy:
+ *   qkv, dqkv : [B, T, (Hq + 2*Hkv) * Dh], per position q heads 0..Hq-1, then
+ *               k heads, then v heads, each Dh wide (storage dtype)
+ *   out, dout : [B, T, Hq * Dh]  (= [B, T, Hq, Dh], the merged heads)
+ *   lse       : [B, Hq, T] float32
+ * Same computation, dtypes, head widths, errors and workspace
+ * (rca_attn_bwd_workspace_size) as rca_attn_fwd / rca_attn_bwd. 16-byte aligned.
+ */
+rca_status rca_attn_fwd_qkv(const void* qkv, int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t Dh,
+                            void* out, float* lse, rca_dtype dt, void* cuda_stream);
+rca_status rca_attn_bwd_qkv(const void* qkv, const void* out, const float* lse, const void* dout, void* dqkv,
+                            int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t Dh, rca_dtype dt,
+                            void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 /*
  * Materialized causal attention and its probability-returning diagnostic

@@ -192,3 +192,15 @@ def test_materialized_workspace_size(lib):
     n32 = lib.rca_attn_materialized_workspace_size(4, 16, 16, 2048, 64, 0)
     assert 4 * 16 * 2048 * 2048 * 4 < n32 < n
     assert lib.rca_attn_materialized_workspace_size(4, 16, 16, 2048, 96, 1) == 0
+
+
+def test_qkv_validation(lib):
+    assert lib.rca_attn_fwd_qkv(NULL, 1, 8, 2, 2, 64, FAKE, FAKE, 1, NULL) == 1
+    assert "null" in lib.rca_last_error().decode()
+    assert lib.rca_attn_fwd_qkv(FAKE, 1, 8, 3, 2, 64, FAKE, FAKE, 1, NULL) == 1
+    assert "Hq % Hkv" in lib.rca_last_error().decode()
+    assert lib.rca_attn_fwd_qkv(ctypes.c_void_p(4104), 1, 8, 2, 2, 64, FAKE, FAKE, 1, NULL) == 1
+    assert "aligned" in lib.rca_last_error().decode()
+    assert lib.rca_attn_bwd_qkv(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 2, 2, 64, 1, ctypes.c_void_p(1 << 20), 16,
+                                NULL) == 1
+    assert "too small" in lib.rca_last_error().decode()
