@@ -21,3 +21,4 @@ from .materialized import (  # noqa: F401
     head_backward_probs,
     materialized_backward,
 )
+from .varlen import attention_backward_varlen, attention_forward_varlen  # noqa: F401
