@@ -18,9 +18,11 @@ from ._native import (  # noqa: F401  (C-ABI names)
     rca_attn_bwd_noalloc,
     rca_attn_bwd_preprocess,
     rca_attn_bwd_qkv,
+    rca_attn_bwd_varlen,
     rca_attn_bwd_workspace_size,
     rca_attn_fwd,
     rca_attn_fwd_qkv,
+    rca_attn_fwd_varlen,
     rca_attn_materialized_bwd,
     rca_attn_materialized_fwd,
     rca_attn_materialized_workspace_size,
@@ -53,6 +55,10 @@ __all__ = [
     "causal_attention_qkv",
     "rca_attn_fwd_qkv",
     "rca_attn_bwd_qkv",
+    "attention_forward_varlen",
+    "attention_backward_varlen",
+    "rca_attn_fwd_varlen",
+    "rca_attn_bwd_varlen",
     "materialized_forward",
     "materialized_backward",
     "rca_attn_materialized_fwd",
@@ -151,6 +157,28 @@ def paged_decode(q, k_pool, v_pool, page_table, seq_lens, workspace=None, stream
         workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
     rca_paged_decode(q, k_pool, v_pool, page_table, seq_lens, out, lse, workspace, stream)
     return out, lse
+
+
+def attention_forward_varlen(q, k, v, seq_lens, stream=None):
+    """Right-padded batch with per-sequence lengths seq_lens (int32 [B], device).
+    Returns (out, lse); padding rows are zero, their LSE -inf."""
+    import torch
+
+    B, T, Hq, Dh = q.shape
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    rca_attn_fwd_varlen(q, k, v, seq_lens, out, lse, stream)
+    return out, lse
+
+
+def attention_backward_varlen(q, k, v, out, lse, dout, seq_lens, workspace=None, stream=None):
+    """Returns (dq, dk, dv); zero at padding positions, dout there is ignored."""
+    import torch
+
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = workspace if workspace is not None else workspace_for(q, k)
+    rca_attn_bwd_varlen(q, k, v, out, lse, dout.contiguous(), seq_lens, dq, dk, dv, ws, stream)
+    return dq, dk, dv
 
 
 def attention_forward_qkv(qkv, Hq, Hkv, stream=None):

@@ -62,6 +62,9 @@ _SIG = {
     "rca_attn_fwd_qkv": (ctypes.c_int, [_P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_int, _P]),
     "rca_attn_bwd_qkv": (ctypes.c_int, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_int, _P, ctypes.c_size_t,
                                         _P]),
+    "rca_attn_fwd_varlen": (ctypes.c_int, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_int, _P]),
+    "rca_attn_bwd_varlen": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                           ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "rca_selftest_device_timeout": (ctypes.c_int, [_P]),
     "rca_stream_status": (ctypes.c_int, [_P]),
     "rca_set_wait_timeout_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
@@ -303,6 +306,28 @@ def rca_attn_bwd_qkv(qkv, Hq, Hkv, out, lse, dout, dqkv, workspace, stream=None)
     _check(lib().rca_attn_bwd_qkv(_ptr(qkv), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dqkv), B, T, Hq, Hkv, Dh,
                                   _dtype_code(qkv), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                   _stream(stream)))
+
+
+def _check_lens(seq_lens, B):
+    torch = _torch()
+    if seq_lens.dtype != torch.int32 or tuple(seq_lens.shape) != (B,):
+        raise ValueError("seq_lens must be int32 [B]")
+
+
+def rca_attn_fwd_varlen(q, k, v, seq_lens, out, lse, stream=None):
+    B, Hq, Hkv, T, Dh = _shape(q, k)
+    _check_lens(seq_lens, B)
+    _check(lib().rca_attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), B, Hq, Hkv, T, Dh, _ptr(out),
+                                     _ptr(lse), _dtype_code(q), _stream(stream)))
+
+
+def rca_attn_bwd_varlen(q, k, v, out, lse, dout, seq_lens, dq, dk, dv, workspace, stream=None):
+    B, Hq, Hkv, T, Dh = _shape(q, k)
+    _check_lens(seq_lens, B)
+    _check(lib().rca_attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(seq_lens),
+                                     _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, T, Dh, _dtype_code(q),
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream(stream)))
 
 
 def rca_selftest_device_timeout(stream=None):

@@ -41,6 +41,8 @@ struct PreArgs {
   float* dq_acc;  // [B, T, Hq, Dh]
   float* lse2;    // [B, Hq, Tpad]  -LSE * log2(e); -inf on padded rows
   float* dvec;    // [B, Hq, Tpad]  -D; 0 on padded rows
+  const int* lens;  // per-sequence lengths (right padding), or null
+  int* status;
   int B, Hq, T, Dh, Tpad;
 };
 
@@ -66,6 +68,17 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const PreArgs 
     b = static_cast<int>(bt / static_cast<IT>(a.Tpad));
   }
   const bool live = in && t < a.T;
+  // A padding row of a variable-length batch is kept out of the backward:
+  // LSE2 = -inf makes its recomputed probabilities exactly 0, and D = 0.
+  bool real = live;
+  if (live && a.lens) {
+    int L = __ldg(a.lens + b);
+    if (L < 0 || L > a.T) {
+      atomicExch(a.status, kStatusBadInput);
+      L = L < 0 ? 0 : a.T;
+    }
+    real = t < L;
+  }
   float acc = 0.f;
   if (live) {
     const size_t off = ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * a.Dh + part * EPL;
@@ -91,8 +104,8 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const PreArgs 
   for (int o = lpr >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, lpr);
   if (in && part == 0) {
     const size_t so = (static_cast<size_t>(b) * a.Hq + h) * a.Tpad + t;
-    a.dvec[so] = live ? -acc : 0.f;
-    a.lse2[so] = live ? -(a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.T + t] * 1.4426950408889634f)
+    a.dvec[so] = real ? -acc : 0.f;
+    a.lse2[so] = real ? -(a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.T + t] * 1.4426950408889634f)
                       : -INFINITY;
   }
 }

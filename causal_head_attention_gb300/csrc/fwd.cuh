@@ -159,6 +159,7 @@ struct FwdCfg {
 struct FwdArgs {
   void* out;
   float* lse;
+  const int* lens;  // per-sequence lengths (right padding), or null: rows t >= lens[b] are padding
   int* status;
   unsigned long long timeout_ns;
   int B, Hq, Hkv, T, Dh, group, n_qt;
@@ -173,6 +174,15 @@ struct FwdArgs {
 struct FwdItem {
   int b, h, kvh, qt, nkv;
 };
+
+// Length of sequence b of a variable-length batch, clamped to [0, T]; a value
+// outside that range is recorded as a bad device-side input.
+__device__ __forceinline__ int seq_len(const FwdArgs& a, int b) {
+  const int L = __ldg(a.lens + b);
+  if (L >= 0 && L <= a.T) return L;
+  atomicExch(a.status, kStatusBadInput);
+  return L < 0 ? 0 : a.T;
+}
 __device__ __forceinline__ bool fwd_item(const FwdArgs& a, int k, FwdItem& it) {
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
   const long long idx = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
@@ -791,6 +801,12 @@ __global__ void __launch_bounds__(512, 1)
       tc_fence_before();
       mbar_arrive(bar(C::B_OFREE));
       const bool valid = q_idx < a.T;
+      // Padding rows (variable-length batches) are written as zeros, LSE -inf.
+      const bool pad = a.lens && q_idx >= seq_len(a, it.b);
+      if (pad) {
+#pragma unroll
+        for (int i = 0; i < W; ++i) o[i] = 0.f;
+      }
       const size_t row_off = ((static_cast<size_t>(it.b) * a.T + q_idx) * a.Hq + it.h) * a.Dh;
       const int ncol = a.Dh - g * W;  // valid columns in this warpgroup's range
       if (valid && ncol > 0) {
@@ -810,7 +826,8 @@ __global__ void __launch_bounds__(512, 1)
         }
       }
       if (g == 0 && valid)
-        a.lse[(static_cast<size_t>(it.b) * a.Hq + it.h) * a.T + q_idx] = (mt + __log2f(lt)) * 0.69314718055994531f;
+        a.lse[(static_cast<size_t>(it.b) * a.Hq + it.h) * a.T + q_idx] =
+            pad ? -INFINITY : (mt + __log2f(lt)) * 0.69314718055994531f;
       tb += it.nkv;
     }
     end_role();
@@ -849,6 +866,7 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_after();
         const int q_idx = it.qt * C::BM + row;
         const bool valid = q_idx < a.T;
+        const bool pad = a.lens && q_idx >= seq_len(a, it.b);  // padding row: zeros, LSE -inf
         const size_t row_off = ((static_cast<size_t>(it.b) * a.T + q_idx) * a.Hq + it.h) * a.Dh;
 #pragma unroll
         for (int c = 0; c < DHP / 32; ++c) {
@@ -870,6 +888,10 @@ __global__ void __launch_bounds__(512, 1)
             tc_fence_before();
             mbar_arrive(bar(C::B_OFREE));  // both partials read: the next item's products may start
           }
+          if (pad) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0.f;
+          }
           const int nc = a.Dh - 32 * c;  // valid columns in this block
           if (valid && nc > 0) {
             uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + row_off + 32 * c);
@@ -882,7 +904,7 @@ __global__ void __launch_bounds__(512, 1)
         }
         if (valid)
           a.lse[(static_cast<size_t>(it.b) * a.Hq + it.h) * a.T + q_idx] =
-              (mt + __log2f(lt)) * 0.69314718055994531f;
+              pad ? -INFINITY : (mt + __log2f(lt)) * 0.69314718055994531f;
         tb += it.nkv;
       }
     }

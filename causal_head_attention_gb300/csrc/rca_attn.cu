@@ -294,7 +294,8 @@ DecodeWs decode_ws_layout(int64_t B, int64_t Hq, int64_t Dh, int64_t page_size, 
 // ---------------------------------------------------------------------------
 template <bool TF32, int DHP>
 rca_status launch_fwd(const void* q, const void* k, const void* v, int64_t B, int64_t Hq, int64_t Hkv,
-                      int64_t T, int64_t Dh, void* out, float* lse, cudaStream_t st, int64_t qs, int64_t kvs) {
+                      int64_t T, int64_t Dh, void* out, float* lse, cudaStream_t st, int64_t qs, int64_t kvs,
+                      const int* lens) {
   using C = rca::FwdCfg<TF32, DHP>;
   static std::atomic<unsigned long long> smem_set{0};
   CUtensorMap mq, mk, mv;
@@ -321,6 +322,7 @@ rca_status launch_fwd(const void* q, const void* k, const void* v, int64_t B, in
   rca::FwdArgs a{};
   a.out = out;
   a.lse = lse;
+  a.lens = lens;
   a.status = status;
   a.timeout_ns = g_timeout_ns.load();
   a.B = int(B); a.Hq = int(Hq); a.Hkv = int(Hkv); a.T = int(T); a.Dh = int(Dh);
@@ -461,13 +463,13 @@ rca_status launch_bwd_main(const void* q, const void* k, const void* v, const vo
 // contiguous [B, T, H, Dh]); dkvs the same for the dK, dV outputs.
 rca_status do_fwd(const void* q, const void* k, const void* v, int64_t B, int64_t Hq, int64_t Hkv, int64_t T,
                   int64_t Dh, void* out, float* lse, rca_dtype dt, cudaStream_t st, int64_t qs = 0,
-                  int64_t kvs = 0) {
+                  int64_t kvs = 0, const int* lens = nullptr) {
   if (dt == RCA_BF16) {
-    if (Dh <= 64) return launch_fwd<false, 64>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs);
-    return launch_fwd<false, 128>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs);
+    if (Dh <= 64) return launch_fwd<false, 64>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs, lens);
+    return launch_fwd<false, 128>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs, lens);
   }
-  if (Dh <= 32) return launch_fwd<true, 32>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs);
-  return launch_fwd<true, 64>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs);
+  if (Dh <= 32) return launch_fwd<true, 32>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs, lens);
+  return launch_fwd<true, 64>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs, lens);
 }
 
 rca_status do_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
@@ -489,9 +491,12 @@ rca_status do_bwd_main(const void* q, const void* k, const void* v, const void* 
 }
 
 rca_status do_preprocess(const void* out, const float* lse, const void* dout, int64_t B, int64_t Hq, int64_t T,
-                         int64_t Dh, rca_dtype dt, void* ws, const WsLayout& L, cudaStream_t st) {
+                         int64_t Dh, rca_dtype dt, void* ws, const WsLayout& L, cudaStream_t st,
+                         const int* lens = nullptr) {
   uint8_t* w = static_cast<uint8_t*>(ws);
   rca::PreArgs a{};
+  a.lens = lens;
+  if (lens) RCA_CHECK(status_word(&a.status));
   a.out = out;
   a.lse = lse;
   a.dout = dout;
@@ -895,6 +900,47 @@ rca_status rca_attn_bwd_qkv(const void* qkv, const void* out, const float* lse, 
                         dbase + (Hq + Hkv) * Dh * es, B, Hq, Hkv, T, Dh, dt, workspace, L, st, nullptr, row, row,
                         row));
   return do_convert(dbase, B, Hq, T, Dh, dt, workspace, L, st, row);
+  RCA_GUARD_END
+}
+
+// ---------------------------------------------------------------------------
+// Padded / variable-length batches (right padding, lengths on the device)
+// ---------------------------------------------------------------------------
+rca_status rca_attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* seq_lens, int64_t B,
+                               int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, void* out, float* lse, rca_dtype dt,
+                               void* cuda_stream) {
+  RCA_GUARD_BEGIN
+  g_err.clear();
+  if (!q || !k || !v || !seq_lens || !out || !lse)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_fwd_varlen: null pointer");
+  RCA_CHECK(check_shape(B, Hq, Hkv, T, Dh, dt));
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_fwd_varlen: tensors must be 16-byte aligned, seq_lens 4-byte");
+  return do_fwd(q, k, v, B, Hq, Hkv, T, Dh, out, lse, dt, static_cast<cudaStream_t>(cuda_stream), 0, 0,
+                seq_lens);
+  RCA_GUARD_END
+}
+
+rca_status rca_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                               const void* dout, const int32_t* seq_lens, void* dq, void* dk, void* dv, int64_t B,
+                               int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt, void* workspace,
+                               size_t workspace_bytes, void* cuda_stream) {
+  RCA_GUARD_BEGIN
+  g_err.clear();
+  if (!q || !k || !v || !out || !lse || !dout || !seq_lens || !dq || !dk || !dv)
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd_varlen: null pointer");
+  RCA_CHECK(check_shape(B, Hq, Hkv, T, Dh, dt));
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd_varlen: tensors must be 16-byte aligned, seq_lens 4-byte");
+  const WsLayout L = ws_layout(B, Hq, Hkv, T, Dh, dt);
+  RCA_CHECK(check_ws(workspace, workspace_bytes, L));
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  RCA_CHECK(do_preprocess(out, lse, dout, B, Hq, T, Dh, dt, workspace, L, st, seq_lens));
+  RCA_CHECK(do_bwd_main(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, dt, workspace, L, st));
+  return do_convert(dq, B, Hq, T, Dh, dt, workspace, L, st);
   RCA_GUARD_END
 }
 

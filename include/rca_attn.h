@@ -78,8 +78,8 @@ typedef enum {
 /* Storage dtype of q/k/v/out/dout/dq/dk/dv; selects the tensor-core operand type. */
 typedef enum { RCA_F32_TF32 = 0, RCA_BF16 = 1 } rca_dtype;
 
-/* ABI version: upper 16 bits major, lower 16 bits minor (0x00010003 = 1.3). */
-#define RCA_ABI_VERSION 0x00010003u
+/* ABI version: upper 16 bits major, lower 16 bits minor (0x00010004 = 1.4). */
+#define RCA_ABI_VERSION 0x00010004u
 uint32_t rca_abi_version(void);
 
 /* Message of the last failed call on this thread ("" if none). The pointer is
@@ -166,6 +166,30 @@ rca_status rca_attn_bwd_noalloc(const void* q, const void* k, const void* v, con
                                 const float* lse, const void* dout, void* dq, void* dk, void* dv,
                                 int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
                                 rca_dtype dt, void* cuda_stream);
+
+/*
+ * Padded / variable-length batches (algo-v1-codepoint "docs/ARCHITECTURE.md",
+ * "model.py": rows where no key is allowed are zeroed and must not produce NaN).
+ * The batch holds B sequences padded on the right to T positions; sequence b
+ * is positions 0 .. seq_lens[b]-1 (0 <= seq_lens[b] <= T; int32, device memory).
+ * A padding position is neither a query nor a key:
+ *   - real rows (t < seq_lens[b]) equal causal attention over the sequence's
+ *     first seq_lens[b] positions (causality alone keeps padding keys out);
+ *   - padding rows get out = 0 and lse = -inf; their dq, dk, dv rows are 0;
+ *     their dout is ignored; seq_lens[b] = 0 gives an all-zero sequence.
+ * Inputs at padding positions are read but cannot affect real outputs as long
+ * as they are finite (e.g. zeros): a NaN or Inf there would propagate through
+ * the tensor-core products (0 * NaN). A length outside [0, T] is clamped and
+ * recorded as RCA_ERR_DEVICE_INVALID_INPUT. Same layouts, dtypes, head widths,
+ * workspace and errors as rca_attn_fwd / rca_attn_bwd otherwise.
+ */
+rca_status rca_attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* seq_lens,
+                               int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
+                               void* out, float* lse, rca_dtype dt, void* cuda_stream);
+rca_status rca_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                               const void* dout, const int32_t* seq_lens, void* dq, void* dk, void* dv,
+                               int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt,
+                               void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 /*
  * Fused QKV layout (an addition around the pages' operation: the pages project

@@ -204,3 +204,13 @@ def test_qkv_validation(lib):
     assert lib.rca_attn_bwd_qkv(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 2, 2, 64, 1, ctypes.c_void_p(1 << 20), 16,
                                 NULL) == 1
     assert "too small" in lib.rca_last_error().decode()
+
+
+def test_varlen_validation(lib):
+    assert lib.rca_attn_fwd_varlen(FAKE, FAKE, FAKE, NULL, 1, 2, 2, 8, 64, FAKE, FAKE, 1, NULL) == 1
+    assert "null" in lib.rca_last_error().decode()
+    assert lib.rca_attn_fwd_varlen(FAKE, FAKE, FAKE, ctypes.c_void_p(4098), 1, 2, 2, 8, 64, FAKE, FAKE, 1, NULL) == 1
+    assert "4-byte" in lib.rca_last_error().decode()
+    assert lib.rca_attn_bwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 2, 0, 64, 1,
+                                   ctypes.c_void_p(1 << 20), 1 << 30, NULL) == 1
+    assert "fully masked" in lib.rca_last_error().decode()
