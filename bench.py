@@ -418,8 +418,13 @@ def run_gpu(args, w, world, rank, local):
                "sample": f"{n} of {w.B * w.Hkv} (batch, KV-head) groups of the same workload, fwd+bwd, fp64, "
                          f"{dt:.1f} s"}
 
+    fused_qkv = varlen = None
+    if rank == 0 and not args.no_extras:
+        fused_qkv = bench_fused_qkv(w, dev, stream, max(5, args.steps // 2), 3)
+        varlen = bench_varlen(w, dev, stream, max(5, args.steps // 2), 3)
+
     mat = None
-    if rank == 0 and not args.no_materialized and w.B * w.Hq * w.T * w.T * 4 <= 2 ** 31:
+    if rank == 0 and not args.no_extras and w.B * w.Hq * w.T * w.T * 4 <= 2 ** 31:
         mat = bench_materialized(w, dev, stream, max(3, args.steps // 5), 2, P)
 
     decode = None
@@ -448,10 +453,100 @@ def run_gpu(args, w, world, rank, local):
             "gpu_launches": 4 * args.steps,
             "paged_decode": decode,
             "materialized": mat,
+            "fused_qkv": fused_qkv,
+            "varlen": varlen,
             "src_digest": src_digest(),
         }
         print(json.dumps(line), flush=True)
     return 0
+
+
+def bench_varlen(w, dev, stream, steps, warmup):
+    """Variable-length batch on the workload's shape: sequence lengths drawn
+    uniform in [1, T] (seeded), right padding. Padding rows are computed and
+    zeroed (no tile is skipped), so the step costs what the dense step costs;
+    the effective rate counts only the causal work of the real tokens."""
+    import causal_head_attention_gb300 as rca
+
+    q0, k0, v0, do0 = make_inputs(w)
+    q, k, v, do = (x.to(dev) for x in (q0, k0, v0, do0))
+    g = torch.Generator().manual_seed(w.seed + 100)
+    lens_h = torch.randint(1, w.T + 1, (w.B,), generator=g, dtype=torch.int32)
+    lens = lens_h.to(dev)
+    out, lse = torch.empty_like(q), torch.empty((w.B, w.Hq, w.T), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = rca.workspace_for(q, k)
+
+    def step():
+        rca.rca_attn_fwd_varlen(q, k, v, lens, out, lse, stream)
+        rca.rca_attn_bwd_varlen(q, k, v, out, lse, do, lens, dq, dk, dv, ws, stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    rca.rca_stream_status(stream)
+    ms = a.elapsed_time(b) / steps
+    real_flops = 3.5 * sum(4.0 * w.Hq * int(n) * int(n) * w.Dh / 2.0 for n in lens_h)
+    return {"workload": w.describe(), "lens": [int(x) for x in lens_h], "ms_per_step": ms,
+            "effective_tflops": real_flops / (ms * 1e-3) / 1e12,
+            "note": "padding rows computed then zeroed; effective rate counts real tokens only"}
+
+
+def bench_fused_qkv(w, dev, stream, steps, warmup):
+    """Fused projection layout on one workload: a training step (forward +
+    backward) reading q, k, v in place from qkv [B,T,(Hq+2Hkv)Dh] and writing
+    dqkv in place, against the same step with the split and concatenation
+    copies a caller of the separate-tensor entry points would need."""
+    import causal_head_attention_gb300 as rca
+
+    q0, k0, v0, do0 = make_inputs(w)
+    B, T, Hq, Dh, Hkv = w.B, w.T, w.Hq, w.Dh, w.Hkv
+    qkv = torch.cat([q0.reshape(B, T, -1), k0.reshape(B, T, -1), v0.reshape(B, T, -1)], dim=2).to(dev)
+    dout = do0.reshape(B, T, Hq * Dh).to(dev)
+    out = torch.empty((B, T, Hq * Dh), dtype=qkv.dtype, device=dev)
+    lse = torch.empty((B, Hq, T), dtype=torch.float32, device=dev)
+    dqkv = torch.empty_like(qkv)
+    ws = torch.empty(rca.rca_attn_bwd_workspace_size(B, Hq, Hkv, T, Dh, qkv.dtype), dtype=torch.uint8, device=dev)
+
+    def fused():
+        rca.rca_attn_fwd_qkv(qkv, Hq, Hkv, out, lse, stream)
+        rca.rca_attn_bwd_qkv(qkv, Hq, Hkv, out, lse, dout, dqkv, ws, stream)
+
+    def with_copies():
+        q = qkv[:, :, : Hq * Dh].reshape(B, T, Hq, Dh).contiguous()
+        k = qkv[:, :, Hq * Dh: (Hq + Hkv) * Dh].reshape(B, T, Hkv, Dh).contiguous()
+        v = qkv[:, :, (Hq + Hkv) * Dh:].reshape(B, T, Hkv, Dh).contiguous()
+        o = torch.empty_like(q)
+        rca.rca_attn_fwd(q, k, v, o, lse, stream)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        rca.rca_attn_bwd(q, k, v, o, lse, dout.reshape(B, T, Hq, Dh), dq, dk, dv, ws, stream)
+        torch.cat([dq.reshape(B, T, -1), dk.reshape(B, T, -1), dv.reshape(B, T, -1)], dim=2, out=dqkv)
+
+    res = {}
+    for name, fn in (("fused", fused), ("separate_with_copies", with_copies)):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        rca.rca_stream_status(stream)
+        ms = a.elapsed_time(b) / steps
+        res[name] = {"ms_per_step": ms, "tflops": 3.5 * fwd_flops(w) / (ms * 1e-3) / 1e12}
+    res["workload"] = w.describe()
+    res["note"] = "inputs stay in L2 between steps here (one buffer set); compare the two arms, not the headline"
+    return res
 
 
 def bench_materialized(w, dev, stream, steps, warmup, P):
@@ -637,7 +732,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the paged decode measurement")
-    ap.add_argument("--no-materialized", action="store_true", help="skip the materialized-path measurement")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the fused-layout, variable-length and materialized-path measurements")
     ap.add_argument("--decode-steps", type=int, default=50)
     ap.add_argument("--decode-cpu-budget", type=float, default=3.0)
     args = ap.parse_args()
