@@ -24,6 +24,7 @@ from ._native import (  # noqa: F401  (C-ABI names)
     rca_attn_fwd_qkv,
     rca_attn_fwd_varlen,
     rca_attn_materialized_bwd,
+    rca_attn_varlen_workspace_size,
     rca_attn_materialized_fwd,
     rca_attn_materialized_workspace_size,
     rca_causal_softmax,
@@ -59,6 +60,7 @@ __all__ = [
     "attention_backward_varlen",
     "rca_attn_fwd_varlen",
     "rca_attn_bwd_varlen",
+    "rca_attn_varlen_workspace_size",
     "materialized_forward",
     "materialized_backward",
     "rca_attn_materialized_fwd",
@@ -159,7 +161,15 @@ def paged_decode(q, k_pool, v_pool, page_table, seq_lens, workspace=None, stream
     return out, lse
 
 
-def attention_forward_varlen(q, k, v, seq_lens, stream=None):
+def varlen_workspace_for(q, k):
+    import torch
+
+    B, T, Hq, Dh = q.shape
+    n = rca_attn_varlen_workspace_size(B, Hq, k.shape[2], T, Dh, q.dtype)
+    return torch.empty(n, dtype=torch.uint8, device=q.device)
+
+
+def attention_forward_varlen(q, k, v, seq_lens, workspace=None, stream=None):
     """Right-padded batch with per-sequence lengths seq_lens (int32 [B], device).
     Returns (out, lse); padding rows are zero, their LSE -inf."""
     import torch
@@ -167,7 +177,8 @@ def attention_forward_varlen(q, k, v, seq_lens, stream=None):
     B, T, Hq, Dh = q.shape
     out = torch.empty_like(q)
     lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
-    rca_attn_fwd_varlen(q, k, v, seq_lens, out, lse, stream)
+    ws = workspace if workspace is not None else varlen_workspace_for(q, k)
+    rca_attn_fwd_varlen(q, k, v, seq_lens, out, lse, ws, stream)
     return out, lse
 
 
@@ -176,7 +187,7 @@ def attention_backward_varlen(q, k, v, out, lse, dout, seq_lens, workspace=None,
     import torch
 
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = workspace if workspace is not None else workspace_for(q, k)
+    ws = workspace if workspace is not None else varlen_workspace_for(q, k)
     rca_attn_bwd_varlen(q, k, v, out, lse, dout.contiguous(), seq_lens, dq, dk, dv, ws, stream)
     return dq, dk, dv
 

@@ -62,7 +62,9 @@ _SIG = {
     "rca_attn_fwd_qkv": (ctypes.c_int, [_P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_int, _P]),
     "rca_attn_bwd_qkv": (ctypes.c_int, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_int, _P, ctypes.c_size_t,
                                         _P]),
-    "rca_attn_fwd_varlen": (ctypes.c_int, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_int, _P]),
+    "rca_attn_varlen_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I, _I, ctypes.c_int]),
+    "rca_attn_fwd_varlen": (ctypes.c_int, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_int, _P,
+                                           ctypes.c_size_t, _P]),
     "rca_attn_bwd_varlen": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                            ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "rca_selftest_device_timeout": (ctypes.c_int, [_P]),
@@ -314,11 +316,20 @@ def _check_lens(seq_lens, B):
         raise ValueError("seq_lens must be int32 [B]")
 
 
-def rca_attn_fwd_varlen(q, k, v, seq_lens, out, lse, stream=None):
+def rca_attn_varlen_workspace_size(B, Hq, Hkv, T, Dh, dt) -> int:
+    """dt: RCA_BF16 / RCA_F32_TF32, or a torch dtype."""
+    if not isinstance(dt, int):
+        torch = _torch()
+        dt = RCA_BF16 if dt == torch.bfloat16 else RCA_F32_TF32
+    return lib().rca_attn_varlen_workspace_size(B, Hq, Hkv, T, Dh, dt)
+
+
+def rca_attn_fwd_varlen(q, k, v, seq_lens, out, lse, workspace, stream=None):
     B, Hq, Hkv, T, Dh = _shape(q, k)
     _check_lens(seq_lens, B)
     _check(lib().rca_attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), B, Hq, Hkv, T, Dh, _ptr(out),
-                                     _ptr(lse), _dtype_code(q), _stream(stream)))
+                                     _ptr(lse), _dtype_code(q), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def rca_attn_bwd_varlen(q, k, v, out, lse, dout, seq_lens, dq, dk, dv, workspace, stream=None):

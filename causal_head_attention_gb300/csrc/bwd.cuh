@@ -272,6 +272,8 @@ struct BwdArgs {
   void* dk;
   void* dv;
   long long dkv_row;   // elements between consecutive positions of dK, dV (Hkv * Dh if contiguous)
+  const int4* items;       // variable-length batches: work list {b, kvh, j, n_i} (null: all items)
+  const int* n_items_dev;  // its length (device)
   float* dq_acc;       // [B, T, Hq, Dh]
   const float* lse2;   // [B, Hq, Tpad]
   const float* dvec;   // [B, Hq, Tpad]
@@ -293,6 +295,16 @@ struct BwdItem {
 __device__ __forceinline__ bool bwd_item(const BwdArgs& a, int k, BwdItem& it) {
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
   const long long idx = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
+  if (a.items) {  // variable-length batch: the planned list (tiles of padding left out)
+    if (idx >= __ldg(a.n_items_dev)) return false;
+    const int4 e = __ldg(a.items + idx);
+    it.b = e.x;
+    it.kvh = e.y;
+    it.j = e.z;
+    it.n_i = e.w;
+    it.n_it = a.group * it.n_i;
+    return true;
+  }
   if (idx >= a.n_items) return false;
   const int bk_count = a.B * a.Hkv;
   it.j = static_cast<int>(idx / bk_count);
@@ -338,6 +350,8 @@ __global__ void __launch_bounds__(512, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 8 * C::NBAR + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // A CTA past the end of a planned work list has no item at all.
+  if (a.items && static_cast<int>(blockIdx.x) >= __ldg(a.n_items_dev)) return;
 
   if (threadIdx.x == 0) {
     for (int x = 0; x < C::KVB; ++x) {

@@ -160,6 +160,8 @@ struct FwdArgs {
   void* out;
   float* lse;
   const int* lens;  // per-sequence lengths (right padding), or null: rows t >= lens[b] are padding
+  const int4* items;     // variable-length batches: work list {b, h, qt, -} (null: all items)
+  const int* n_items_dev;  // its length (device)
   int* status;
   unsigned long long timeout_ns;
   int B, Hq, Hkv, T, Dh, group, n_qt;
@@ -186,6 +188,16 @@ __device__ __forceinline__ int seq_len(const FwdArgs& a, int b) {
 __device__ __forceinline__ bool fwd_item(const FwdArgs& a, int k, FwdItem& it) {
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
   const long long idx = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
+  if (a.items) {  // variable-length batch: the planned list (tiles of padding left out)
+    if (idx >= __ldg(a.n_items_dev)) return false;
+    const int4 e = __ldg(a.items + idx);
+    it.b = e.x;
+    it.h = e.y;
+    it.qt = e.z;
+    it.nkv = it.qt + 1;
+    it.kvh = it.h / a.group;
+    return true;
+  }
   if (idx >= a.n_items) return false;
   const int bh_count = a.B * a.Hq;
   const int level = static_cast<int>(idx / bh_count), bh = static_cast<int>(idx % bh_count);
@@ -244,6 +256,8 @@ __global__ void __launch_bounds__(512, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 8 * C::NBAR + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // A CTA past the end of a planned work list has no item at all.
+  if (a.items && static_cast<int>(blockIdx.x) >= __ldg(a.n_items_dev)) return;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::QB; ++i) {

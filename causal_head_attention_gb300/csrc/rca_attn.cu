@@ -17,6 +17,7 @@
 #include "decode.h"
 #include "fwd.cuh"
 #include "materialized.h"
+#include "varlen.cuh"
 
 namespace rca {
 // Failure-detection self-test: one warp waits, with the same time-bounded wait
@@ -295,7 +296,7 @@ DecodeWs decode_ws_layout(int64_t B, int64_t Hq, int64_t Dh, int64_t page_size, 
 template <bool TF32, int DHP>
 rca_status launch_fwd(const void* q, const void* k, const void* v, int64_t B, int64_t Hq, int64_t Hkv,
                       int64_t T, int64_t Dh, void* out, float* lse, cudaStream_t st, int64_t qs, int64_t kvs,
-                      const int* lens) {
+                      const int* lens, const int4* items, const int* n_items_dev) {
   using C = rca::FwdCfg<TF32, DHP>;
   static std::atomic<unsigned long long> smem_set{0};
   CUtensorMap mq, mk, mv;
@@ -323,6 +324,8 @@ rca_status launch_fwd(const void* q, const void* k, const void* v, int64_t B, in
   a.out = out;
   a.lse = lse;
   a.lens = lens;
+  a.items = items;
+  a.n_items_dev = n_items_dev;
   a.status = status;
   a.timeout_ns = g_timeout_ns.load();
   a.B = int(B); a.Hq = int(Hq); a.Hkv = int(Hkv); a.T = int(T); a.Dh = int(Dh);
@@ -370,7 +373,7 @@ template <bool HL, int DHB>
 rca_status launch_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
                            int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, void* ws,
                            const WsLayout& L, cudaStream_t st, int* status_override, int64_t qs, int64_t kvs,
-                           int64_t dkvs) {
+                           int64_t dkvs, const int4* items, const int* n_items_dev) {
   using C = rca::BwdCfg<HL, DHB>;
   static std::atomic<unsigned long long> smem_set{0};
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -433,6 +436,8 @@ rca_status launch_bwd_main(const void* q, const void* k, const void* v, const vo
   a.dk = dk;
   a.dv = dv;
   a.dkv_row = dkvs;
+  a.items = items;
+  a.n_items_dev = n_items_dev;
   a.dq_acc = reinterpret_cast<float*>(w + L.dq_off);
   a.lse2 = reinterpret_cast<const float*>(w + L.lse2_off);
   a.dvec = reinterpret_cast<const float*>(w + L.d_off);
@@ -463,31 +468,106 @@ rca_status launch_bwd_main(const void* q, const void* k, const void* v, const vo
 // contiguous [B, T, H, Dh]); dkvs the same for the dK, dV outputs.
 rca_status do_fwd(const void* q, const void* k, const void* v, int64_t B, int64_t Hq, int64_t Hkv, int64_t T,
                   int64_t Dh, void* out, float* lse, rca_dtype dt, cudaStream_t st, int64_t qs = 0,
-                  int64_t kvs = 0, const int* lens = nullptr) {
+                  int64_t kvs = 0, const int* lens = nullptr, const int4* items = nullptr,
+                  const int* n_items_dev = nullptr) {
   if (dt == RCA_BF16) {
-    if (Dh <= 64) return launch_fwd<false, 64>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs, lens);
-    return launch_fwd<false, 128>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs, lens);
+    if (Dh <= 64)
+      return launch_fwd<false, 64>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs, lens, items, n_items_dev);
+    return launch_fwd<false, 128>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs, lens, items, n_items_dev);
   }
-  if (Dh <= 32) return launch_fwd<true, 32>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs, lens);
-  return launch_fwd<true, 64>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs, lens);
+  if (Dh <= 32)
+    return launch_fwd<true, 32>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs, lens, items, n_items_dev);
+  return launch_fwd<true, 64>(q, k, v, B, Hq, Hkv, T, Dh, out, lse, st, qs, kvs, lens, items, n_items_dev);
 }
 
 rca_status do_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
                        int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt, void* ws,
                        const WsLayout& L, cudaStream_t st, int* status_override = nullptr, int64_t qs = 0,
-                       int64_t kvs = 0, int64_t dkvs = 0) {
+                       int64_t kvs = 0, int64_t dkvs = 0, const int4* items = nullptr,
+                       const int* n_items_dev = nullptr) {
   if (qs == 0) qs = Hq * Dh;
   if (kvs == 0) kvs = Hkv * Dh;
   if (dkvs == 0) dkvs = Hkv * Dh;
   if (dt == RCA_BF16) {
     if (Dh <= 64)
       return launch_bwd_main<false, 64>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st, status_override, qs,
-                                        kvs, dkvs);
+                                        kvs, dkvs, items, n_items_dev);
     return launch_bwd_main<false, 128>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st, status_override, qs,
-                                       kvs, dkvs);
+                                       kvs, dkvs, items, n_items_dev);
   }
   return launch_bwd_main<true, 64>(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st, status_override, qs, kvs,
-                                   dkvs);
+                                   dkvs, items, n_items_dev);
+}
+
+// ---------------------------------------------------------------------------
+// Variable-length batches: planned work lists (after the backward's scratch)
+// ---------------------------------------------------------------------------
+constexpr int64_t kVarlenMaxBatch = 4096, kVarlenMaxT = 131072;
+
+struct VarlenLayout {
+  size_t fwd_items, bwd_items, counts, total;  // offsets past the backward scratch
+};
+
+VarlenLayout varlen_layout(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt) {
+  VarlenLayout v{};
+  const size_t n_qt = size_t((T + 127) / 128);
+  v.fwd_items = round256(ws_layout(B, Hq, Hkv, T, Dh, dt).total);
+  v.bwd_items = v.fwd_items + round256(size_t(B) * Hq * n_qt * 16);
+  v.counts = v.bwd_items + round256(size_t(B) * Hkv * n_qt * 16);
+  v.total = v.counts + 256;
+  return v;
+}
+
+rca_status check_varlen(int64_t B, int64_t T) {
+  if (B > kVarlenMaxBatch || T > kVarlenMaxT)
+    return fail(RCA_ERR_UNSUPPORTED, "variable-length batches take B <= %lld and T <= %lld (got B=%lld T=%lld)",
+                (long long)kVarlenMaxBatch, (long long)kVarlenMaxT, (long long)B, (long long)T);
+  return RCA_OK;
+}
+
+// Builds both work lists from the lengths; returns their device pointers.
+rca_status plan_varlen(const int* lens, int64_t B, int64_t Hq, int64_t Hkv, int64_t T, void* ws, const VarlenLayout& V,
+                       cudaStream_t st, const int4** fwd_items, const int** fwd_count, const int4** bwd_items,
+                       const int** bwd_count) {
+  char* w = static_cast<char*>(ws);
+  rca::VarlenPlanArgs a{};
+  a.lens = lens;
+  a.fwd_items = reinterpret_cast<int4*>(w + V.fwd_items);
+  a.bwd_items = reinterpret_cast<int4*>(w + V.bwd_items);
+  a.fwd_count = reinterpret_cast<int*>(w + V.counts);
+  a.bwd_count = a.fwd_count + 1;
+  RCA_CHECK(status_word(&a.status));
+  a.B = int(B);
+  a.Hq = int(Hq);
+  a.Hkv = int(Hkv);
+  a.T = int(T);
+  a.n_qt = int((T + 127) / 128);
+  const size_t smem = (2 * size_t(B) + 3 * (size_t(a.n_qt) + 1)) * sizeof(int);
+  rca::varlen_plan_kernel<<<1, rca::kVarlenPlanThreads, smem, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch varlen_plan_kernel");
+  *fwd_items = a.fwd_items;
+  *fwd_count = a.fwd_count;
+  *bwd_items = a.bwd_items;
+  *bwd_count = a.bwd_count;
+  return RCA_OK;
+}
+
+// Zero the rows at or past each sequence's length (and -inf LSE) of x [B, T, H, Dh].
+rca_status zero_padding(void* x, float* lse, const int* lens, int64_t B, int64_t T, int64_t H, int64_t Dh,
+                        rca_dtype dt, cudaStream_t st) {
+  const int64_t nvec = B * T * H * Dh * (dt == RCA_BF16 ? 2 : 4) / 16;
+  int sms = 0;
+  RCA_CHECK(sm_count(&sms));
+  const int64_t want = (nvec + 255) / 256, cap = int64_t(sms) * 8;
+  const unsigned grid = unsigned(want < cap ? (want > 0 ? want : 1) : cap);
+  if (dt == RCA_BF16)
+    rca::varlen_zero_kernel<2><<<grid, 256, 0, st>>>(x, lse, lens, int(B), int(T), int(H), int(Dh));
+  else
+    rca::varlen_zero_kernel<4><<<grid, 256, 0, st>>>(x, lse, lens, int(B), int(T), int(H), int(Dh));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch varlen_zero_kernel");
+  return RCA_OK;
 }
 
 rca_status do_preprocess(const void* out, const float* lse, const void* dout, int64_t B, int64_t Hq, int64_t T,
@@ -906,19 +986,34 @@ rca_status rca_attn_bwd_qkv(const void* qkv, const void* out, const float* lse, 
 // ---------------------------------------------------------------------------
 // Padded / variable-length batches (right padding, lengths on the device)
 // ---------------------------------------------------------------------------
+size_t rca_attn_varlen_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hkv > Hq || T < 1 || Dh < 1 || B > kVarlenMaxBatch || T > kVarlenMaxT) return 0;
+  if (dt != RCA_BF16 && dt != RCA_F32_TF32) return 0;
+  return varlen_layout(B, Hq, Hkv, T, Dh, dt).total;
+}
+
 rca_status rca_attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* seq_lens, int64_t B,
                                int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, void* out, float* lse, rca_dtype dt,
-                               void* cuda_stream) {
+                               void* workspace, size_t workspace_bytes, void* cuda_stream) {
   RCA_GUARD_BEGIN
   g_err.clear();
   if (!q || !k || !v || !seq_lens || !out || !lse)
     return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_fwd_varlen: null pointer");
   RCA_CHECK(check_shape(B, Hq, Hkv, T, Dh, dt));
+  RCA_CHECK(check_varlen(B, T));
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) ||
       (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
     return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_fwd_varlen: tensors must be 16-byte aligned, seq_lens 4-byte");
-  return do_fwd(q, k, v, B, Hq, Hkv, T, Dh, out, lse, dt, static_cast<cudaStream_t>(cuda_stream), 0, 0,
-                seq_lens);
+  const VarlenLayout V = varlen_layout(B, Hq, Hkv, T, Dh, dt);
+  WsLayout W{};
+  W.total = V.total;
+  RCA_CHECK(check_ws(workspace, workspace_bytes, W));
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  const int4 *fi = nullptr, *bi = nullptr;
+  const int *fc = nullptr, *bc = nullptr;
+  RCA_CHECK(plan_varlen(seq_lens, B, Hq, Hkv, T, workspace, V, st, &fi, &fc, &bi, &bc));
+  RCA_CHECK(do_fwd(q, k, v, B, Hq, Hkv, T, Dh, out, lse, dt, st, 0, 0, seq_lens, fi, fc));
+  return zero_padding(out, lse, seq_lens, B, T, Hq, Dh, dt, st);
   RCA_GUARD_END
 }
 
@@ -931,16 +1026,25 @@ rca_status rca_attn_bwd_varlen(const void* q, const void* k, const void* v, cons
   if (!q || !k || !v || !out || !lse || !dout || !seq_lens || !dq || !dk || !dv)
     return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd_varlen: null pointer");
   RCA_CHECK(check_shape(B, Hq, Hkv, T, Dh, dt));
+  RCA_CHECK(check_varlen(B, T));
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) ||
       !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
       (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
     return fail(RCA_ERR_INVALID_ARGUMENT, "rca_attn_bwd_varlen: tensors must be 16-byte aligned, seq_lens 4-byte");
   const WsLayout L = ws_layout(B, Hq, Hkv, T, Dh, dt);
-  RCA_CHECK(check_ws(workspace, workspace_bytes, L));
+  const VarlenLayout V = varlen_layout(B, Hq, Hkv, T, Dh, dt);
+  WsLayout W = L;
+  W.total = V.total;
+  RCA_CHECK(check_ws(workspace, workspace_bytes, W));
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  const int4 *fi = nullptr, *bi = nullptr;
+  const int *fc = nullptr, *bc = nullptr;
+  RCA_CHECK(plan_varlen(seq_lens, B, Hq, Hkv, T, workspace, V, st, &fi, &fc, &bi, &bc));
   RCA_CHECK(do_preprocess(out, lse, dout, B, Hq, T, Dh, dt, workspace, L, st, seq_lens));
-  RCA_CHECK(do_bwd_main(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, dt, workspace, L, st));
-  return do_convert(dq, B, Hq, T, Dh, dt, workspace, L, st);
+  RCA_CHECK(do_bwd_main(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, dt, workspace, L, st, nullptr, 0, 0, 0, bi, bc));
+  RCA_CHECK(do_convert(dq, B, Hq, T, Dh, dt, workspace, L, st));
+  RCA_CHECK(zero_padding(dk, nullptr, seq_lens, B, T, Hkv, Dh, dt, st));
+  return zero_padding(dv, nullptr, seq_lens, B, T, Hkv, Dh, dt, st);
   RCA_GUARD_END
 }
 

@@ -1,0 +1,137 @@
+// Variable-length batches: work lists that leave out the tiles made only of
+// padding, and the zero fill of the rows those tiles would have written.
+//
+// A batch of B sequences is right-padded to T positions; sequence b has
+// nq_b = ceil(L_b / 128) tiles of 128 positions that hold real tokens.
+//  * forward items (b, h, qt) exist for qt < nq_b; an item of query tile qt
+//    has qt + 1 key tiles, so the list is ordered by decreasing qt (the order
+//    the dense schedule uses, longest items first);
+//  * backward items (b, kvh, j) exist for key tiles j < nq_b and iterate over
+//    the n_i = nq_b - j query tiles j .. nq_b - 1, so the list is ordered by
+//    decreasing n_i.
+// One CTA builds both lists: a counting sort of the sequences by nq_b gives,
+// for every level, the sequences that reach it as a prefix of the sorted
+// order, and prefix sums over the levels give where each level starts.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "tc.cuh"
+
+namespace rca {
+
+constexpr int kVarlenPlanThreads = 1024;
+
+struct VarlenPlanArgs {
+  const int* lens;
+  int4* fwd_items;  // {b, h, qt, 0}
+  int* fwd_count;
+  int4* bwd_items;  // {b, kvh, j, n_i}
+  int* bwd_count;
+  int* status;
+  int B, Hq, Hkv, T, n_qt;
+};
+
+// Dynamic shared memory: nq[B], order[B], cnt[n_qt + 1] (#sequences with
+// nq_b > l for level l), fwd_off[n_qt + 1], bwd_off[n_qt + 1].
+__global__ void __launch_bounds__(kVarlenPlanThreads) varlen_plan_kernel(const VarlenPlanArgs a) {
+  extern __shared__ int sm[];
+  int* nq = sm;
+  int* order = nq + a.B;
+  int* cnt = order + a.B;           // cnt[l] = #{b : nq_b > l}, l = 0 .. n_qt
+  int* fwd_off = cnt + a.n_qt + 1;  // start of forward level l (qt = n_qt - 1 - l)
+  int* bwd_off = fwd_off + a.n_qt + 1;  // start of backward level l (n_i = n_qt - l)
+  const int tid = threadIdx.x;
+  for (int l = tid; l <= a.n_qt; l += blockDim.x) cnt[l] = 0;
+  __syncthreads();
+  for (int b = tid; b < a.B; b += blockDim.x) {
+    int L = __ldg(a.lens + b);
+    if (L < 0 || L > a.T) {
+      atomicExch(a.status, kStatusBadInput);
+      L = L < 0 ? 0 : a.T;
+    }
+    nq[b] = (L + 127) / 128;
+    atomicAdd(&cnt[nq[b]], 1);  // histogram of nq for now
+  }
+  __syncthreads();
+  if (tid == 0) {
+    // Counting sort by decreasing nq: first slot of each value's run.
+    int pos = 0;
+    for (int v = a.n_qt; v >= 0; --v) {
+      const int c = cnt[v];
+      cnt[v] = pos;
+      pos += c;
+    }
+  }
+  __syncthreads();
+  for (int b = tid; b < a.B; b += blockDim.x) order[atomicAdd(&cnt[nq[b]], 1)] = b;
+  __syncthreads();
+  if (tid == 0) {
+    // cnt[v] is now the end of value v's run = #{b : nq_b >= v}; shift to
+    // #{b : nq_b > l} = #{b : nq_b >= l + 1}, then the level offsets.
+    for (int l = 0; l < a.n_qt; ++l) cnt[l] = cnt[l + 1];
+    cnt[a.n_qt] = 0;
+    int f = 0, g = 0;
+    for (int l = 0; l < a.n_qt; ++l) {
+      fwd_off[l] = f;
+      f += a.Hq * cnt[a.n_qt - 1 - l];  // query tile qt = n_qt - 1 - l: sequences with nq_b > qt
+      bwd_off[l] = g;
+      g += a.Hkv * cnt[a.n_qt - 1 - l];  // n_i = n_qt - l: sequences with nq_b >= n_i
+    }
+    fwd_off[a.n_qt] = f;
+    bwd_off[a.n_qt] = g;
+    *a.fwd_count = f;
+    *a.bwd_count = g;
+  }
+  __syncthreads();
+  // Entry e of a level: rank r = e / heads among the sorted sequences that
+  // reach the level, head e % heads.
+  auto level_of = [&](const int* off, int e) {
+    int lo = 0, hi = a.n_qt;  // off[lo] <= e < off[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (off[mid] <= e) lo = mid;
+      else hi = mid;
+    }
+    return lo;
+  };
+  const int nf = fwd_off[a.n_qt];
+  for (int e = tid; e < nf; e += blockDim.x) {
+    const int l = level_of(fwd_off, e), r = (e - fwd_off[l]) / a.Hq, h = (e - fwd_off[l]) % a.Hq;
+    a.fwd_items[e] = make_int4(order[r], h, a.n_qt - 1 - l, 0);
+  }
+  const int nb = bwd_off[a.n_qt];
+  for (int e = tid; e < nb; e += blockDim.x) {
+    const int l = level_of(bwd_off, e), r = (e - bwd_off[l]) / a.Hkv, kvh = (e - bwd_off[l]) % a.Hkv;
+    const int b = order[r], ni = a.n_qt - l;
+    a.bwd_items[e] = make_int4(b, kvh, nq[b] - ni, ni);
+  }
+}
+
+// Zero the rows of positions t >= L_b of a [B, T, H, Dh] tensor (storage
+// dtype, ES bytes) and, if lse is given, set lse[b, h, t] = -inf there. One
+// thread per 16 bytes.
+template <int ES>
+__global__ void __launch_bounds__(256)
+    varlen_zero_kernel(void* __restrict__ x, float* __restrict__ lse, const int* __restrict__ lens, int B, int T,
+                       int H, int Dh) {
+  const long long vec_per_row = static_cast<long long>(H) * Dh * ES / 16;
+  const long long n = static_cast<long long>(B) * T * vec_per_row;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = i / vec_per_row;
+    const int t = static_cast<int>(row % T), b = static_cast<int>(row / T);
+    int L = __ldg(lens + b);
+    L = L < 0 ? 0 : (L > T ? T : L);
+    if (t < L) continue;
+    reinterpret_cast<uint4*>(x)[i] = make_uint4(0, 0, 0, 0);
+    const int v = static_cast<int>(i % vec_per_row);
+    if (lse && v * 16 / ES % Dh == 0) {
+      const int h = v * 16 / ES / Dh;
+      lse[(static_cast<long long>(b) * H + h) * T + t] = -INFINITY;
+    }
+  }
+}
+
+}  // namespace rca

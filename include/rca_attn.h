@@ -78,8 +78,8 @@ typedef enum {
 /* Storage dtype of q/k/v/out/dout/dq/dk/dv; selects the tensor-core operand type. */
 typedef enum { RCA_F32_TF32 = 0, RCA_BF16 = 1 } rca_dtype;
 
-/* ABI version: upper 16 bits major, lower 16 bits minor (0x00010004 = 1.4). */
-#define RCA_ABI_VERSION 0x00010004u
+/* ABI version: upper 16 bits major, lower 16 bits minor (0x00010005 = 1.5). */
+#define RCA_ABI_VERSION 0x00010005u
 uint32_t rca_abi_version(void);
 
 /* Message of the last failed call on this thread ("" if none). The pointer is
@@ -180,12 +180,19 @@ rca_status rca_attn_bwd_noalloc(const void* q, const void* k, const void* v, con
  * Inputs at padding positions are read but cannot affect real outputs as long
  * as they are finite (e.g. zeros): a NaN or Inf there would propagate through
  * the tensor-core products (0 * NaN). A length outside [0, T] is clamped and
- * recorded as RCA_ERR_DEVICE_INVALID_INPUT. Same layouts, dtypes, head widths,
- * workspace and errors as rca_attn_fwd / rca_attn_bwd otherwise.
+ * recorded as RCA_ERR_DEVICE_INVALID_INPUT. Tiles of 128 positions made only of
+ * padding are not computed: both calls first plan the work from seq_lens on the
+ * device, and the rows of those tiles are written as zeros.
+ * workspace: at least rca_attn_varlen_workspace_size(...) bytes for either call
+ * (the backward's scratch plus the work lists), 256-byte aligned, contents on
+ * entry irrelevant. B <= 4096 and T <= 131072 (else RCA_ERR_UNSUPPORTED). Same
+ * layouts, dtypes, head widths and errors as rca_attn_fwd / rca_attn_bwd otherwise.
  */
+size_t rca_attn_varlen_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt);
 rca_status rca_attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* seq_lens,
                                int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
-                               void* out, float* lse, rca_dtype dt, void* cuda_stream);
+                               void* out, float* lse, rca_dtype dt,
+                               void* workspace, size_t workspace_bytes, void* cuda_stream);
 rca_status rca_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* out, const float* lse,
                                const void* dout, const int32_t* seq_lens, void* dq, void* dk, void* dv,
                                int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt,

@@ -207,10 +207,18 @@ def test_qkv_validation(lib):
 
 
 def test_varlen_validation(lib):
-    assert lib.rca_attn_fwd_varlen(FAKE, FAKE, FAKE, NULL, 1, 2, 2, 8, 64, FAKE, FAKE, 1, NULL) == 1
+    WS, WB = ctypes.c_void_p(1 << 20), 1 << 30
+    assert lib.rca_attn_fwd_varlen(FAKE, FAKE, FAKE, NULL, 1, 2, 2, 8, 64, FAKE, FAKE, 1, WS, WB, NULL) == 1
     assert "null" in lib.rca_last_error().decode()
-    assert lib.rca_attn_fwd_varlen(FAKE, FAKE, FAKE, ctypes.c_void_p(4098), 1, 2, 2, 8, 64, FAKE, FAKE, 1, NULL) == 1
+    assert lib.rca_attn_fwd_varlen(FAKE, FAKE, FAKE, ctypes.c_void_p(4098), 1, 2, 2, 8, 64, FAKE, FAKE, 1, WS, WB,
+                                   NULL) == 1
     assert "4-byte" in lib.rca_last_error().decode()
+    assert lib.rca_attn_fwd_varlen(FAKE, FAKE, FAKE, FAKE, 5000, 2, 2, 8, 64, FAKE, FAKE, 1, WS, WB, NULL) == 2
+    assert "B <= 4096" in lib.rca_last_error().decode()
+    assert lib.rca_attn_fwd_varlen(FAKE, FAKE, FAKE, FAKE, 1, 2, 2, 8, 64, FAKE, FAKE, 1, WS, 64, NULL) == 1
+    assert "too small" in lib.rca_last_error().decode()
+    assert lib.rca_attn_varlen_workspace_size(4, 16, 16, 2048, 64, 1) > lib.rca_attn_bwd_workspace_size(
+        4, 16, 16, 2048, 64, 1)
     assert lib.rca_attn_bwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 2, 0, 64, 1,
                                    ctypes.c_void_p(1 << 20), 1 << 30, NULL) == 1
     assert "fully masked" in lib.rca_last_error().decode()
