@@ -292,10 +292,11 @@ struct BwdArgs {
 struct BwdItem {
   int b, kvh, j, n_i, n_it;
 };
+template <bool LIST>
 __device__ __forceinline__ bool bwd_item(const BwdArgs& a, int k, BwdItem& it) {
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
   const long long idx = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
-  if (a.items) {  // variable-length batch: the planned list (tiles of padding left out)
+  if constexpr (LIST) {  // variable-length batch: the planned list (tiles of padding left out)
     if (idx >= __ldg(a.n_items_dev)) return false;
     const int4 e = __ldg(a.items + idx);
     it.b = e.x;
@@ -336,7 +337,7 @@ __device__ __forceinline__ void store_half_row_bf16(uint32_t panel, int rl, cons
   }
 }
 
-template <bool HL, int DHB>
+template <bool HL, int DHB, bool LIST>
 __global__ void __launch_bounds__(512, 1)
     attn_bwd_main_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   using C = BwdCfg<HL, DHB>;
@@ -351,7 +352,9 @@ __global__ void __launch_bounds__(512, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // A CTA past the end of a planned work list has no item at all.
-  if (a.items && static_cast<int>(blockIdx.x) >= __ldg(a.n_items_dev)) return;
+  if constexpr (LIST) {
+    if (static_cast<int>(blockIdx.x) >= __ldg(a.n_items_dev)) return;
+  }
 
   if (threadIdx.x == 0) {
     for (int x = 0; x < C::KVB; ++x) {
@@ -419,7 +422,7 @@ __global__ void __launch_bounds__(512, 1)
       bool ok = true;
       int gi = 0, n = 0;
       BwdItem itm{};
-      for (; ok && bwd_item(a, n, itm); ++n) {
+      for (; ok && bwd_item<LIST>(a, n, itm); ++n) {
         // K_j, V_j of the item into K/V buffer n % KVB.
         const int x = n % C::KVB;
         if (n >= C::KVB && !mbar_wait(bar(C::B_KVE + x), ((n / C::KVB) - 1) & 1, w)) break;
@@ -504,7 +507,7 @@ __global__ void __launch_bounds__(512, 1)
       };
       BwdItem itm{};
       int n = 0, gi = 0;
-      bool ok = bwd_item(a, 0, itm);
+      bool ok = bwd_item<LIST>(a, 0, itm);
       if (ok) ok = mbar_wait(bar(C::B_KVF), 0, w) && mbar_wait(bar(C::B_QF), 0, w);
       if (ok) {
         tc_fence_after();
@@ -515,7 +518,7 @@ __global__ void __launch_bounds__(512, 1)
         const int x = n % C::KVB;
         const uint32_t kb = sbase + C::OFF_K + x * 2 * C::OPND;
         BwdItem nxt{};
-        const bool has_next = bwd_item(a, n + 1, nxt);
+        const bool has_next = bwd_item<LIST>(a, n + 1, nxt);
         for (int it = 0; ok && it < itm.n_it; ++it, ++gi) {
           const int s = gi % C::NQS;
           const uint32_t qb = stage(s), dob = stage(s) + C::OPND;
@@ -663,7 +666,7 @@ __global__ void __launch_bounds__(512, 1)
     bool ok = true;
     int gi = 0;
     BwdItem itm{};
-    for (int n = 0; ok && bwd_item(a, n, itm); ++n) {
+    for (int n = 0; ok && bwd_item<LIST>(a, n, itm); ++n) {
       for (int it = 0; it < itm.n_it; ++it, ++gi) {
         if (it == itm.n_it - 1) {
           // ---- dK, dV of the item, written as soon as its last dK product is
@@ -770,7 +773,7 @@ __global__ void __launch_bounds__(512, 1)
     bool ok = true;
     int gi = 0;
     BwdItem itm{};
-    for (int n = 0; ok && bwd_item(a, n, itm); ++n) {
+    for (int n = 0; ok && bwd_item<LIST>(a, n, itm); ++n) {
       const int j = itm.j;
       for (int it = 0; it < itm.n_it; ++it, ++gi) {
         const int s = gi % C::NQS;

@@ -185,10 +185,11 @@ __device__ __forceinline__ int seq_len(const FwdArgs& a, int b) {
   atomicExch(a.status, kStatusBadInput);
   return L < 0 ? 0 : a.T;
 }
+template <bool LIST>
 __device__ __forceinline__ bool fwd_item(const FwdArgs& a, int k, FwdItem& it) {
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
   const long long idx = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
-  if (a.items) {  // variable-length batch: the planned list (tiles of padding left out)
+  if constexpr (LIST) {  // variable-length batch: the planned list (tiles of padding left out)
     if (idx >= __ldg(a.n_items_dev)) return false;
     const int4 e = __ldg(a.items + idx);
     it.b = e.x;
@@ -242,7 +243,7 @@ __device__ __forceinline__ void split_v_half(uint32_t vsrc, uint32_t vhi, uint32
   }
 }
 
-template <bool TF32, int DHP>
+template <bool TF32, int DHP, bool LIST>
 __global__ void __launch_bounds__(512, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
@@ -257,7 +258,9 @@ __global__ void __launch_bounds__(512, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // A CTA past the end of a planned work list has no item at all.
-  if (a.items && static_cast<int>(blockIdx.x) >= __ldg(a.n_items_dev)) return;
+  if constexpr (LIST) {
+    if (static_cast<int>(blockIdx.x) >= __ldg(a.n_items_dev)) return;
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::QB; ++i) {
@@ -335,7 +338,7 @@ __global__ void __launch_bounds__(512, 1)
       int kn = 0, kj = 0, tk = 0;  // K cursor: item, tile within it, tiles loaded
       int vn = 0, vj = 0, tv = 0;  // V cursor
       int nq = 0;                  // query tiles loaded
-      bool khave = fwd_item(a, 0, ik), vhave = fwd_item(a, 0, iv);
+      bool khave = fwd_item<LIST>(a, 0, ik), vhave = fwd_item<LIST>(a, 0, iv);
       bool ok = true;
       auto load_k = [&]() -> bool {
         if (kj == 0) {
@@ -356,7 +359,7 @@ __global__ void __launch_bounds__(512, 1)
         ++tk;
         if (++kj == ik.nkv) {
           kj = 0;
-          khave = fwd_item(a, ++kn, ik);
+          khave = fwd_item<LIST>(a, ++kn, ik);
         }
         return true;
       };
@@ -371,7 +374,7 @@ __global__ void __launch_bounds__(512, 1)
         ++tv;
         if (++vj == iv.nkv) {
           vj = 0;
-          vhave = fwd_item(a, ++vn, iv);
+          vhave = fwd_item<LIST>(a, ++vn, iv);
         }
         if (khave) ok = load_k();
       }
@@ -404,7 +407,7 @@ __global__ void __launch_bounds__(512, 1)
       const uint64_t dk0 = make_sdesc(sbase + C::OFF_K, 16, 1024);
       FwdItem is{};
       int sn = 0, sj = 0, ts = 0;  // item, tile within it, global tile
-      bool shave = fwd_item(a, 0, is);
+      bool shave = fwd_item<LIST>(a, 0, is);
       while (ok && shave) {
         const int qb = sn % C::QB;
         const int sk = ts % C::NSK;
@@ -427,7 +430,7 @@ __global__ void __launch_bounds__(512, 1)
         if (++sj == is.nkv) {
           tc_commit(bar(C::B_QE + qb));  // last S of the item: its query buffer is free
           sj = 0;
-          shave = fwd_item(a, ++sn, is);
+          shave = fwd_item<LIST>(a, ++sn, is);
         }
       }
       // Exit path: all issued MMAs finish before TMEM is released.
@@ -443,7 +446,7 @@ __global__ void __launch_bounds__(512, 1)
       const uint64_t dp0 = make_sdesc(sbase + C::OFF_P, 16, 1024);
       FwdItem ip{};
       int pn = 0, pj = 0, tp = 0;  // item, tile within it, global tile
-      bool phave = fwd_item(a, 0, ip);
+      bool phave = fwd_item<LIST>(a, 0, ip);
       while (ok && phave) {
         // Before the first product of work item n >= 1 the epilogue of item
         // n - 1 must have read the O partials.
@@ -501,7 +504,7 @@ __global__ void __launch_bounds__(512, 1)
         if (++pj == ip.nkv) {
           tc_commit(bar(C::B_ITEMD));  // every product of the item issued: done when they complete
           pj = 0;
-          phave = fwd_item(a, ++pn, ip);
+          phave = fwd_item<LIST>(a, ++pn, ip);
         }
       }
       tc_commit(bar(C::B_FIN + 1));
@@ -549,7 +552,7 @@ __global__ void __launch_bounds__(512, 1)
     int tb = 0;  // global number of this work item's first key tile
     for (int n = 0; ok; ++n) {
       FwdItem it{};
-      if (!fwd_item(a, n, it)) break;
+      if (!fwd_item<LIST>(a, n, it)) break;
       const int q_idx = it.qt * C::BM + row;
       float m = -INFINITY, l = 0.f;
       if constexpr (C::PP) {
@@ -859,7 +862,7 @@ __global__ void __launch_bounds__(512, 1)
       bool ok = true;
       int tb = 0;
       FwdItem it{};
-      for (int n = 0; ok && fwd_item(a, n, it); ++n) {
+      for (int n = 0; ok && fwd_item<LIST>(a, n, it); ++n) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_STAT + (n & 1)), (n >> 1) & 1, w));
         if (!ok) break;
         const float* stat = reinterpret_cast<const float*>(smem + C::OFF_STAT) + (n & 1) * 512;

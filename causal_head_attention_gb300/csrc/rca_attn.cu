@@ -298,28 +298,29 @@ rca_status launch_fwd(const void* q, const void* k, const void* v, int64_t B, in
                       int64_t T, int64_t Dh, void* out, float* lse, cudaStream_t st, int64_t qs, int64_t kvs,
                       const int* lens, const int4* items, const int* n_items_dev) {
   using C = rca::FwdCfg<TF32, DHP>;
-  static std::atomic<unsigned long long> smem_set{0};
+  static std::atomic<unsigned long long> smem_set[2] = {};
   CUtensorMap mq, mk, mv;
   RCA_CHECK(make_map(&mq, q, B, T, Hq, Dh, TF32, "q", 128, qs));
   RCA_CHECK(make_map(&mk, k, B, T, Hkv, Dh, TF32, "k", 128, kvs));
   RCA_CHECK(make_map(&mv, v, B, T, Hkv, Dh, TF32, "v", 128, kvs));
   int* status = nullptr;
   RCA_CHECK(status_word(&status));
-  auto kern = rca::attn_fwd_kernel<TF32, DHP>;
-  cudaError_t e = ensure_smem(kern, C::SMEM_BYTES, smem_set);
+  const int li = items ? 1 : 0;  // the work-list instantiation has its own caches
+  auto kern = items ? rca::attn_fwd_kernel<TF32, DHP, true> : rca::attn_fwd_kernel<TF32, DHP, false>;
+  cudaError_t e = ensure_smem(kern, C::SMEM_BYTES, smem_set[li]);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fwd)");
   // Warpgroup register split (setmaxnreg) out of the launch count: checked
   // before the first launch, as in the backward.
-  static std::atomic<int> launch_regs{0};
-  if (launch_regs.load(std::memory_order_acquire) == 0) {
+  static std::atomic<int> launch_regs[2] = {};
+  if (launch_regs[li].load(std::memory_order_acquire) == 0) {
     cudaFuncAttributes fa{};
     e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(fwd)");
-    launch_regs.store(fa.numRegs, std::memory_order_release);
+    launch_regs[li].store(fa.numRegs, std::memory_order_release);
   }
-  if (launch_regs.load(std::memory_order_acquire) != C::LAUNCH_REGS)
+  if (launch_regs[li].load(std::memory_order_acquire) != C::LAUNCH_REGS)
     return fail(RCA_ERR_UNSUPPORTED, "forward kernel built with %d registers per thread, its warpgroup split needs %d",
-                launch_regs.load(), C::LAUNCH_REGS);
+                launch_regs[li].load(), C::LAUNCH_REGS);
   rca::FwdArgs a{};
   a.out = out;
   a.lse = lse;
@@ -375,7 +376,7 @@ rca_status launch_bwd_main(const void* q, const void* k, const void* v, const vo
                            const WsLayout& L, cudaStream_t st, int* status_override, int64_t qs, int64_t kvs,
                            int64_t dkvs, const int4* items, const int* n_items_dev) {
   using C = rca::BwdCfg<HL, DHB>;
-  static std::atomic<unsigned long long> smem_set{0};
+  static std::atomic<unsigned long long> smem_set[2] = {};
   uint8_t* w = static_cast<uint8_t*>(ws);
   rca::BwdMaps maps;
   if constexpr (HL) {
@@ -416,22 +417,23 @@ rca_status launch_bwd_main(const void* q, const void* k, const void* v, const vo
   RCA_CHECK(make_map(&maps.dq, w + L.dq_off, B, T, Hq, Dh, true, "dq accumulator", 32));
   int* status = status_override;
   if (!status) RCA_CHECK(status_word(&status));
-  auto kern = rca::attn_bwd_main_kernel<HL, DHB>;
-  cudaError_t e = ensure_smem(kern, C::SMEM_BYTES, smem_set);
+  const int li = items ? 1 : 0;  // the work-list instantiation has its own caches
+  auto kern = items ? rca::attn_bwd_main_kernel<HL, DHB, true> : rca::attn_bwd_main_kernel<HL, DHB, false>;
+  cudaError_t e = ensure_smem(kern, C::SMEM_BYTES, smem_set[li]);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
   // The kernel splits its registers between warpgroups (setmaxnreg) out of the
   // per-thread count it is launched with; a different count would make the
   // split wait forever, so it is checked before the first launch.
-  static std::atomic<int> launch_regs{0};
-  if (launch_regs.load(std::memory_order_acquire) == 0) {
+  static std::atomic<int> launch_regs[2] = {};
+  if (launch_regs[li].load(std::memory_order_acquire) == 0) {
     cudaFuncAttributes fa{};
     e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(bwd)");
-    launch_regs.store(fa.numRegs, std::memory_order_release);
+    launch_regs[li].store(fa.numRegs, std::memory_order_release);
   }
-  if (launch_regs.load(std::memory_order_acquire) != C::LAUNCH_REGS)
+  if (launch_regs[li].load(std::memory_order_acquire) != C::LAUNCH_REGS)
     return fail(RCA_ERR_UNSUPPORTED, "backward kernel built with %d registers per thread, its warpgroup split needs %d",
-                launch_regs.load(), C::LAUNCH_REGS);
+                launch_regs[li].load(), C::LAUNCH_REGS);
   rca::BwdArgs a{};
   a.dk = dk;
   a.dv = dv;
