@@ -707,7 +707,8 @@ def bench_decode(w, dev, stream, steps, warmup, cpu_budget, P):
         "workload": w.describe(), "name": w.name, "metric": "paged decode K/V streaming GB/s",
         "us_per_call": ms * 1e3, "us_min": per[0] * 1e3,
         "calls_per_s": 1e3 / ms, "tokens_per_s": w.B * 1e3 / ms,
-        "roofline": {"kernel": "decode (+ combine)", "bound": "hbm", "achieved": gbs, "peak": P["hbm_gbs"],
+        "roofline": {"kernel": "decode_mma_kernel" if w.dtype == "bf16" and w.Hq // w.Hkv >= 2 else "decode_kernel",
+                     "bound": "hbm", "achieved": gbs, "peak": P["hbm_gbs"],
                      "unit": "GB/s", "frac": gbs / P["hbm_gbs"], "bytes_per_call": nbytes,
                      "traffic": ncu_traffic("decode", w.name)},
         "e2e": {"us_per_call": e_ms * 1e3, "h2d_bytes_per_call": sum(x.numel() * x.element_size() for x in (hq, ht, hl)),

@@ -32,8 +32,13 @@
 //    2^8 (so probabilities stay <= 256): each lane then takes one exponential
 //    per block and the probabilities are broadcast for the fp32x2 P * V update.
 //  * A request whose length fits one chunk writes O and LSE directly; longer
-//    requests leave (max, sum, unnormalised O) per chunk and a combine kernel
-//    merges them.
+//    requests leave (max, sum, unnormalised O) per chunk and a combine kernel,
+//    launched as a programmatic dependent (its launch overlaps the decode
+//    kernel's tail), merges them.
+//  * bf16 storage with two or more query heads per KV head runs the group's
+//    two products on the tensor cores instead (decode_mma_kernel below): the
+//    same items, loads and softmax, with the dot products and P * V as
+//    warp-level MMAs fed straight from the loaded registers.
 // Device-side inputs are checked as they are read: a page ID outside
 // [0, num_pages) is never dereferenced (its positions read as zeros) and a
 // length outside [1, max_pages * page_size] makes that request's outputs NaN;
@@ -51,7 +56,7 @@
 namespace rca {
 namespace dec {
 
-constexpr int NW = 4;  // warps per CTA (decode and combine kernels)
+constexpr int NW = 4;  // warps per CTA (decode kernels); the combine kernel has NT threads too
 constexpr int NT = NW * 32;
 constexpr unsigned FULL = 0xffffffffu;
 constexpr float kRaise = 8.f;  // raise the running max when a score passes it by more (base 2)
@@ -254,6 +259,43 @@ __device__ __forceinline__ Item item_of(const Args& a, const int* pre, int upb, 
   it.s0 = it.c * kDecodeChunk;
   it.s1 = min(L, it.s0 + kDecodeChunk);
   return it;
+}
+
+// Merges the NW warps' partial states of one item (written to shared memory by
+// every warp before the call) and writes the output rows and LSE, or the
+// item's partial when the request spans several chunks. One thread per
+// (head, column); ends with the block synchronised so the buffers can be
+// reused.
+template <bool BF16, int DH, int G>
+__device__ __forceinline__ void finish_item(const Args& a, const Item& it, const float (&red_acc)[NW][G][DH],
+                                            const float (&red_m)[NW][G], const float (&red_l)[NW][G]) {
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * DH; idx += NT) {
+    const int h = idx / DH, d = idx - h * DH;
+    float M = red_m[0][h];
+#pragma unroll
+    for (int q = 1; q < NW; ++q) M = fmaxf(M, red_m[q][h]);
+    float Ls = 0.f, A = 0.f;
+#pragma unroll
+    for (int q = 0; q < NW; ++q) {
+      const float wt = ex2(red_m[q][h] - M);
+      Ls += red_l[q][h] * wt;
+      A += red_acc[q][h][d] * wt;
+    }
+    const int64_t row = int64_t(it.b) * a.Hq + it.h0 + h;
+    if (it.nch == 1) {
+      store_elem<BF16>(a.out, row * DH + d, A / Ls);
+      if (d == 0) a.lse[row] = 0.69314718055994531f * (M + lg2(Ls));
+    } else {
+      const int64_t pr = row * a.maxch + it.c;
+      a.part_acc[pr * DH + d] = A;
+      if (d == 0) {
+        a.part_ml[pr * 2] = M;
+        a.part_ml[pr * 2 + 1] = Ls;
+      }
+    }
+  }
+  __syncthreads();
 }
 
 // Warp w of a CTA takes blocks j = w, w + NW, ... of an item; block j covers
@@ -490,86 +532,366 @@ __global__ void __launch_bounds__(NT, (Cfg<BF16, DH, G>::MINB)) decode_kernel(Ar
         }
       }
     }
-    __syncthreads();
-    // Merge the warps; one thread per (head, column).
-    for (int idx = tid; idx < G * DH; idx += NT) {
-      const int h = idx / DH, d = idx - h * DH;
-      float M = red_m[0][h];
-#pragma unroll
-      for (int q = 1; q < NW; ++q) M = fmaxf(M, red_m[q][h]);
-      float Ls = 0.f, A = 0.f;
-#pragma unroll
-      for (int q = 0; q < NW; ++q) {
-        const float wt = ex2(red_m[q][h] - M);
-        Ls += red_l[q][h] * wt;
-        A += red_acc[q][h][d] * wt;
-      }
-      const int64_t row = int64_t(it.b) * a.Hq + it.h0 + h;
-      if (it.nch == 1) {
-        store_elem<BF16>(a.out, row * DH + d, A / Ls);
-        if (d == 0) a.lse[row] = 0.69314718055994531f * (M + lg2(Ls));
-      } else {
-        const int64_t pr = row * a.maxch + it.c;
-        a.part_acc[pr * DH + d] = A;
-        if (d == 0) {
-          a.part_ml[pr * 2] = M;
-          a.part_ml[pr * 2 + 1] = Ls;
-        }
-      }
-    }
-    __syncthreads();
+    finish_item<BF16, DH, G>(a, it, red_acc, red_m, red_l);
   }
   if (bad_page) atomicExch(a.status, kStatusBadInput);
 }
 
-// Merges the chunk partials of requests longer than one chunk. One warp per
-// (request, query head, 32-column slice): lane c of a 32-chunk window weighs
-// chunk c once (2^(m_c - M)), the weights are broadcast, and each lane sums
-// its column over the chunks with the loads of several chunks in flight.
+// ---------------------------------------------------------------------------
+// Tensor-core variant (bf16 storage). The G query rows of a KV head group
+// share every K and V row, so a block of 16 positions is two small dense
+// products, run as warp-level m16n8k16 bf16 MMAs with fp32 accumulation and
+// the G heads padded to the 8 columns of n:
+//   S^T [16 positions x 8 heads]  = K [16 x Dh] . Q^T [Dh x 8]
+//   O^T [Dh x 8 heads]           += V^T [Dh x 16] . P^T [16 x 8]
+// The operand fragments are filled straight from 16-byte global loads (no
+// shared-memory staging, the same load pattern as the CUDA-core kernel):
+//  * the order of the head dimension inside q . k is free, so the dims are
+//    dealt to the four lanes of a quad such that a lane's share of a K row
+//    (and of the query row) is whole vectors, consecutive lanes reading
+//    consecutive vectors;
+//  * the output dims are dealt to the eight lane groups the same way for V;
+//    a V^T fragment register pairs one dim of two positions (one byte permute);
+//  * the S^T accumulator becomes the P^T operand after one 8x8 transpose of
+//    each half (movmatrix). The probabilities enter as bf16 hi + lo parts
+//    (two MMAs), so the output keeps the accuracy of fp32 probabilities.
+// Softmax state per lane: the running max and partial sum of its two heads
+// (2t, 2t + 1 for quad lane t), the max being the same across the lane groups.
+// ---------------------------------------------------------------------------
+#ifndef DEC_MMA_PREFETCH
+#define DEC_MMA_PREFETCH 0
+#endif
+#ifndef DEC_MMA_MINB
+#define DEC_MMA_MINB (DEC_MMA_PREFETCH ? 2 : 3)
+#endif
+static_assert(kDecodeChunk / 16 <= 32 * NW, "a warp's block pages fit one lane each");
+
+template <int DH>
+struct MmaCfg {
+  static constexpr int S = DH / 16;  // k-steps of the score product = m-tiles of the output
+  static constexpr int KW = DH / 8;  // 32-bit words of a K (or query) row per quad lane
+  static constexpr int KL = KW * 4 < 16 ? KW * 4 : 16;  // bytes per load
+  static constexpr int NKL = KW * 4 / KL;
+  static constexpr int VW = DH / 16;  // words of a V row per lane group
+  static constexpr int VL = VW * 4 < 16 ? VW * 4 : 16;
+  static constexpr int NVL = VW * 4 / VL;
+  // Word j of quad lane t's share of a K / query row is the row's word
+  // kword(j, t); words 2s and 2s + 1 hold the lane's k-step-s operand columns
+  // (2t, 2t + 1) and (2t + 8, 2t + 9).
+  __host__ __device__ static constexpr int kword(int j, int t) {
+    return ((j / (KL / 4)) * 4 + t) * (KL / 4) + j % (KL / 4);
+  }
+  // Word r of lane group g's share of a V row is the row's word vword(r, g):
+  // its low / high halves are output m-tile r's rows g / g + 8.
+  __host__ __device__ static constexpr int vword(int r, int g) {
+    return ((r / (VL / 4)) * 8 + g) * (VL / 4) + r % (VL / 4);
+  }
+};
+
+// One warp block's K and V fragments (see MmaCfg): K rows g, g + 8 and V
+// rows 2t, 2t + 1, 2t + 8, 2t + 9 of 16 consecutive positions.
+template <int DH>
+struct MmaBlock {
+  uint32_t kw[2][DH / 8];
+  uint32_t vw[4][DH / 16];
+};
+
+template <int BYTES, bool ONCE>
+__device__ __forceinline__ void ld_words(const char* p, uint32_t* w) {
+  if constexpr (BYTES == 16) {
+    if constexpr (ONCE)
+      asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                   : "l"(p));
+    else
+      asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                   : "l"(p));
+  } else if constexpr (BYTES == 8) {
+    asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "l"(p));
+  } else {
+    static_assert(BYTES == 4, "load width");
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(w[0]) : "l"(p));
+  }
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 matrix of 16-bit values held one word per lane (row
+// lane / 4, columns 2 (lane % 4) and 2 (lane % 4) + 1).
+__device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+template <int DH, int G>
+__global__ void __launch_bounds__(NT, DEC_MMA_MINB) decode_mma_kernel(Args a) {
+  using M = MmaCfg<DH>;
+  constexpr int S = M::S, KW = M::KW, KL = M::KL, VL = M::VL, ROW = DH * 2;
+  static_assert(G >= 1 && G <= 8, "a group fills at most the 8 columns of n");
+
+  __shared__ __align__(16) float red_acc[NW][G][DH];  // float2 stores
+  __shared__ float red_m[NW][G], red_l[NW][G];
+  __shared__ int warp_tot[NW];
+  extern __shared__ int pre[];  // [B + 1]
+
+  build_prefix<true, NT>(a, pre, warp_tot, DH);  // ends with __syncthreads
+  const int upb = a.Hkv * a.ngc;
+  const int total = pre[a.B] * upb;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;  // lane group (row of a fragment), quad lane
+  const int pmask = (1 << a.page_shift) - 1;
+  const bool one_page = a.page_shift >= 4;  // a block of 16 aligned positions lies in one page
+  bool bad_page = false;
+
+  for (int item = blockIdx.x; item < total; item += gridDim.x) {
+    const Item it = item_of<G>(a, pre, upb, item);
+    const int nblk = (it.s1 - it.s0 + 15) >> 4;
+    const int32_t* trow = a.table + int64_t(it.b) * a.max_pages;
+    const int64_t head_off = int64_t(it.kv) << a.page_shift;
+
+    // Query head g of the group as the score product's n column g (zero
+    // columns past the group).
+    uint32_t qw[KW];
+#pragma unroll
+    for (int j = 0; j < KW; ++j) qw[j] = 0;
+    if (g < G) {
+      const char* qrow = a.q + (int64_t(it.b) * a.Hq + it.h0 + g) * ROW;
+#pragma unroll
+      for (int i = 0; i < M::NKL; ++i) ld_words<KL, false>(qrow + (i * 4 + t) * KL, qw + i * (KL / 4));
+    }
+    float m0 = -1e30f, m1 = -1e30f, l0 = 0.f, l1 = 0.f;  // heads 2t, 2t + 1
+    float acc[S][4];
+#pragma unroll
+    for (int r = 0; r < S; ++r) acc[r][0] = acc[r][1] = acc[r][2] = acc[r][3] = 0.f;
+
+    // This warp takes blocks warp, warp + NW, ... of the item; lane i reads
+    // the page of its i-th block up front, so a block's K/V loads never wait
+    // for a page-table load.
+    const int nmy = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
+    int pg_lane = 0;
+    if (one_page && lane < nmy) pg_lane = __ldg(trow + ((it.s0 + (warp + lane * NW) * 16) >> a.page_shift));
+
+    // Loads of the warp's i-th block: K rows g, g + 8; V rows 2t, 2t + 1, 2t + 8, 2t + 9.
+    auto load_block = [&](MmaBlock<DH>& bk, int i) {
+      const int p0 = it.s0 + (warp + i * NW) * 16;
+      int64_t blk = -1;  // byte offset of position p0's row when the block lies in one page
+      if (one_page) {
+        const int pg = __shfl_sync(FULL, pg_lane, i);
+        if (static_cast<unsigned>(pg) < static_cast<unsigned>(a.num_pages))
+          blk = (((int64_t(pg) * a.Hkv) << a.page_shift) + head_off + (p0 & pmask)) * ROW;
+        else
+          bad_page = true;
+      }
+      // Byte offset of position p0 + d's row, or -1 (past the end, or a bad page).
+      auto row_of = [&](int d) -> int64_t {
+        const int pos = p0 + d;
+        if (pos >= it.s1) return -1;
+        if (one_page) return blk < 0 ? -1 : blk + int64_t(d) * ROW;
+        const int pg = __ldg(trow + (pos >> a.page_shift));
+        if (static_cast<unsigned>(pg) >= static_cast<unsigned>(a.num_pages)) {
+          bad_page = true;
+          return -1;
+        }
+        return (((int64_t(pg) * a.Hkv) << a.page_shift) + head_off + (pos & pmask)) * ROW;
+      };
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t r = row_of(g + 8 * h);
+#pragma unroll
+        for (int n = 0; n < M::NKL; ++n) {
+          if (r >= 0) {
+            ld_words<KL, true>(a.kp + r + (n * 4 + t) * KL, bk.kw[h] + n * (KL / 4));
+          } else {
+#pragma unroll
+            for (int w = 0; w < KL / 4; ++w) bk.kw[h][n * (KL / 4) + w] = 0;
+          }
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int64_t r = row_of(2 * t + (c & 1) + 8 * (c >> 1));
+#pragma unroll
+        for (int n = 0; n < M::NVL; ++n) {
+          if (r >= 0) {
+            ld_words<VL, true>(a.vp + r + (n * 8 + g) * VL, bk.vw[c] + n * (VL / 4));
+          } else {
+#pragma unroll
+            for (int w = 0; w < VL / 4; ++w) bk.vw[c][n * (VL / 4) + w] = 0;
+          }
+        }
+      }
+    };
+
+    auto compute_block = [&](const MmaBlock<DH>& bk, int i) {
+      const int p0 = it.s0 + (warp + i * NW) * 16;
+      // Scores: s[0], s[1] = position g, heads 2t, 2t + 1; s[2], s[3] = position g + 8.
+      float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < S; ++k)
+        mma_bf16_16816(s, bk.kw[0][2 * k], bk.kw[1][2 * k], bk.kw[0][2 * k + 1], bk.kw[1][2 * k + 1], qw[2 * k],
+                       qw[2 * k + 1]);
+      const bool va = p0 + g < it.s1, vb = p0 + g + 8 < it.s1;
+      const float x0 = va ? s[0] * a.qscale : -INFINITY, x1 = va ? s[1] * a.qscale : -INFINITY;
+      const float x2 = vb ? s[2] * a.qscale : -INFINITY, x3 = vb ? s[3] * a.qscale : -INFINITY;
+      // Raise the running max only when a score passes it by more than 2^8.
+      const bool raise = fmaxf(x0, x2) > m0 + kRaise || fmaxf(x1, x3) > m1 + kRaise;
+      if (__any_sync(FULL, raise)) {
+        float n0 = fmax3(m0, x0, x2), n1 = fmax3(m1, x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          n0 = fmaxf(n0, __shfl_xor_sync(FULL, n0, off));
+          n1 = fmaxf(n1, __shfl_xor_sync(FULL, n1, off));
+        }
+        const float al0 = ex2(m0 - n0), al1 = ex2(m1 - n1);
+#pragma unroll
+        for (int r = 0; r < S; ++r) {
+          acc[r][0] *= al0;
+          acc[r][1] *= al1;
+          acc[r][2] *= al0;
+          acc[r][3] *= al1;
+        }
+        l0 *= al0;
+        l1 *= al1;
+        m0 = n0;
+        m1 = n1;
+      }
+      const float pa = ex2(x0 - m0), pb = ex2(x1 - m1), pc = ex2(x2 - m0), pd = ex2(x3 - m1);
+      l0 += pa + pc;
+      l1 += pb + pd;
+      uint32_t hi01, lo01, hi23, lo23;
+      split_bf16x2(pa, pb, hi01, lo01);
+      split_bf16x2(pc, pd, hi23, lo23);
+      const uint32_t bh0 = transpose8x8(hi01), bh1 = transpose8x8(hi23);
+      const uint32_t bl0 = transpose8x8(lo01), bl1 = transpose8x8(lo23);
+#pragma unroll
+      for (int r = 0; r < S; ++r) {
+        const uint32_t a0 = __byte_perm(bk.vw[0][r], bk.vw[1][r], 0x5410);
+        const uint32_t a1 = __byte_perm(bk.vw[0][r], bk.vw[1][r], 0x7632);
+        const uint32_t a2 = __byte_perm(bk.vw[2][r], bk.vw[3][r], 0x5410);
+        const uint32_t a3 = __byte_perm(bk.vw[2][r], bk.vw[3][r], 0x7632);
+        mma_bf16_16816(acc[r], a0, a1, a2, a3, bh0, bh1);
+        mma_bf16_16816(acc[r], a0, a1, a2, a3, bl0, bl1);
+      }
+    };
+
+#if DEC_MMA_PREFETCH
+    // Two blocks in flight: the next block's loads are issued before this
+    // block's products.
+    MmaBlock<DH> b0, b1;
+    if (nmy > 0) load_block(b0, 0);
+    for (int i = 0; i < nmy; i += 2) {
+      if (i + 1 < nmy) load_block(b1, i + 1);
+      compute_block(b0, i);
+      if (i + 1 < nmy) {
+        if (i + 2 < nmy) load_block(b0, i + 2);
+        compute_block(b1, i + 1);
+      }
+    }
+#else
+    for (int i = 0; i < nmy; ++i) {
+      MmaBlock<DH> bk;
+      load_block(bk, i);
+      compute_block(bk, i);
+    }
+#endif
+
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(FULL, l0, off);
+      l1 += __shfl_xor_sync(FULL, l1, off);
+    }
+    // acc[r] = O^T rows (dims) of word vword(r, g), columns (heads) 2t, 2t + 1.
+    const int ha = 2 * t, hb = 2 * t + 1;
+#pragma unroll
+    for (int r = 0; r < S; ++r) {
+      const int w = M::vword(r, g);
+      if (ha < G) *reinterpret_cast<float2*>(&red_acc[warp][ha][2 * w]) = make_float2(acc[r][0], acc[r][2]);
+      if (hb < G) *reinterpret_cast<float2*>(&red_acc[warp][hb][2 * w]) = make_float2(acc[r][1], acc[r][3]);
+    }
+    if (g == 0) {
+      if (ha < G) {
+        red_m[warp][ha] = m0;
+        red_l[warp][ha] = l0;
+      }
+      if (hb < G) {
+        red_m[warp][hb] = m1;
+        red_l[warp][hb] = l1;
+      }
+    }
+    finish_item<true, DH, G>(a, it, red_acc, red_m, red_l);
+  }
+  if (bad_page) atomicExch(a.status, kStatusBadInput);
+}
+
+// Merges the chunk partials of requests longer than one chunk: one thread per
+// (request, query head, 4 columns), all of whose loads are independent of one
+// another but for the chunk maxima (2^(m_c - M) weighs chunk c against the
+// largest max M). Launched as a programmatic dependent of the decode kernel, so
+// its launch overlaps the decode kernel's tail; griddepcontrol.wait holds it
+// until the decode grid has finished and its writes are visible.
 template <bool BF16, int DH>
 __global__ void __launch_bounds__(NT) decode_combine_kernel(Args a) {
-  constexpr int NS = (DH + 31) / 32;  // column slices per row
-  const int lane = threadIdx.x & 31;
-  const int64_t wid = int64_t(blockIdx.x) * NW + (threadIdx.x >> 5);
-  if (wid >= int64_t(a.B) * a.Hq * NS) return;
-  const int64_t row = wid / NS;
-  const int d = int(wid - row * NS) * 32 + lane;
-  const int b = int(row / a.Hq);
-  const int L = __ldg(a.lens + b);
+  constexpr int NQ = DH / 4;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int64_t id = int64_t(blockIdx.x) * NT + threadIdx.x;
+  if (id >= int64_t(a.B) * a.Hq * NQ) return;
+  const int64_t row = id / NQ;
+  const int d = int(id - row * NQ) * 4;
+  const int L = __ldg(a.lens + row / a.Hq);
   if (!len_ok(L, a)) return;  // written as NaN by the decode kernel
   const int nch = n_chunks(L);
   if (nch == 1) return;       // written by the decode kernel
   const float* ml = a.part_ml + row * a.maxch * 2;
-  const float* pa = a.part_acc + row * a.maxch * DH;
+  const float* pa = a.part_acc + row * a.maxch * DH + d;
   float M = -INFINITY;
-  for (int c = lane; c < nch; c += 32) M = fmaxf(M, __ldg(ml + 2 * c));
-#pragma unroll
-  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, off));
-  float Ls = 0.f, o = 0.f;
-  for (int c0 = 0; c0 < nch; c0 += 32) {
-    const int c = c0 + lane;
-    float wc = 0.f;
-    if (c < nch) {
-      wc = ex2(__ldg(ml + 2 * c) - M);
-      Ls += __ldg(ml + 2 * c + 1) * wc;
-    }
-    const int n = min(32, nch - c0);
 #pragma unroll 8
-    for (int i = 0; i < n; ++i) {
-      const float w = __shfl_sync(FULL, wc, i);
-      if (d < DH) o += __ldg(pa + int64_t(c0 + i) * DH + d) * w;
-    }
+  for (int c = 0; c < nch; ++c) M = fmaxf(M, __ldcg(ml + 2 * c));
+  float Ls = 0.f;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+  for (int c = 0; c < nch; ++c) {
+    const float2 mc = __ldcg(reinterpret_cast<const float2*>(ml + 2 * c));
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(pa + int64_t(c) * DH));
+    const float w = ex2(mc.x - M);
+    Ls += mc.y * w;
+    o.x += v.x * w;
+    o.y += v.y * w;
+    o.z += v.z * w;
+    o.w += v.w * w;
   }
-#pragma unroll
-  for (int off = 16; off; off >>= 1) Ls += __shfl_xor_sync(FULL, Ls, off);
-  if (d < DH) store_elem<BF16>(a.out, row * DH + d, o / Ls);
+  const float r = 1.f / Ls;
+  store_elem<BF16>(a.out, row * DH + d, o.x * r);
+  store_elem<BF16>(a.out, row * DH + d + 1, o.y * r);
+  store_elem<BF16>(a.out, row * DH + d + 2, o.z * r);
+  store_elem<BF16>(a.out, row * DH + d + 3, o.w * r);
   if (d == 0) a.lse[row] = 0.69314718055994531f * (M + lg2(Ls));
+}
+
+// bf16 groups of at least this many query heads take the tensor-core kernel.
+#ifndef DEC_MMA_MIN_G
+#define DEC_MMA_MIN_G 2
+#endif
+
+template <bool BF16, int DH, int G>
+constexpr auto decode_entry() {
+  if constexpr (BF16 && G >= DEC_MMA_MIN_G)
+    return decode_mma_kernel<DH, G>;
+  else
+    return decode_kernel<BF16, DH, G>;
 }
 
 template <bool BF16, int DH, int G>
 cudaError_t launch(const DecodeParams& p, const Args& a, cudaStream_t st) {
-  auto k = decode_kernel<BF16, DH, G>;
-  using C = Cfg<BF16, DH, G>;
+  const auto k = decode_entry<BF16, DH, G>();
   const size_t dyn = size_t(p.B + 1) * sizeof(int);
   // Opt in once per device to the largest dynamic size any batch needs.
   static std::atomic<unsigned long long> opted{0};
@@ -592,9 +914,17 @@ cudaError_t launch(const DecodeParams& p, const Args& a, cudaStream_t st) {
   k<<<dim3(unsigned(grid)), NT, dyn, st>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.maxch <= 1) return e;
-  const int64_t warps = p.B * p.Hq * ((DH + 31) / 32);
-  decode_combine_kernel<BF16, DH><<<dim3(unsigned((warps + NW - 1) / NW)), NT, 0, st>>>(a);
-  return cudaGetLastError();
+  const int64_t threads = p.B * p.Hq * (DH / 4);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned((threads + NT - 1) / NT));
+  cfg.blockDim = dim3(NT);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<BF16, DH>, a);
 }
 
 template <bool BF16, int DH>

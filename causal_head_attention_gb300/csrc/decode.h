@@ -41,8 +41,9 @@ inline int64_t decode_max_chunks(int64_t page_size, int64_t max_pages) {
   return (page_size * max_pages + kDecodeChunk - 1) / kDecodeChunk;
 }
 
-// Enqueues the decode kernel and, when some request spans several items, the
-// combine kernel. Arguments are validated by the caller.
+// Enqueues the decode kernel and, when some request can span several items,
+// the combine kernel (a programmatic dependent launch). Arguments are validated
+// by the caller.
 cudaError_t launch_paged_decode(const DecodeParams& p, cudaStream_t st);
 
 }  // namespace rca

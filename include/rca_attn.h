@@ -78,8 +78,8 @@ typedef enum {
 /* Storage dtype of q/k/v/out/dout/dq/dk/dv; selects the tensor-core operand type. */
 typedef enum { RCA_F32_TF32 = 0, RCA_BF16 = 1 } rca_dtype;
 
-/* ABI version: upper 16 bits major, lower 16 bits minor (0x00010005 = 1.5). */
-#define RCA_ABI_VERSION 0x00010005u
+/* ABI version: upper 16 bits major, lower 16 bits minor (0x00010006 = 1.6). */
+#define RCA_ABI_VERSION 0x00010006u
 uint32_t rca_abi_version(void);
 
 /* Message of the last failed call on this thread ("" if none). The pointer is
@@ -304,8 +304,11 @@ rca_status rca_causal_softmax_bwd(const float* probs, float* grad, const float* 
  *                       request's last page are never read)
  *   seq_lens          : [B] int32
  *   lse               : [B, Hq] float32
- * RCA_BF16: bfloat16 storage; RCA_F32_TF32: float32 storage. Both compute in
- * fp32 on the CUDA cores (no tensor-core rounding). Dh in {16, 32, 64, 128};
+ * RCA_BF16: bfloat16 storage; RCA_F32_TF32: float32 storage. Arithmetic is
+ * fp32 on the stored values: float32 storage and bf16 with one query head per
+ * KV head on the CUDA cores; bf16 with Hq/Hkv >= 2 on the tensor cores (exact
+ * bf16 products with fp32 accumulation, probabilities entering the P*V product
+ * as a bf16 hi + lo pair, so still ~fp32-accurate). Dh in {16, 32, 64, 128};
  * page_size a power of two in [1, 65536]; 1 <= B <= 8192;
  * max_pages * page_size <= 2^30. q, k_pool and v_pool 16-byte aligned,
  * page_table, seq_lens and lse 4-byte aligned.

@@ -148,7 +148,7 @@ def test_decode_workspace_size(lib):
     assert lib.rca_paged_decode_workspace_size(4, 8, 8, 64, 16, 16, 1) == 256
     # B * Hq * chunks rows of (max, sum) and Dh floats
     n = lib.rca_paged_decode_workspace_size(64, 16, 16, 64, 16, 128, 1)
-    assert n >= 64 * 16 * 8 * (64 + 2) * 4
+    assert n >= 64 * 16 * 8 * (64 + 2) * 4 and n % 256 == 0
     assert lib.rca_paged_decode_workspace_size(4, 8, 8, 96, 16, 16, 1) == 0
     assert lib.rca_paged_decode_workspace_size(4, 8, 8, 64, 12, 16, 1) == 0
 
