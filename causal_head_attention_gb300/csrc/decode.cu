@@ -832,42 +832,76 @@ __global__ void __launch_bounds__(NT, DEC_MMA_MINB) decode_mma_kernel(Args a) {
   if (bad_page) atomicExch(a.status, kStatusBadInput);
 }
 
-// Merges the chunk partials of requests longer than one chunk: one thread per
-// (request, query head, 4 columns), all of whose loads are independent of one
-// another but for the chunk maxima (2^(m_c - M) weighs chunk c against the
-// largest max M). Launched as a programmatic dependent of the decode kernel, so
-// its launch overlaps the decode kernel's tail; griddepcontrol.wait holds it
-// until the decode grid has finished and its writes are visible.
+// Folds one partial (max m2, sum l2, unnormalised row v2) into a running
+// merge (M, L, o): both are rescaled to the larger max. An empty side (max
+// -inf, nothing merged yet) gets weight 0.
+__device__ __forceinline__ void merge_partial(float& M, float& L, float4& o, float m2, float l2, const float4& v2) {
+  const float Mn = fmaxf(M, m2);
+  if (Mn == -INFINITY) return;  // both sides empty
+  const float wa = ex2(M - Mn), wb = ex2(m2 - Mn);
+  L = L * wa + l2 * wb;
+  o.x = o.x * wa + v2.x * wb;
+  o.y = o.y * wa + v2.y * wb;
+  o.z = o.z * wa + v2.z * wb;
+  o.w = o.w * wa + v2.w * wb;
+  M = Mn;
+}
+
+// Merges the chunk partials of requests longer than one chunk. Each
+// (request, query head, 4 columns) is shared by 4 adjacent lanes: lane s folds
+// chunks s, s + 4, ... in one online pass, CB chunks' loads in flight at once,
+// then the 4 lanes merge by shuffles. Launched as a programmatic dependent of
+// the decode kernel, so its launch overlaps the decode kernel's tail;
+// griddepcontrol.wait holds it until the decode grid has finished and its
+// writes are visible. The partials were written by that grid, so they are read
+// through L2 (ld.global.cg).
 template <bool BF16, int DH>
 __global__ void __launch_bounds__(NT) decode_combine_kernel(Args a) {
-  constexpr int NQ = DH / 4;
+  constexpr int NQ = DH / 4, SPLIT = 4, CB = 8;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t id = int64_t(blockIdx.x) * NT + threadIdx.x;
-  if (id >= int64_t(a.B) * a.Hq * NQ) return;
-  const int64_t row = id / NQ;
-  const int d = int(id - row * NQ) * 4;
+  const int64_t unit = id / SPLIT;  // the 4 lanes of a unit exit together
+  const int sub = int(id % SPLIT);
+  if (unit >= int64_t(a.B) * a.Hq * NQ) return;
+  const int64_t row = unit / NQ;
+  const int d = int(unit - row * NQ) * 4;
   const int L = __ldg(a.lens + row / a.Hq);
   if (!len_ok(L, a)) return;  // written as NaN by the decode kernel
   const int nch = n_chunks(L);
   if (nch == 1) return;       // written by the decode kernel
   const float* ml = a.part_ml + row * a.maxch * 2;
   const float* pa = a.part_acc + row * a.maxch * DH + d;
-  float M = -INFINITY;
-#pragma unroll 8
-  for (int c = 0; c < nch; ++c) M = fmaxf(M, __ldcg(ml + 2 * c));
-  float Ls = 0.f;
+  float M = -INFINITY, Ls = 0.f;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-  for (int c = 0; c < nch; ++c) {
-    const float2 mc = __ldcg(reinterpret_cast<const float2*>(ml + 2 * c));
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(pa + int64_t(c) * DH));
-    const float w = ex2(mc.x - M);
-    Ls += mc.y * w;
-    o.x += v.x * w;
-    o.y += v.y * w;
-    o.z += v.z * w;
-    o.w += v.w * w;
+  for (int c0 = sub; c0 < nch; c0 += SPLIT * CB) {
+    float2 mc[CB];
+    float4 v[CB];
+#pragma unroll
+    for (int k = 0; k < CB; ++k) {
+      const int c = c0 + SPLIT * k;
+      if (c < nch) {
+        mc[k] = __ldcg(reinterpret_cast<const float2*>(ml + 2 * c));
+        v[k] = __ldcg(reinterpret_cast<const float4*>(pa + int64_t(c) * DH));
+      } else {
+        mc[k] = make_float2(-INFINITY, 0.f);
+        v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < CB; ++k) merge_partial(M, Ls, o, mc[k].x, mc[k].y, v[k]);
   }
+  const unsigned gmask = 0xfu << (threadIdx.x & 28);
+#pragma unroll
+  for (int off = 1; off < SPLIT; off <<= 1) {
+    float4 vo;
+    const float mo = __shfl_xor_sync(gmask, M, off), lo = __shfl_xor_sync(gmask, Ls, off);
+    vo.x = __shfl_xor_sync(gmask, o.x, off);
+    vo.y = __shfl_xor_sync(gmask, o.y, off);
+    vo.z = __shfl_xor_sync(gmask, o.z, off);
+    vo.w = __shfl_xor_sync(gmask, o.w, off);
+    merge_partial(M, Ls, o, mo, lo, vo);
+  }
+  if (sub != 0) return;
   const float r = 1.f / Ls;
   store_elem<BF16>(a.out, row * DH + d, o.x * r);
   store_elem<BF16>(a.out, row * DH + d + 1, o.y * r);
@@ -914,7 +948,7 @@ cudaError_t launch(const DecodeParams& p, const Args& a, cudaStream_t st) {
   k<<<dim3(unsigned(grid)), NT, dyn, st>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.maxch <= 1) return e;
-  const int64_t threads = p.B * p.Hq * (DH / 4);
+  const int64_t threads = p.B * p.Hq * (DH / 4) * 4;  // 4 lanes per (row, 4 columns)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned((threads + NT - 1) / NT));
   cfg.blockDim = dim3(NT);
