@@ -2,7 +2,8 @@
 
 Small caches are compared element by element over every output: head widths
 16..128, both storage dtypes, page sizes 1..256, query groups 1..16 (including
-a group that is not a power of two), lengths of one position, on page and
+a group that is not a power of two; bf16 groups of 2 or more run on the tensor
+cores, at every head width), lengths of one position, on page and
 chunk boundaries (a chunk is 256 positions) and ragged. The two full-size decode
 workloads run in the launch configuration the benchmark times and are compared
 on sampled requests (the longest, the one-position one and a middle one), every
@@ -77,6 +78,10 @@ SMALL = [
     ("g16_bf16", 2, 16, 1, 64, 8, 300, "bf16", [300, 64]),
     ("one_chunk_only", 4, 4, 4, 64, 16, 256, "bf16", [256, 1, 16, 255]),
     ("all_len1", 5, 2, 1, 128, 4, 4, "bf16", [1, 1, 1, 1, 1]),
+    # tensor-core kernel at Dh = 16 (8-byte K and 4-byte V fragment loads), pages
+    # smaller than its 16-position block and pages holding whole blocks
+    ("dh16_bf16_g4_ps2", 2, 8, 2, 16, 2, 300, "bf16", [300, 33]),
+    ("dh16_bf16_g2_ps32", 3, 4, 2, 16, 32, 600, "bf16", [600, 1, 257]),
 ]
 
 
