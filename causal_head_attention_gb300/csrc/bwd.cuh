@@ -80,7 +80,9 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const PreArgs 
     real = t < L;
   }
   float acc = 0.f;
-  if (live) {
+  // Padding rows of a variable-length batch are neither read nor zeroed in
+  // the accumulator: their dQ rows are written as zeros by the conversion.
+  if (real) {
     const size_t off = ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * a.Dh + part * EPL;
     const uint4 o = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.out) + off * ES);
     const uint4 g = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.dout) + off * ES);

@@ -555,20 +555,41 @@ rca_status plan_varlen(const int* lens, int64_t B, int64_t Hq, int64_t Hkv, int6
   return RCA_OK;
 }
 
-// Zero the rows at or past each sequence's length (and -inf LSE) of x [B, T, H, Dh].
+// Zero the rows at or past each sequence's length (and -inf LSE) of x [B, T, H, Dh]:
+// one grid column per sequence, covering only its padding.
 rca_status zero_padding(void* x, float* lse, const int* lens, int64_t B, int64_t T, int64_t H, int64_t Dh,
                         rca_dtype dt, cudaStream_t st) {
-  const int64_t nvec = B * T * H * Dh * (dt == RCA_BF16 ? 2 : 4) / 16;
+  const int64_t per_seq = T * H * Dh * (dt == RCA_BF16 ? 2 : 4) / 16;  // 16-byte vectors
   int sms = 0;
   RCA_CHECK(sm_count(&sms));
-  const int64_t want = (nvec + 255) / 256, cap = int64_t(sms) * 8;
-  const unsigned grid = unsigned(want < cap ? (want > 0 ? want : 1) : cap);
+  const int64_t want = (per_seq + 1023) / 1024, cap = std::max<int64_t>(1, int64_t(sms) * 8 / B);
+  const dim3 grid(unsigned(std::max<int64_t>(1, std::min(want, cap))), unsigned(B));
   if (dt == RCA_BF16)
-    rca::varlen_zero_kernel<2><<<grid, 256, 0, st>>>(x, lse, lens, int(B), int(T), int(H), int(Dh));
+    rca::varlen_zero_kernel<2><<<grid, 256, 0, st>>>(x, lse, lens, int(T), int(H), int(Dh));
   else
-    rca::varlen_zero_kernel<4><<<grid, 256, 0, st>>>(x, lse, lens, int(B), int(T), int(H), int(Dh));
+    rca::varlen_zero_kernel<4><<<grid, 256, 0, st>>>(x, lse, lens, int(T), int(H), int(Dh));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch varlen_zero_kernel");
+  return RCA_OK;
+}
+
+// dQ of a variable-length batch: real rows converted from the accumulator,
+// padding rows written as zeros.
+rca_status varlen_convert(void* dq, const int* lens, int64_t B, int64_t Hq, int64_t T, int64_t Dh, rca_dtype dt,
+                          const void* ws, const WsLayout& L, cudaStream_t st) {
+  const float* acc = reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws) + L.dq_off);
+  const long long row4 = Hq * Dh / 4;
+  int sms = 0;
+  RCA_CHECK(sm_count(&sms));
+  const int64_t want = (T * row4 + 1023) / 1024, cap = std::max<int64_t>(1, int64_t(sms) * 8 / B);
+  const dim3 grid(unsigned(std::max<int64_t>(1, std::min(want, cap))), unsigned(B));
+  const float scale = float(1.0 / std::sqrt(double(Dh)));
+  if (dt == RCA_BF16)
+    rca::varlen_dq_convert_kernel<false><<<grid, 256, 0, st>>>(acc, dq, lens, int(T), row4, scale);
+  else
+    rca::varlen_dq_convert_kernel<true><<<grid, 256, 0, st>>>(acc, dq, lens, int(T), row4, scale);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch varlen_dq_convert_kernel");
   return RCA_OK;
 }
 
@@ -1044,7 +1065,7 @@ rca_status rca_attn_bwd_varlen(const void* q, const void* k, const void* v, cons
   RCA_CHECK(plan_varlen(seq_lens, B, Hq, Hkv, T, workspace, V, st, &fi, &fc, &bi, &bc));
   RCA_CHECK(do_preprocess(out, lse, dout, B, Hq, T, Dh, dt, workspace, L, st, seq_lens));
   RCA_CHECK(do_bwd_main(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, dt, workspace, L, st, nullptr, 0, 0, 0, bi, bc));
-  RCA_CHECK(do_convert(dq, B, Hq, T, Dh, dt, workspace, L, st));
+  RCA_CHECK(varlen_convert(dq, seq_lens, B, Hq, T, Dh, dt, workspace, L, st));
   RCA_CHECK(zero_padding(dk, nullptr, seq_lens, B, T, Hkv, Dh, dt, st));
   return zero_padding(dv, nullptr, seq_lens, B, T, Hkv, Dh, dt, st);
   RCA_GUARD_END

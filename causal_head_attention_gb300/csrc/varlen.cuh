@@ -110,26 +110,63 @@ __global__ void __launch_bounds__(kVarlenPlanThreads) varlen_plan_kernel(const V
 }
 
 // Zero the rows of positions t >= L_b of a [B, T, H, Dh] tensor (storage
-// dtype, ES bytes) and, if lse is given, set lse[b, h, t] = -inf there. One
-// thread per 16 bytes.
+// dtype, ES bytes) and, if lse is given, set lse[b, h, t] = -inf there.
+// blockIdx.y is the sequence b; its padding is one contiguous range of
+// 16-byte vectors, [L_b * vpr, T * vpr) of its slab, so no thread divides to
+// find its row and none touches a real row.
 template <int ES>
 __global__ void __launch_bounds__(256)
-    varlen_zero_kernel(void* __restrict__ x, float* __restrict__ lse, const int* __restrict__ lens, int B, int T,
-                       int H, int Dh) {
-  const long long vec_per_row = static_cast<long long>(H) * Dh * ES / 16;
-  const long long n = static_cast<long long>(B) * T * vec_per_row;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long row = i / vec_per_row;
-    const int t = static_cast<int>(row % T), b = static_cast<int>(row / T);
-    int L = __ldg(lens + b);
-    L = L < 0 ? 0 : (L > T ? T : L);
-    if (t < L) continue;
-    reinterpret_cast<uint4*>(x)[i] = make_uint4(0, 0, 0, 0);
-    const int v = static_cast<int>(i % vec_per_row);
-    if (lse && v * 16 / ES % Dh == 0) {
-      const int h = v * 16 / ES / Dh;
+    varlen_zero_kernel(void* __restrict__ x, float* __restrict__ lse, const int* __restrict__ lens, int T, int H,
+                       int Dh) {
+  const int b = blockIdx.y;
+  int L = __ldg(lens + b);
+  L = L < 0 ? 0 : (L > T ? T : L);
+  const long long vpr = static_cast<long long>(H) * Dh * ES / 16;  // vectors per position
+  uint4* slab = reinterpret_cast<uint4*>(x) + static_cast<long long>(b) * T * vpr;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long first = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (long long i = L * vpr + first; i < T * vpr; i += stride) slab[i] = make_uint4(0, 0, 0, 0);
+  if (lse) {
+    const int np = T - L;  // padding positions of each head's LSE row
+    for (long long k = first; k < static_cast<long long>(H) * np; k += stride) {
+      const int h = static_cast<int>(k / np), t = L + static_cast<int>(k - static_cast<long long>(h) * np);
       lse[(static_cast<long long>(b) * H + h) * T + t] = -INFINITY;
+    }
+  }
+}
+
+// dQ = scale * accumulator for a variable-length batch: blockIdx.y is the
+// sequence b; rows t < L_b are converted, rows past it written as zeros
+// without reading the accumulator (the backward leaves those rows stale).
+// row4 = Hq * Dh / 4 float4 groups per position; U loads in flight per thread.
+template <bool F32>
+__global__ void __launch_bounds__(256)
+    varlen_dq_convert_kernel(const float* __restrict__ acc, void* __restrict__ dq, const int* __restrict__ lens,
+                             int T, long long row4, float scale) {
+  constexpr int U = 4;
+  const int b = blockIdx.y;
+  int L = __ldg(lens + b);
+  L = L < 0 ? 0 : (L > T ? T : L);
+  const long long base = static_cast<long long>(b) * T * row4, n = T * row4, real = L * row4;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += U * stride) {
+    float4 v[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const long long j = i + k * stride;
+      v[k] = j < real ? reinterpret_cast<const float4*>(acc)[base + j] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const long long j = i + k * stride;
+      if (j >= n) continue;
+      if constexpr (F32) {
+        reinterpret_cast<float4*>(dq)[base + j] =
+            make_float4(v[k].x * scale, v[k].y * scale, v[k].z * scale, v[k].w * scale);
+      } else {
+        reinterpret_cast<uint2*>(dq)[base + j] = make_uint2(pack_bf16(v[k].x * scale, v[k].y * scale),
+                                                           pack_bf16(v[k].z * scale, v[k].w * scale));
+      }
     }
   }
 }
