@@ -112,6 +112,63 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const PreArgs 
   }
 }
 
+// Variable-length batch: blockIdx.y is the sequence b, and only the rows the
+// backward reads are visited: positions t < 128 * ceil(L_b / 128) (the query
+// tiles that hold real rows). Real rows (t < L_b) get D and LSE2 and a zeroed
+// accumulator row; the rest of their last tile gets D = 0, LSE2 = -inf. Rows
+// past it are never read and not written. Same lane groups as the dense
+// kernel (lpr lanes per row, a power of two).
+template <bool F32>
+__global__ void __launch_bounds__(256) attn_bwd_preprocess_varlen_kernel(const PreArgs a) {
+  constexpr int ES = F32 ? 4 : 2;
+  constexpr int EPL = 16 / ES;
+  const int b = blockIdx.y;
+  int L = __ldg(a.lens + b);
+  if (L < 0 || L > a.T) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicExch(a.status, kStatusBadInput);
+    L = L < 0 ? 0 : a.T;
+  }
+  const unsigned lpr = static_cast<unsigned>(a.Dh / EPL);
+  const unsigned rows = static_cast<unsigned>((L + 127) / 128 * 128) * a.Hq;  // (t, h) rows of real tiles
+  const unsigned stride = gridDim.x * blockDim.x;
+  for (unsigned i0 = blockIdx.x * blockDim.x; i0 < rows * lpr; i0 += stride) {  // uniform per block
+    const unsigned gid = i0 + threadIdx.x;
+    const unsigned row = gid / lpr, part = gid % lpr;
+    const bool in = row < rows;
+    const int t = static_cast<int>(row / a.Hq), h = static_cast<int>(row % a.Hq);
+    const bool real = in && t < L;
+    float acc = 0.f;
+    if (real) {
+      const size_t off = ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * a.Dh + part * EPL;
+      const uint4 o = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.out) + off * ES);
+      const uint4 g = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.dout) + off * ES);
+      const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+      const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if constexpr (F32) {
+          acc = fmaf(__uint_as_float(ow[i]), __uint_as_float(gw[i]), acc);
+        } else {
+          const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[i]));
+          const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[i]));
+          acc = fmaf(of.x, gf.x, acc);
+          acc = fmaf(of.y, gf.y, acc);
+        }
+      }
+      float4* z = reinterpret_cast<float4*>(a.dq_acc + off);
+#pragma unroll
+      for (int i = 0; i < EPL / 4; ++i) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (unsigned o = lpr >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, lpr);
+    if (in && part == 0) {
+      const size_t so = (static_cast<size_t>(b) * a.Hq + h) * a.Tpad + t;
+      a.dvec[so] = real ? -acc : 0.f;
+      a.lse2[so] = real ? -(a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.T + t] * 1.4426950408889634f)
+                        : -INFINITY;
+    }
+  }
+}
+
 // ----------------------------------------------------------------------------
 // dQ convert
 // ----------------------------------------------------------------------------

@@ -555,19 +555,20 @@ rca_status plan_varlen(const int* lens, int64_t B, int64_t Hq, int64_t Hkv, int6
   return RCA_OK;
 }
 
-// Zero the rows at or past each sequence's length (and -inf LSE) of x [B, T, H, Dh]:
-// one grid column per sequence, covering only its padding.
+// Zero the rows at or past each sequence's length (and -inf LSE) of x [B, T, H, Dh]
+// and, if given, of x2 of the same shape: one grid column per sequence (and
+// tensor), covering only its padding.
 rca_status zero_padding(void* x, float* lse, const int* lens, int64_t B, int64_t T, int64_t H, int64_t Dh,
-                        rca_dtype dt, cudaStream_t st) {
+                        rca_dtype dt, cudaStream_t st, void* x2 = nullptr) {
   const int64_t per_seq = T * H * Dh * (dt == RCA_BF16 ? 2 : 4) / 16;  // 16-byte vectors
   int sms = 0;
   RCA_CHECK(sm_count(&sms));
   const int64_t want = (per_seq + 1023) / 1024, cap = std::max<int64_t>(1, int64_t(sms) * 8 / B);
-  const dim3 grid(unsigned(std::max<int64_t>(1, std::min(want, cap))), unsigned(B));
+  const dim3 grid(unsigned(std::max<int64_t>(1, std::min(want, cap))), unsigned(B), x2 ? 2u : 1u);
   if (dt == RCA_BF16)
-    rca::varlen_zero_kernel<2><<<grid, 256, 0, st>>>(x, lse, lens, int(T), int(H), int(Dh));
+    rca::varlen_zero_kernel<2><<<grid, 256, 0, st>>>(x, x2, lse, lens, int(T), int(H), int(Dh));
   else
-    rca::varlen_zero_kernel<4><<<grid, 256, 0, st>>>(x, lse, lens, int(T), int(H), int(Dh));
+    rca::varlen_zero_kernel<4><<<grid, 256, 0, st>>>(x, x2, lse, lens, int(T), int(H), int(Dh));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch varlen_zero_kernel");
   return RCA_OK;
@@ -608,6 +609,21 @@ rca_status do_preprocess(const void* out, const float* lse, const void* dout, in
   a.dvec = reinterpret_cast<float*>(w + L.d_off);
   a.B = int(B); a.Hq = int(Hq); a.T = int(T); a.Dh = int(Dh); a.Tpad = int(L.Tpad);
   const int64_t lpr = Dh / (dt == RCA_BF16 ? 8 : 4);
+  if (lens && L.Tpad * Hq * lpr < (int64_t(1) << 31)) {
+    // Variable-length batch: one grid column per sequence, over the rows of
+    // its real tiles only.
+    int sms = 0;
+    RCA_CHECK(sm_count(&sms));
+    const int64_t want = (L.Tpad * Hq * lpr + 255) / 256, cap = std::max<int64_t>(1, int64_t(sms) * 8 / B);
+    const dim3 grid(unsigned(std::max<int64_t>(1, std::min(want, cap))), unsigned(B));
+    if (dt == RCA_BF16)
+      rca::attn_bwd_preprocess_varlen_kernel<false><<<grid, 256, 0, st>>>(a);
+    else
+      rca::attn_bwd_preprocess_varlen_kernel<true><<<grid, 256, 0, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launch attn_bwd_preprocess_varlen_kernel");
+    return RCA_OK;
+  }
   const int64_t threads = B * L.Tpad * Hq * lpr;
   const unsigned grid = unsigned((threads + 255) / 256);
   const bool narrow = (int64_t(grid) * 256) < (int64_t(1) << 31);  // 32-bit thread indices suffice
@@ -1066,8 +1082,7 @@ rca_status rca_attn_bwd_varlen(const void* q, const void* k, const void* v, cons
   RCA_CHECK(do_preprocess(out, lse, dout, B, Hq, T, Dh, dt, workspace, L, st, seq_lens));
   RCA_CHECK(do_bwd_main(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, dt, workspace, L, st, nullptr, 0, 0, 0, bi, bc));
   RCA_CHECK(varlen_convert(dq, seq_lens, B, Hq, T, Dh, dt, workspace, L, st));
-  RCA_CHECK(zero_padding(dk, nullptr, seq_lens, B, T, Hkv, Dh, dt, st));
-  return zero_padding(dv, nullptr, seq_lens, B, T, Hkv, Dh, dt, st);
+  return zero_padding(dk, nullptr, seq_lens, B, T, Hkv, Dh, dt, st, dv);
   RCA_GUARD_END
 }
 

@@ -114,10 +114,16 @@ __global__ void __launch_bounds__(kVarlenPlanThreads) varlen_plan_kernel(const V
 // blockIdx.y is the sequence b; its padding is one contiguous range of
 // 16-byte vectors, [L_b * vpr, T * vpr) of its slab, so no thread divides to
 // find its row and none touches a real row.
+// blockIdx.z = 1 (when x2 is given) zeroes the padding of x2 instead, a
+// second tensor of the same shape, in the same launch.
 template <int ES>
 __global__ void __launch_bounds__(256)
-    varlen_zero_kernel(void* __restrict__ x, float* __restrict__ lse, const int* __restrict__ lens, int T, int H,
-                       int Dh) {
+    varlen_zero_kernel(void* __restrict__ x, void* __restrict__ x2, float* __restrict__ lse,
+                       const int* __restrict__ lens, int T, int H, int Dh) {
+  if (blockIdx.z == 1) {
+    x = x2;
+    lse = nullptr;
+  }
   const int b = blockIdx.y;
   int L = __ldg(lens + b);
   L = L < 0 ? 0 : (L > T ? T : L);
