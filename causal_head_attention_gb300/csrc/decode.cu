@@ -558,11 +558,11 @@ __global__ void __launch_bounds__(NT, (Cfg<BF16, DH, G>::MINB)) decode_kernel(Ar
 // Softmax state per lane: the running max and partial sum of its two heads
 // (2t, 2t + 1 for quad lane t), the max being the same across the lane groups.
 // ---------------------------------------------------------------------------
-#ifndef DEC_MMA_PREFETCH
-#define DEC_MMA_PREFETCH 0
-#endif
+// Resident CTAs per SM the tensor-core kernel's registers are sized for (one
+// 16-position block of K and V per warp in flight; a second block in flight
+// at 2 CTAs per SM, or 4 CTAs per SM with spills, both measured slower).
 #ifndef DEC_MMA_MINB
-#define DEC_MMA_MINB (DEC_MMA_PREFETCH ? 2 : 3)
+#define DEC_MMA_MINB 3
 #endif
 static_assert(kDecodeChunk / 16 <= 32 * NW, "a warp's block pages fit one lane each");
 
@@ -783,26 +783,11 @@ __global__ void __launch_bounds__(NT, DEC_MMA_MINB) decode_mma_kernel(Args a) {
       }
     };
 
-#if DEC_MMA_PREFETCH
-    // Two blocks in flight: the next block's loads are issued before this
-    // block's products.
-    MmaBlock<DH> b0, b1;
-    if (nmy > 0) load_block(b0, 0);
-    for (int i = 0; i < nmy; i += 2) {
-      if (i + 1 < nmy) load_block(b1, i + 1);
-      compute_block(b0, i);
-      if (i + 1 < nmy) {
-        if (i + 2 < nmy) load_block(b0, i + 2);
-        compute_block(b1, i + 1);
-      }
-    }
-#else
     for (int i = 0; i < nmy; ++i) {
       MmaBlock<DH> bk;
       load_block(bk, i);
       compute_block(bk, i);
     }
-#endif
 
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
