@@ -199,3 +199,27 @@ def test_validation_errors_do_not_launch():
         rca.rca_paged_decode(q, kp, vp, table, lens, out, lse, ws)
     assert ei.value.status == 1 and "workspace" in str(ei.value)
     rca.rca_stream_status()
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 1), (2, 2)], ids=["tensor_core_g4", "cuda_core_g1"])
+def test_maximum_batch(hq, hkv):
+    """8192 requests (the most one call takes): every CTA rebuilds the request
+    prefix sums over the whole batch in shared memory. Sampled requests are
+    compared element by element; every output must be finite."""
+    w = PagedWorkload(f"maxbatch_{hq}_{hkv}", 8192, hq, hkv, 16, 16, 300, "bf16", 25)
+    q, kp, vp, table, lens = make_paged_inputs(w)
+    out, lse = run_gpu(q, kp, vp, table, lens)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    n = lens.numpy()
+    rows = sorted({0, 1, 4095, 4096, 8191, int(np.argmax(n)), int(np.argmin(n))})
+    ref_o, ref_l = oracle_of(q, kp, vp, table, lens, rows)
+    check(w.name, "bf16", out, lse, ref_o, ref_l, rows)
+
+
+def test_maximum_page_size():
+    """Pages of 65536 positions (the largest page size) and a request spanning two."""
+    w = PagedWorkload("maxpage", 2, 4, 2, 16, 65536, 70000, "bf16", 26)
+    q, kp, vp, table, lens = make_paged_inputs(w, [70000, 5])
+    out, lse = run_gpu(q, kp, vp, table, lens)
+    ref_o, ref_l = oracle_of(q, kp, vp, table, lens)
+    check("maxpage", "bf16", out, lse, ref_o, ref_l)

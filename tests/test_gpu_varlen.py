@@ -123,3 +123,33 @@ def test_bad_length_is_reported():
     out2, _ = rca.attention_forward_varlen(qd, kd, vd, torch.tensor([64, 64], dtype=torch.int32, device=dev))
     rca.rca_stream_status()
     assert torch.equal(out, out2)  # clamped to T
+
+
+def test_maximum_batch_sampled():
+    """4096 sequences (the most one call takes) of one tile each: the planner
+    sorts and lists them all on the device. Padding is exactly zero everywhere;
+    sampled sequences, including empty and full ones, match the oracle."""
+    B, T = 4096, 128
+    w = small("vl_maxbatch", B, 2, 1, T, 64, "bf16", seed=45)
+    q, k, v, do = make_inputs(w)
+    g = torch.Generator().manual_seed(46)
+    lens = torch.randint(0, T + 1, (B,), generator=g)
+    lens[0], lens[1], lens[B - 1] = 0, T, 1
+    lens = lens.tolist()
+    out, lse, dq, dk, dv = run(q, k, v, do, lens)
+    m = real_mask(lens, T)
+    for name, x in (("O", out), ("dQ", dq), ("dK", dk), ("dV", dv)):
+        assert torch.all(x.float().cpu()[torch.from_numpy(~m)] == 0), f"{name} nonzero at padding"
+    sel = [0, 1, 2, 2047, B - 2, B - 1]
+    q64, k64, v64, do64 = (to64(x)[sel] for x in (q, k, v, do))
+    ls = [lens[i] for i in sel]
+    o_ref, l_ref = oracle.attention_forward_varlen(q64, k64, v64, ls)
+    g_ref = oracle.attention_backward_varlen(q64, k64, v64, do64, ls)
+    ms = real_mask(ls, T)
+    got = {"O": to64(out)[sel], "dQ": to64(dq)[sel], "dK": to64(dk)[sel], "dV": to64(dv)[sel]}
+    ref = {"O": o_ref, "dQ": g_ref[0], "dK": g_ref[1], "dV": g_ref[2]}
+    for n in got:
+        assert rel_fro(got[n][ms], ref[n][ms]) <= TOL["bf16"][n], n
+    lg = to64(lse)[sel]
+    lm = np.broadcast_to(ms[:, None, :], lg.shape)
+    assert np.all(np.isneginf(lg[~lm])) and rel_fro(lg[lm], l_ref[lm]) <= TOL["bf16"]["LSE"]
