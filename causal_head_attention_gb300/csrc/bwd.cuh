@@ -252,9 +252,10 @@ struct BwdCfg {
   static constexpr int SMEM_LIMIT = 232448;
   static constexpr int BAR_BYTES = 1024;
   static constexpr int STAGE_BYTES = 2 * OPND + 1024;   // Q, dO, LSE2[128], D[128]
-  // bf16 storage with a 64-column head: dQ is staged as fp32, 32 columns at a
-  // time, for bulk tensor reductions in a 16 KB panel of its own.
-  static constexpr bool TMA_DQ = !HL && DHB == 64;
+  // bf16 storage: dQ is staged as fp32, 32 columns at a time, for bulk tensor
+  // reductions in a 16 KB panel of its own (per-thread vector reductions of a
+  // whole dQ partial per iteration saturate the load/store queue).
+  static constexpr bool TMA_DQ = !HL && (DHB == 64 || DHB == 128);
   static constexpr int DQS_BYTES = TMA_DQ ? PANEL : 0;
   static constexpr int AVAIL = SMEM_LIMIT - 1024 - BAR_BYTES - KVB * 2 * OPND - DQS_BYTES;
   static constexpr int NQS_SEP = (AVAIL - P_SMEM - P_BYTES) / STAGE_BYTES;
@@ -285,7 +286,6 @@ struct BwdCfg {
   // dQ products are pending; that needs a second Q/dO stage, separate P^T and
   // dS^T buffers and dQ columns of its own.
   static constexpr bool PREFETCH = (NQS >= 2) && !DQ_ALIAS && !SHARE;
-  static_assert(!TMA_DQ || PREFETCH, "bulk dQ reduction assumes the prefetch schedule");
   static_assert(!PTB || PREFETCH, "persistent CTAs assume the prefetch schedule");
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_T = make_idesc(false, 128, 128, false, false);   // S^T, dP^T
