@@ -252,10 +252,11 @@ struct BwdCfg {
   static constexpr int SMEM_LIMIT = 232448;
   static constexpr int BAR_BYTES = 1024;
   static constexpr int STAGE_BYTES = 2 * OPND + 1024;   // Q, dO, LSE2[128], D[128]
-  // bf16 storage: dQ is staged as fp32, 32 columns at a time, for bulk tensor
-  // reductions in a 16 KB panel of its own (per-thread vector reductions of a
-  // whole dQ partial per iteration saturate the load/store queue).
-  static constexpr bool TMA_DQ = !HL && (DHB == 64 || DHB == 128);
+  // dQ is staged as fp32, 32 columns at a time, for bulk tensor reductions in
+  // a 16 KB panel of its own (per-thread vector reductions of a whole dQ
+  // partial per iteration saturate the load/store queue); every layout but
+  // the 32-column head has the room.
+  static constexpr bool TMA_DQ = DHB == 64 || DHB == 128;
   static constexpr int DQS_BYTES = TMA_DQ ? PANEL : 0;
   static constexpr int AVAIL = SMEM_LIMIT - 1024 - BAR_BYTES - KVB * 2 * OPND - DQS_BYTES;
   static constexpr int NQS_SEP = (AVAIL - P_SMEM - P_BYTES) / STAGE_BYTES;
