@@ -254,10 +254,8 @@ struct BwdCfg {
   static constexpr int STAGE_BYTES = 2 * OPND + 1024;   // Q, dO, LSE2[128], D[128]
   // dQ is staged as fp32, 32 columns at a time, for bulk tensor reductions in
   // a 16 KB panel of its own (per-thread vector reductions of a whole dQ
-  // partial per iteration saturate the load/store queue); every layout but
-  // the 32-column head has the room.
-  static constexpr bool TMA_DQ = DHB == 64 || DHB == 128;
-  static constexpr int DQS_BYTES = TMA_DQ ? PANEL : 0;
+  // partial per iteration saturate the load/store queue).
+  static constexpr int DQS_BYTES = PANEL;
   static constexpr int AVAIL = SMEM_LIMIT - 1024 - BAR_BYTES - KVB * 2 * OPND - DQS_BYTES;
   static constexpr int NQS_SEP = (AVAIL - P_SMEM - P_BYTES) / STAGE_BYTES;
   static constexpr int NQS_SHR = (AVAIL - P_BYTES) / STAGE_BYTES;
@@ -334,7 +332,6 @@ struct BwdArgs {
   long long dkv_row;   // elements between consecutive positions of dK, dV (Hkv * Dh if contiguous)
   const int4* items;       // variable-length batches: work list {b, kvh, j, n_i} (null: all items)
   const int* n_items_dev;  // its length (device)
-  float* dq_acc;       // [B, T, Hq, Dh]
   const float* lse2;   // [B, Hq, Tpad]
   const float* dvec;   // [B, Hq, Tpad]
   int* status;
@@ -715,11 +712,10 @@ __global__ void __launch_bounds__(512, 1)
     // is done, so the compute warpgroups go straight on to the next item.
     // Warp q reads TMEM lanes 32 q .. 32 q + 31 (query rows) of every dQ
     // partial, 32 head columns at a time, and adds them to the fp32
-    // accumulator: bf16 storage with a 64-column head stages each 32 x 32
-    // block in the warp's 4 KB, 128-byte-swizzled slice of the staging panel
-    // and adds it with a bulk tensor reduction issued by the warp's lane 0
-    // (the slice is rewritten only after that lane's previous reduction has
-    // read it); otherwise every lane adds its row with vector reductions.
+    // accumulator: each 32 x 32 block is staged in the warp's 4 KB,
+    // 128-byte-swizzled slice of the staging panel and added with a bulk
+    // tensor reduction issued by the warp's lane 0 (the slice is rewritten only
+    // after that lane's previous reduction has read it).
     const int quarter = warp;
     const int rl = quarter * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -786,40 +782,28 @@ __global__ void __launch_bounds__(512, 1)
             tc_fence_before();
             mbar_arrive(bar(C::B_ITF));  // dQ(gi) read: its columns may be overwritten
           }
-          if constexpr (C::TMA_DQ) {
-            const uint32_t panel = sbase + C::OFF_DQS;
-            if (lane == 0) bulk_wait_read0();  // the previous block has been read from the slice
-            __syncwarp();
+          const uint32_t panel = sbase + C::OFF_DQS;
+          if (lane == 0) bulk_wait_read0();  // the previous block has been read from the slice
+          __syncwarp();
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              st_shared_v4(panel + rl * 128 + ((k ^ (rl & 7)) << 4), r[4 * k], r[4 * k + 1], r[4 * k + 2],
-                           r[4 * k + 3]);
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              if (32 * c < a.Dh)  // a block past the head width has nothing to add
-                tma_reduce_add_4d(&maps.dq, panel + quarter * 4096, 32 * c, h, i * 128 + quarter * 32, itm.b);
-              bulk_commit();
-            }
-          } else {
-            const int qrow = i * 128 + rl;
-            const int ncol = a.Dh - 32 * c;
-            if (qrow < a.T && ncol > 0) {
-              float* dst = a.dq_acc + ((static_cast<size_t>(itm.b) * a.T + qrow) * a.Hq + h) * a.Dh + 32 * c;
-#pragma unroll
-              for (int u = 0; u < 8; ++u)
-                if (4 * u < ncol)
-                  red_add_v4(dst + 4 * u, __uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
-                             __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
-            }
+          for (int k = 0; k < 8; ++k)
+            st_shared_v4(panel + rl * 128 + ((k ^ (rl & 7)) << 4), r[4 * k], r[4 * k + 1], r[4 * k + 2],
+                         r[4 * k + 3]);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            // A block past the head width has nothing to add; columns and rows
+            // past the tensor's edge (a head narrower than the 32-column box, a
+            // partial last query tile) are clipped by the reduction itself.
+            if (32 * c < a.Dh)
+              tma_reduce_add_4d(&maps.dq, panel + quarter * 4096, 32 * c, h, i * 128 + quarter * 32, itm.b);
+            bulk_commit();
           }
         }
       }
     }
-    if constexpr (C::TMA_DQ) {
-      if (lane == 0) bulk_wait0();  // every bulk reduction this warp issued has landed
-      __syncwarp();
-    }
+    if (lane == 0) bulk_wait0();  // every bulk reduction this warp issued has landed
+    __syncwarp();
     end_role();
   } else {
     reg_alloc<C::REG_CMP>();

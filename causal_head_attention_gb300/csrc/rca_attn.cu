@@ -440,7 +440,6 @@ rca_status launch_bwd_main(const void* q, const void* k, const void* v, const vo
   a.dkv_row = dkvs;
   a.items = items;
   a.n_items_dev = n_items_dev;
-  a.dq_acc = reinterpret_cast<float*>(w + L.dq_off);
   a.lse2 = reinterpret_cast<const float*>(w + L.lse2_off);
   a.dvec = reinterpret_cast<const float*>(w + L.d_off);
   a.status = status;

@@ -342,12 +342,6 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
-// Vector fp32 reduction into global memory with no returned value (no
-// scoreboard dependency for the issuing thread).
-__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
 // Three-input maximum (one instruction on sm_100+).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
