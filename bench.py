@@ -226,6 +226,51 @@ def oracle_sample(w, budget_s: float, max_groups: int | None = None):
     return done * per_group, dt, threads, done
 
 
+def input_sets(w) -> tuple[int, int]:
+    """(number of rotating input copies, bytes of one copy): enough distinct
+    copies of a step's inputs that together they exceed twice the L2 size."""
+    es = 2 if w.dtype == "bf16" else 4
+    set_bytes = es * w.B * w.T * w.Dh * (2 * w.Hq + 2 * w.Hkv)
+    return max(2, -(-2 * L2_BYTES // set_bytes) + 1), set_bytes
+
+
+def config_for(w, world: int) -> dict:
+    """The `config` object of the JSON line; both arms print the same one."""
+    nsets, set_bytes = input_sets(w)
+    return {"workload": w.describe(), "name": w.name, "global_batch": w.B * world, "seq_len": w.T,
+            "heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.Dh, "parallelism": f"independent units x{world}",
+            "l2": f"GPU arm: {nsets} rotating input sets ({nsets * set_bytes / 2**20:.0f} MiB) > L2",
+            "flop_convention": "fwd 4*B*H*T^2*Dh/2; bwd 2.5x fwd; step 3.5x fwd"}
+
+
+def launches_per_step(w) -> int:
+    """Kernels this library launches per training step: forward, preprocess,
+    backward main, dQ conversion; fp32 storage adds the four bf16 hi/lo splits
+    of Q, dO, K and V."""
+    return 4 if w.dtype == "bf16" else 8
+
+
+def nominal_tflops(sms: int, sm_mhz: float, dtype: str) -> float:
+    """Nominal dense tensor peak at the sampled SM clock: SMs x 8192 bf16
+    FLOP per clock per SM (one M=128 N=256 K=16 tcgen05 MMA per 128 cycles),
+    half that for TF32 operands."""
+    per_clk = 8192.0 if dtype == "bf16" else 4096.0
+    return sms * per_clk * sm_mhz * 1e6 / 1e12
+
+
+def spread(xs) -> dict:
+    """Mean, median, 10th and 90th percentile of a list of per-step times (ms)."""
+    s = sorted(xs)
+    n = len(s)
+
+    def pct(p):
+        i = (n - 1) * p
+        lo, hi = int(i), min(int(i) + 1, n - 1)
+        return s[lo] + (s[hi] - s[lo]) * (i - lo)
+
+    return {"mean": sum(s) / n, "median": pct(0.5), "p10": pct(0.1), "p90": pct(0.9)}
+
+
 def run_reference(args, w, world, rank):
     if rank != 0:
         return 0
@@ -244,7 +289,7 @@ def run_reference(args, w, world, rank):
         "impl": "reference", "metric": args.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / len(steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": w.describe(), "name": w.name, "parallelism": "none (host cores)"},
+        "data": "synthetic", "config": config_for(w, world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": f"{n_groups} of {w.B * w.Hkv} (batch, KV-head) groups per step, fwd+bwd, fp64"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -267,8 +312,8 @@ def run_gpu(args, w, world, rank, local):
     P = peaks()
 
     q0, k0, v0, do0 = make_inputs(rank_workload(w, rank))
-    set_bytes = sum(x.numel() * x.element_size() for x in (q0, k0, v0, do0))
-    nsets = max(2, -(-2 * L2_BYTES // set_bytes) + 1)
+    nsets, set_bytes = input_sets(w)
+    assert set_bytes == sum(x.numel() * x.element_size() for x in (q0, k0, v0, do0))
     # Distinct copies of the same inputs, so each step reads memory the previous
     # steps evicted from L2.
     base = tuple(x.to(dev) for x in (q0, k0, v0, do0))
@@ -297,18 +342,15 @@ def run_gpu(args, w, world, rank, local):
         if ev is not None:
             ev[4].record(stream)
 
-    # Warm-up: at least W steps and at least ~1 s of work, with the clock sampler
-    # already running, so that clock samples cover the GPU under this load.
+    # Warm-up: exactly W untimed steps. The clock sampler runs from here to the
+    # end of a >= 1 s run of the same step right after the timed region, so its
+    # samples (100 ms apart) cover the GPU under this load, the timed steps
+    # included.
     clk = ClockSampler(local)
     clk.start()
-    t_w = time.perf_counter()
-    i = 0
-    while i < args.warmup or time.perf_counter() - t_w < args.min_warmup_s:
+    for i in range(args.warmup):
         step(i)
-        i += 1
-        if i % 64 == 0:
-            torch.cuda.synchronize(dev)
-    n_warm = i
+    n_warm = args.warmup
     rca.rca_stream_status(stream)
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
@@ -322,7 +364,20 @@ def run_gpu(args, w, world, rank, local):
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
+    # The same step again, untimed, for at least min_warmup_s: clock samples
+    # under load (the timed steps alone last only milliseconds).
+    t_c = time.perf_counter()
+    n_clock = 0
+    while time.perf_counter() - t_c < args.min_warmup_s:
+        step(n_warm + args.steps + n_clock)
+        n_clock += 1
+        if n_clock % 64 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
     clocks = clk.stop()
+    if clocks is not None:
+        clocks["window"] = (f"{args.warmup} warm-up + {args.steps} timed steps + {n_clock} more steps "
+                            f"({time.perf_counter() - t_c:.1f} s) after the timed region")
     rca.rca_stream_status(stream)
     total_ms = t_start.elapsed_time(t_end)
     per = {"fwd": [], "bwd_preprocess": [], "bwd_main": [], "bwd_dq_convert": []}
@@ -331,6 +386,7 @@ def run_gpu(args, w, world, rank, local):
         for j, n in enumerate(names):
             per[n].append(e[j].elapsed_time(e[j + 1]))
     avg = {n: sum(v) / len(v) for n, v in per.items()}
+    step_spread = spread([e[0].elapsed_time(e[4]) for e in evs])
 
     ms = max_over_ranks(total_ms, world) / args.steps
     F = fwd_flops(w)
@@ -360,6 +416,20 @@ def run_gpu(args, w, world, rank, local):
             d["unit"] = "GB/s"
             d["frac"] = d["achieved"] / P["hbm_gbs"]
         d["share"] = d["ms"] / sum(avg.values())
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    clk_mhz = (clocks or {}).get("sm_mhz") or 2070.0
+    peak_nom = nominal_tflops(sms, clk_mhz, w.dtype)
+    for d in kern.values():
+        if d["bound"] == "tensor":
+            d["frac_of_nominal"] = d["achieved"] / peak_nom
+    bwd_ms = avg["bwd_preprocess"] + avg["bwd_main"] + avg["bwd_dq_convert"]
+    bwd_tflops = 2.5 * F / (bwd_ms * 1e-3) / 1e12
+    fracs = {
+        "fwd_frac_of_peak": kern["fwd"]["frac"],
+        "bwd_frac_of_peak": bwd_tflops / peak_tc,
+        "fwd_frac_of_nominal": kern["fwd"]["achieved"] / peak_nom,
+        "bwd_frac_of_nominal": bwd_tflops / peak_nom,
+    }
     dom = max(kern, key=lambda n: kern[n]["ms"])
     dk_ = kern[dom]
     roofline = {
@@ -367,6 +437,11 @@ def run_gpu(args, w, world, rank, local):
         "peak": peak_tc if dk_["bound"] == "tensor" else P["hbm_gbs"], "unit": dk_["unit"],
         "frac": dk_["frac"], "traffic": ncu_traffic(dom, w.name),
         "peak_source": f"{P['source']} (bf16 burst{'; tf32 = bf16/2 nominal ratio' if w.dtype != 'bf16' else ''})",
+        "peak_nominal": peak_nom,
+        "peak_nominal_source": f"{sms} SMs x {8192 if w.dtype == 'bf16' else 4096} FLOP/clk/SM x {clk_mhz:.0f} MHz "
+                               "(median sampled SM clock)",
+        "frac_of_nominal": dk_.get("frac_of_nominal"),
+        **fracs,
     }
 
     # End to end: pinned host inputs -> device -> fwd+bwd -> outputs back to
@@ -471,22 +546,24 @@ def run_gpu(args, w, world, rank, local):
 
     if rank == 0:
         line = {
-            "metric": args.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-            "warmup": n_warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "metric": args.metric, "value": value, "unit": "TFLOP/s", **fracs,
+            "n_gpus": world, "steps": args.steps,
+            "warmup": n_warm, "ms_per_step": ms, "step_ms": step_spread, "higher_is_better": True,
+            "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32 (tf32 MMA)", "data": "synthetic",
-            "config": {"workload": w.describe(), "name": w.name, "global_batch": w.B * world, "seq_len": w.T,
-                       "heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.Dh, "parallelism": f"independent units x{world}",
-                       "l2": f"{nsets} rotating input sets ({nsets * set_bytes / 2**20:.0f} MiB) > L2",
-                       "flop_convention": "fwd 4*B*H*T^2*Dh/2; bwd 2.5x fwd; step 3.5x fwd"},
+            "config": config_for(w, world),
             "roofline": roofline,
+            "min_convention": {
+                "note": "backward counted as 2 x forward (no recompute), step as 3 x forward",
+                "bwd_tflops": 2.0 * F / (bwd_ms * 1e-3) / 1e12,
+                "step_tflops": aggregate_tflops(3.0 * F, world, ms),
+            },
             "kernels": {n: {k2: (round(v2, 6) if isinstance(v2, float) else v2) for k2, v2 in d.items()}
                         for n, d in kern.items()},
-            "fwd_frac_of_peak": kern["fwd"]["frac"],
-            "bwd_frac_of_peak": 2.5 * F / ((avg["bwd_preprocess"] + avg["bwd_main"] + avg["bwd_dq_convert"]) * 1e-3) / 1e12 / peak_tc,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": clocks,
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": launches_per_step(w) * args.steps,
             "paged_decode": decode,
             "materialized": mat,
             "fused_qkv": fused_qkv,
@@ -780,7 +857,8 @@ def main():
     ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(BY_NAME))
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--min-warmup-s", type=float, default=1.0,
-                    help="warm-up runs at least this long (clock samples under load)")
+                    help="after the timed steps, the same step runs untimed at least this long "
+                         "(clock samples under load)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the paged decode measurement")

@@ -33,6 +33,7 @@ from ._native import (  # noqa: F401  (C-ABI names)
     rca_paged_decode,
     rca_paged_decode_workspace_size,
     rca_selftest_device_timeout,
+    rca_selftest_noalloc_timeout,
     rca_set_wait_timeout_ns,
     rca_stream_status,
 )
@@ -75,6 +76,7 @@ __all__ = [
     "rca_last_error",
     "rca_set_wait_timeout_ns",
     "rca_selftest_device_timeout",
+    "rca_selftest_noalloc_timeout",
 ]
 
 

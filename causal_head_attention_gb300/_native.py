@@ -68,6 +68,7 @@ _SIG = {
     "rca_attn_bwd_varlen": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                            ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "rca_selftest_device_timeout": (ctypes.c_int, [_P]),
+    "rca_selftest_noalloc_timeout": (ctypes.c_int, [_P]),
     "rca_stream_status": (ctypes.c_int, [_P]),
     "rca_set_wait_timeout_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
 }
@@ -149,6 +150,38 @@ def _shape(q, k):
     return B, Hq, k.shape[2], T, Dh
 
 
+def _attn_args(q, k, v=None, *, like_q=(), like_k=(), lse=None, workspace=None):
+    """Checks every tensor of a full-sequence call against q and k before any
+    pointer reaches the library: q [B,T,Hq,Dh], k and v [B,T,Hkv,Dh] with the
+    same B, T and Dh; the tensors in like_q (out, dout, dq) shaped and typed as
+    q, those in like_k (dk, dv) as k; lse float32 [B,Hq,T]; all on q's device.
+    Returns (B, Hq, Hkv, T, Dh)."""
+    torch = _torch()
+    B, Hq, Hkv, T, Dh = _shape(q, k)
+    if tuple(k.shape) != (B, T, Hkv, Dh):
+        raise ValueError(f"k must be [B,T,Hkv,Dh] with q's B, T and Dh; got q {tuple(q.shape)}, k {tuple(k.shape)}")
+    named = [("k", k, (B, T, Hkv, Dh))]
+    if v is not None:
+        named.append(("v", v, (B, T, Hkv, Dh)))
+    named += [(n, t, (B, T, Hq, Dh)) for n, t in like_q]
+    named += [(n, t, (B, T, Hkv, Dh)) for n, t in like_k]
+    for name, t, shape in named:
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must have shape {shape}, got {tuple(t.shape)}")
+        if t.dtype != q.dtype:
+            raise TypeError(f"{name} must have q's dtype {q.dtype}, got {t.dtype}")
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}")
+    if lse is not None:
+        if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, T):
+            raise ValueError(f"lse must be float32 [B,Hq,T] = {(B, Hq, T)}, got {lse.dtype} {tuple(lse.shape)}")
+        if lse.device != q.device:
+            raise ValueError(f"lse is on {lse.device}, q on {q.device}")
+    if workspace is not None and workspace.device != q.device:
+        raise ValueError(f"workspace is on {workspace.device}, q on {q.device}")
+    return B, Hq, Hkv, T, Dh
+
+
 def rca_abi_version() -> int:
     return lib().rca_abi_version()
 
@@ -162,7 +195,7 @@ def rca_set_wait_timeout_ns(ns: int) -> int:
 
 
 def rca_attn_fwd(q, k, v, out, lse, stream=None):
-    B, Hq, Hkv, T, Dh = _shape(q, k)
+    B, Hq, Hkv, T, Dh = _attn_args(q, k, v, like_q=[("out", out)], lse=lse)
     _check(lib().rca_attn_fwd(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, T, Dh, _ptr(out), _ptr(lse),
                               _dtype_code(q), _stream(stream)))
 
@@ -176,13 +209,15 @@ def rca_attn_bwd_workspace_size(B, Hq, Hkv, T, Dh, dt) -> int:
 
 
 def rca_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, workspace, stream=None):
-    B, Hq, Hkv, T, Dh = _shape(q, k)
+    B, Hq, Hkv, T, Dh = _attn_args(q, k, v, like_q=[("out", out), ("dout", dout), ("dq", dq)],
+                                   like_k=[("dk", dk), ("dv", dv)], lse=lse, workspace=workspace)
     _check(lib().rca_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
                               _ptr(dk), _ptr(dv), B, Hq, Hkv, T, Dh, _dtype_code(q), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def rca_attn_bwd_preprocess(out, lse, dout, workspace, Hkv=None, stream=None):
+    _attn_args(out, out, like_q=[("dout", dout)], lse=lse, workspace=workspace)
     B, T, Hq, Dh = out.shape
     Hkv = Hq if Hkv is None else Hkv
     _check(lib().rca_attn_bwd_preprocess(_ptr(out), _ptr(lse), _ptr(dout), B, Hq, Hkv, T, Dh, _dtype_code(out),
@@ -191,7 +226,8 @@ def rca_attn_bwd_preprocess(out, lse, dout, workspace, Hkv=None, stream=None):
 
 
 def rca_attn_bwd_main(q, k, v, dout, dk, dv, workspace, stream=None):
-    B, Hq, Hkv, T, Dh = _shape(q, k)
+    B, Hq, Hkv, T, Dh = _attn_args(q, k, v, like_q=[("dout", dout)], like_k=[("dk", dk), ("dv", dv)],
+                                   workspace=workspace)
     _check(lib().rca_attn_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dk), _ptr(dv), B, Hq, Hkv, T,
                                    Dh, _dtype_code(q), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(stream)))
@@ -206,7 +242,8 @@ def rca_attn_bwd_dq_convert(dq, workspace, Hkv=None, stream=None):
 
 def rca_attn_bwd_noalloc(q, k, v, out, lse, dout, dq, dk, dv, stream=None):
     """Backward with the library's built-in scratch (no workspace, no allocation)."""
-    B, Hq, Hkv, T, Dh = _shape(q, k)
+    B, Hq, Hkv, T, Dh = _attn_args(q, k, v, like_q=[("out", out), ("dout", dout), ("dq", dq)],
+                                   like_k=[("dk", dk), ("dv", dv)], lse=lse)
     _check(lib().rca_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
                                       _ptr(dk), _ptr(dv), B, Hq, Hkv, T, Dh, _dtype_code(q), _stream(stream)))
 
@@ -257,7 +294,7 @@ def _check_probs(probs, B, Hq, T, name="probs"):
 
 
 def rca_attn_materialized_fwd(q, k, v, out, probs, lse, workspace, stream=None):
-    B, Hq, Hkv, T, Dh = _shape(q, k)
+    B, Hq, Hkv, T, Dh = _attn_args(q, k, v, like_q=[("out", out)], lse=lse, workspace=workspace)
     _check_probs(probs, B, Hq, T)
     _check(lib().rca_attn_materialized_fwd(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, T, Dh, _ptr(out), _ptr(probs),
                                            _ptr(lse), _dtype_code(q), _ptr(workspace),
@@ -265,7 +302,8 @@ def rca_attn_materialized_fwd(q, k, v, out, probs, lse, workspace, stream=None):
 
 
 def rca_attn_materialized_bwd(q, k, v, probs, dout, dprobs, dq, dk, dv, workspace, stream=None):
-    B, Hq, Hkv, T, Dh = _shape(q, k)
+    B, Hq, Hkv, T, Dh = _attn_args(q, k, v, like_q=[("dout", dout), ("dq", dq)],
+                                   like_k=[("dk", dk), ("dv", dv)], workspace=workspace)
     _check_probs(probs, B, Hq, T)
     if dprobs is not None:
         _check_probs(dprobs, B, Hq, T, "dprobs")
@@ -325,7 +363,7 @@ def rca_attn_varlen_workspace_size(B, Hq, Hkv, T, Dh, dt) -> int:
 
 
 def rca_attn_fwd_varlen(q, k, v, seq_lens, out, lse, workspace, stream=None):
-    B, Hq, Hkv, T, Dh = _shape(q, k)
+    B, Hq, Hkv, T, Dh = _attn_args(q, k, v, like_q=[("out", out)], lse=lse, workspace=workspace)
     _check_lens(seq_lens, B)
     _check(lib().rca_attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), B, Hq, Hkv, T, Dh, _ptr(out),
                                      _ptr(lse), _dtype_code(q), _ptr(workspace),
@@ -333,7 +371,8 @@ def rca_attn_fwd_varlen(q, k, v, seq_lens, out, lse, workspace, stream=None):
 
 
 def rca_attn_bwd_varlen(q, k, v, out, lse, dout, seq_lens, dq, dk, dv, workspace, stream=None):
-    B, Hq, Hkv, T, Dh = _shape(q, k)
+    B, Hq, Hkv, T, Dh = _attn_args(q, k, v, like_q=[("out", out), ("dout", dout), ("dq", dq)],
+                                   like_k=[("dk", dk), ("dv", dv)], lse=lse, workspace=workspace)
     _check_lens(seq_lens, B)
     _check(lib().rca_attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(seq_lens),
                                      _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, T, Dh, _dtype_code(q),
@@ -343,6 +382,10 @@ def rca_attn_bwd_varlen(q, k, v, out, lse, dout, seq_lens, dq, dk, dv, workspace
 
 def rca_selftest_device_timeout(stream=None):
     _check(lib().rca_selftest_device_timeout(_stream(stream)))
+
+
+def rca_selftest_noalloc_timeout(stream=None):
+    _check(lib().rca_selftest_noalloc_timeout(_stream(stream)))
 
 
 def rca_stream_status(stream=None):

@@ -134,6 +134,11 @@ rca_status status_word(int** out) {
   return RCA_OK;
 }
 
+// Reads and clears the allocation-free backward's device status word on the
+// current device (0 when that entry point was never set up there). Defined
+// with the built-in scratch region at the end of this file.
+rca_status noalloc_take_status(int* out);
+
 // Streaming-multiprocessor count of the current device (cached per device).
 int g_sms[256] = {};
 rca_status sm_count(int* out) {
@@ -1112,6 +1117,13 @@ rca_status rca_stream_status(void* cuda_stream) {
   if (h != 0) {
     cudaMemset(status, 0, sizeof(int));
     cudaDeviceSynchronize();
+  }
+  // The allocation-free backward records its device-side failures in a status
+  // word of its own built-in region; report (and clear) that one too.
+  int hn = 0;
+  RCA_CHECK(noalloc_take_status(&hn));
+  if (h == 0) h = hn;
+  if (h != 0) {
     if (h == rca::kStatusBadInput)
       return fail(RCA_ERR_DEVICE_INVALID_INPUT,
                   "a kernel read an invalid device-side input (a page ID outside [0, num_pages) or a "
@@ -1168,6 +1180,34 @@ rca_status noalloc_setup(void** scratch, int** status) {
   return RCA_OK;
 }
 
+// Only a device on which the entry point has been set up can hold a nonzero
+// word; on any other device the symbol is never touched, so this never makes
+// the driver load the module (and commit the scratch array) on its own.
+rca_status noalloc_take_status(int* out) {
+  *out = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 256) return RCA_OK;
+  int* p = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    p = g_noalloc_status_ptr[dev];
+  }
+  if (!p) return RCA_OK;
+  int h = 0;
+  e = cudaMemcpy(&h, p, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(allocation-free status word)");
+  if (h != 0) {
+    e = cudaMemset(p, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(allocation-free status word)");
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  }
+  *out = h;
+  return RCA_OK;
+}
+
 }  // namespace
 
 extern "C" rca_status rca_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* out,
@@ -1197,5 +1237,20 @@ extern "C" rca_status rca_attn_bwd_noalloc(const void* q, const void* k, const v
   RCA_CHECK(do_preprocess(out, lse, dout, B, Hq, T, Dh, dt, ws, L, st));
   RCA_CHECK(do_bwd_main(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, dt, ws, L, st, status));
   return do_convert(dq, B, Hq, T, Dh, dt, ws, L, st);
+  RCA_GUARD_END
+}
+
+// Failure-detection self-test of the allocation-free path: the same bounded
+// wait as rca_selftest_device_timeout, recording into the built-in status word.
+extern "C" rca_status rca_selftest_noalloc_timeout(void* cuda_stream) {
+  RCA_GUARD_BEGIN
+  g_err.clear();
+  void* ws = nullptr;
+  int* status = nullptr;
+  RCA_CHECK(noalloc_setup(&ws, &status));
+  rca::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(cuda_stream)>>>(status, g_timeout_ns.load());
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch selftest_wait_kernel");
+  return RCA_OK;
   RCA_GUARD_END
 }

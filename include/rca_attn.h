@@ -78,8 +78,8 @@ typedef enum {
 /* Storage dtype of q/k/v/out/dout/dq/dk/dv; selects the tensor-core operand type. */
 typedef enum { RCA_F32_TF32 = 0, RCA_BF16 = 1 } rca_dtype;
 
-/* ABI version: upper 16 bits major, lower 16 bits minor (0x00010006 = 1.6). */
-#define RCA_ABI_VERSION 0x00010006u
+/* ABI version: upper 16 bits major, lower 16 bits minor (0x00010007 = 1.7). */
+#define RCA_ABI_VERSION 0x00010007u
 uint32_t rca_abi_version(void);
 
 /* Message of the last failed call on this thread ("" if none). The pointer is
@@ -151,6 +151,12 @@ rca_status rca_attn_bwd_dq_convert(void* dq, int64_t B, int64_t Hq, int64_t Hkv,
  * that must never reach cudaMalloc, which can synchronise the device).
  *  - Sizes whose scratch (rca_attn_bwd_workspace_size) exceeds 40 MiB are
  *    rejected with RCA_ERR_INVALID_ARGUMENT before anything is launched.
+ *  - The array's 40 MiB are committed on a device when the driver loads this
+ *    library's device code there: at context creation with eager module
+ *    loading, or, with lazy loading (CUDA's default), at the first launch of
+ *    any kernel of this library on that device. A caller that must not see
+ *    that happen mid-loop makes one call at initialisation (any accepted size,
+ *    e.g. B = Hq = Hkv = T = 1, Dh = 16).
  *  - The first call on a device looks up the array's device address with that
  *    device current; make that first call before any stream capture.
  *  - All calls share the one array and it keeps the last call's contents (each
@@ -158,8 +164,8 @@ rca_status rca_attn_bwd_dq_convert(void* dq, int64_t B, int64_t Hq, int64_t Hkv,
  *    work overlaps on the GPU (other streams, other threads) race on it:
  *    serialise them.
  *  - A device-side timeout in these kernels is recorded in a status word of
- *    the built-in region, not in the one rca_stream_status reports; the
- *    kernels still end within the wait limit.
+ *    the built-in region; rca_stream_status() reports it (and clears it) like
+ *    the library's other status word. The kernels end within the wait limit.
  * Never calls cudaMalloc, cudaFree or any allocating routine.
  */
 rca_status rca_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* out,
@@ -340,7 +346,8 @@ rca_status rca_paged_decode(const void* q, const void* k_pool, const void* v_poo
  * Synchronises cuda_stream, then reports (and clears) an asynchronous CUDA
  * error, a device-side timeout (RCA_ERR_DEVICE_TIMEOUT) or an invalid
  * device-side input (RCA_ERR_DEVICE_INVALID_INPUT) recorded by a kernel of this
- * library on the current device. RCA_OK if none happened.
+ * library on the current device, the allocation-free backward's included.
+ * RCA_OK if none happened.
  */
 rca_status rca_stream_status(void* cuda_stream);
 
@@ -353,6 +360,14 @@ rca_status rca_stream_status(void* cuda_stream);
  * clears it); the CUDA context remains usable. Nothing faults or hangs.
  */
 rca_status rca_selftest_device_timeout(void* cuda_stream);
+
+/*
+ * The same self-test for the allocation-free backward's status word: the
+ * waiting kernel records its timeout where rca_attn_bwd_noalloc's kernels do,
+ * and the next rca_stream_status() returns RCA_ERR_DEVICE_TIMEOUT. Sets up the
+ * built-in region on the current device like a first rca_attn_bwd_noalloc call.
+ */
+rca_status rca_selftest_noalloc_timeout(void* cuda_stream);
 
 /*
  * Sets the device-side wait limit in nanoseconds for subsequent launches from

@@ -14,6 +14,71 @@ TOL = {
 }
 
 
+# Per-row bounds. A row is one query row of O / dQ, one key row of dK / dV
+# (Dh elements). Whole-tensor norms can hide a few wrong rows; every row is
+# therefore also held to ROW_FACTOR times the whole-tensor bound, relative to
+# max(||ref_row||, ROW_FLOOR * rms row norm of the tensor). The floor keeps
+# rows whose exact value is (near) zero, e.g. dQ of query 0, from turning
+# rounding noise into a large relative error. A stale, shifted, zeroed or
+# partly written row errs by O(1) and a single wrong element by about
+# 1/sqrt(Dh) of the row, so both stay far above these bounds, while rounding
+# (bf16 P and dS: 2^-9 per element) puts ordinary rows near the whole-tensor
+# error. LSE is checked elementwise: its rounding error is ~1e-6 (fp32 sums,
+# hardware exp2/log2), and any wrong row is off by far more than LSE_ABS.
+ROW_FACTOR = 5.0
+ROW_FLOOR = 0.1
+LSE_ABS = 1e-3
+
+
+def row_violations(got, ref, tol, floor=ROW_FLOOR):
+    """Rows (flattened index over all but the last axis) whose relative error
+    exceeds tol; returns (indices, worst relative error)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    d = got.shape[-1]
+    g2, r2 = got.reshape(-1, d), ref.reshape(-1, d)
+    err = np.linalg.norm(g2 - r2, axis=1)
+    rn = np.linalg.norm(r2, axis=1)
+    rms = float(np.sqrt(np.mean(rn * rn))) if rn.size else 0.0
+    den = np.maximum(rn, floor * rms)
+    den = np.where(den > 0, den, 1.0)
+    rel = err / den
+    return np.flatnonzero(rel > tol), float(rel.max()) if rel.size else 0.0
+
+
+def check_rows(label, got: dict, ref: dict, dt: str):
+    """Per-row checks of O, dQ, dK, dV and the elementwise LSE check; raises
+    AssertionError naming the first offending rows."""
+    tol = TOL[dt]
+    msgs = []
+    for n in ("O", "dQ", "dK", "dV"):
+        if n not in got:
+            continue
+        idx, worst = row_violations(got[n], ref[n], ROW_FACTOR * tol[n])
+        if idx.size:
+            shape = np.asarray(ref[n]).shape[:-1]
+            first = [tuple(int(c) for c in np.unravel_index(i, shape)) for i in idx[:4]]
+            msgs.append(f"{n}: {idx.size} rows above {ROW_FACTOR * tol[n]:.3g} (worst {worst:.3g}), e.g. {first}")
+    if "LSE" in got:
+        g, r = np.asarray(got["LSE"], dtype=np.float64), np.asarray(ref["LSE"], dtype=np.float64)
+        e = np.abs(g - r)
+        if not np.all(e <= LSE_ABS):
+            bad = np.argwhere(e > LSE_ABS)[:4].tolist()
+            msgs.append(f"LSE: max abs err {e.max():.3g} at e.g. {bad}")
+    assert not msgs, f"{label}: " + "; ".join(msgs)
+
+
+def worst_rows(got: dict, ref: dict) -> dict:
+    """Worst per-row relative error of each output (for reporting margins)."""
+    out = {}
+    for n in ("O", "dQ", "dK", "dV"):
+        if n in got:
+            out[n] = row_violations(got[n], ref[n], np.inf)[1]
+    if "LSE" in got:
+        out["LSE_abs"] = float(np.max(np.abs(np.asarray(got["LSE"], np.float64) - np.asarray(ref["LSE"], np.float64))))
+    return out
+
+
 def rel_fro(got, ref, den=None) -> float:
     """||got - ref||_F / ||ref||_F in fp64 (or / den when given)."""
     got = np.asarray(got, dtype=np.float64)
@@ -58,9 +123,9 @@ def group_slices(hq, hkv, b, kv):
     return slice(kv * g, kv * g + g)
 
 
-def compare_group(gpu: dict, q, k, v, do, b, kv):
-    """Oracle for one (batch, KV head) group vs the matching slices of GPU outputs.
-    Returns {name: rel_fro}."""
+def group_outputs(gpu: dict, q, k, v, do, b, kv):
+    """Oracle for one (batch, KV head) group and the matching slices of the GPU
+    outputs: (got, ref), dicts of fp64 arrays with the same shapes."""
     q64, k64, v64, do64 = (to64(x[b : b + 1]) for x in (q, k, v, do))
     ref = oracle.group_reference(q64, k64, v64, do64, 0, kv)
     hs = group_slices(q.shape[2], k.shape[2], b, kv)
@@ -71,4 +136,11 @@ def compare_group(gpu: dict, q, k, v, do, b, kv):
         "dK": to64(gpu["dK"][b, :, kv]),
         "dV": to64(gpu["dV"][b, :, kv]),
     }
+    return got, {n: np.asarray(ref[n], dtype=np.float64).reshape(got[n].shape) for n in got}
+
+
+def compare_group(gpu: dict, q, k, v, do, b, kv):
+    """Oracle for one (batch, KV head) group vs the matching slices of GPU outputs.
+    Returns {name: rel_fro}."""
+    got, ref = group_outputs(gpu, q, k, v, do, b, kv)
     return {n: rel_fro(got[n], ref[n]) for n in got}

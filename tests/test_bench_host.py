@@ -78,3 +78,37 @@ def test_oracle_sample_is_bounded_and_counts_whole_groups():
     per_group = 3.5 * 4.0 * TINY.group * TINY.T * TINY.T * TINY.Dh / 2.0
     assert 1 <= groups <= 2 and threads >= 1 and secs >= 0
     assert flops == groups * per_group
+
+
+def test_step_spread_percentiles():
+    s = bench.spread([float(x) for x in range(1, 12)])  # 1 .. 11
+    assert s["mean"] == pytest.approx(6.0) and s["median"] == pytest.approx(6.0)
+    assert s["p10"] == pytest.approx(2.0) and s["p90"] == pytest.approx(10.0)
+
+
+def test_nominal_peak_arithmetic():
+    # 152 SMs x 8192 bf16 FLOP per clock x 2070 MHz; TF32 at half the rate
+    assert bench.nominal_tflops(152, 2070.0, "bf16") == pytest.approx(152 * 8192 * 2.07e9 / 1e12)
+    assert bench.nominal_tflops(152, 2070.0, "fp32") == pytest.approx(bench.nominal_tflops(152, 2070.0, "bf16") / 2)
+
+
+def test_both_arms_print_the_same_config(capsys):
+    cfg = bench.config_for(HEADLINE, 1)
+    nsets, set_bytes = bench.input_sets(HEADLINE)
+    assert set_bytes == 2 * 4 * 2048 * 64 * (2 * 16 + 2 * 16)
+    assert nsets * set_bytes > 2 * bench.L2_BYTES
+    assert cfg["workload"] == HEADLINE.describe() and cfg["global_batch"] == 4 and str(nsets) in cfg["l2"]
+
+    class A:
+        steps, warmup = 1, 0
+        metric = "m"
+
+    assert bench.run_reference(A, TINY, 1, 0) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["config"] == bench.config_for(TINY, 1)
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_launch_count_per_step():
+    assert bench.launches_per_step(HEADLINE) == 4
+    assert bench.launches_per_step(TINY) == 8

@@ -1,9 +1,14 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
 
 Small shapes are compared over whole tensors (several tiles, ragged tails, every
-head width, GQA). The five specified workloads run at full size in the same
-launch configuration the benchmark times, and are compared on sampled
-(batch, KV head) groups, every element of which the oracle computes exactly.
+head width, GQA). Mid-size shapes have more work items than the GPU has SMs, so
+every persistent CTA walks two or more items (the cross-item prefetch, the
+per-item barrier parities and the hand-over of the TMEM accumulators all run);
+they are compared over whole tensors too. The five specified workloads run at
+full size in the same launch configuration the benchmark times, and are
+compared on sampled (batch, KV head) groups, every element of which the oracle
+computes exactly. Besides the whole-tensor relative Frobenius bounds, every row
+of every compared output is held to a per-row bound (tests/parity.py).
 """
 
 import zlib
@@ -14,7 +19,8 @@ import torch
 
 import causal_head_attention_gb300 as rca
 from causal_head_attention_gb300.inputs import WORKLOADS, make_inputs, small
-from tests.parity import TOL, compare_group, full_reference, rel_fro, to64, uncancelled_norms
+from tests.parity import (TOL, check_rows, full_reference, group_outputs, rel_fro, to64,
+                          uncancelled_norms, worst_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -61,6 +67,38 @@ def test_small_full_tensor(case):
     tol = TOL[dt]
     bad = {n: e for n, e in errs.items() if not e <= tol[n]}
     assert not bad, f"{name}: {errs}"
+    check_rows(name, {n: to64(gpu[n]) for n in ref}, ref, dt)
+
+
+# Shapes with more work items than SMs (152 on GB300): forward items are
+# (b, h, 128-row query tile), backward items (b, KV head, 128-key tile).
+MULTI = [
+    # name, B, Hq, Hkv, T, Dh, dtype            fwd items / bwd items
+    ("bf16_dh64_persistent", 2, 16, 16, 1024, 64, "bf16"),    # 256 / 256
+    ("bf16_dh64_gqa_ragged", 5, 8, 4, 1100, 64, "bf16"),      # 360 / 180, T % 128 = 76
+    ("bf16_dh32_persistent", 2, 8, 8, 1300, 32, "bf16"),      # 176 / 176, T % 128 = 20
+    ("bf16_dh16_persistent", 3, 8, 2, 1030, 16, "bf16"),      # 216 / 54 (backward: one round)
+    ("bf16_dh128_gqa", 2, 8, 4, 2560, 128, "bf16"),           # 320 / 160
+    ("fp32_dh64", 2, 12, 12, 1024, 64, "fp32"),               # 192 / 192
+]
+
+
+@pytest.mark.parametrize("case", MULTI, ids=[c[0] for c in MULTI])
+def test_multi_item_full_tensor(case):
+    name, B, Hq, Hkv, T, Dh, dt = case
+    n_t = (T + 127) // 128
+    assert B * Hq * n_t > 152, "the forward needs more items than SMs"
+    w = small(name, B, Hq, Hkv, T, Dh, dt, seed=zlib.crc32(name.encode()) % 1000)
+    q, k, v, do = make_inputs(w)
+    gpu = run_gpu(q, k, v, do)
+    ref = full_reference(q, k, v, do)
+    got = {n: to64(gpu[n]) for n in ref}
+    errs = {n: rel_fro(got[n], ref[n]) for n in ref}
+    print(f"{name}: whole-tensor {errs}; worst rows {worst_rows(got, ref)}")
+    tol = TOL[dt]
+    bad = {n: e for n, e in errs.items() if not e <= tol[n]}
+    assert not bad, f"{name}: {errs}"
+    check_rows(name, got, ref, dt)
 
 
 def _samples(w):
@@ -77,9 +115,12 @@ def test_workload_sampled_groups(w):
         assert torch.isfinite(gpu[name].float()).all(), f"{w.name}: non-finite {name}"
     tol = TOL[w.dtype]
     for b, kv in _samples(w):
-        errs = compare_group(gpu, q, k, v, do, b, kv)
+        got, ref = group_outputs(gpu, q, k, v, do, b, kv)
+        errs = {n: rel_fro(got[n], ref[n]) for n in got}
+        print(f"{w.name} group (b={b}, kv={kv}): whole {errs}; worst rows {worst_rows(got, ref)}")
         bad = {n: e for n, e in errs.items() if not e <= tol[n]}
         assert not bad, f"{w.name} group (b={b}, kv={kv}): {errs}"
+        check_rows(f"{w.name} group (b={b}, kv={kv})", got, ref, w.dtype)
 
 
 def test_autograd_wrapper_matches_oracle():
