@@ -162,8 +162,13 @@ def attention_forward(q, k, v, scale: float | None = None):
     return o, lse
 
 
-def attention_backward(q, k, v, do, scale: float | None = None):
-    """Whole tensors. Returns (dQ, dK, dV) in fp64; dK/dV sum over each KV group."""
+def attention_backward(q, k, v, do, scale: float | None = None, o=None):
+    """Whole tensors. Returns (dQ, dK, dV) in fp64; dK/dV sum over each KV group.
+
+    o: the forward output the backward is handed ([B,T,Hq,Dh]), from which
+    D = rowsum(dO * O) is formed, as a backward that takes the stored output
+    as an argument does. None: the oracle's own exact forward output, which
+    gives the exact VJP (the two agree when o is that output)."""
     b, t, hq, hkv, dh = _check_shapes(q, k, v)
     scale = default_scale(dh) if scale is None else scale
     g = hq // hkv
@@ -175,6 +180,8 @@ def attention_backward(q, k, v, do, scale: float | None = None):
             kv = h // g
             qh, kh, vh = q[bi, :, h], k[bi, :, kv], v[bi, :, kv]
             oh, _, p = head_forward(qh, kh, vh, scale)
+            if o is not None:
+                oh = np.asarray(o[bi, :, h], dtype=np.float64)
             dqh, dkh, dvh, _ = head_backward(qh, kh, vh, oh, do[bi, :, h], p, scale)
             dq[bi, :, h] = dqh
             dk[bi, :, kv] += dkh
@@ -182,13 +189,15 @@ def attention_backward(q, k, v, do, scale: float | None = None):
     return dq, dk, dv
 
 
-def group_reference(q, k, v, do, b: int, kv: int, scale: float | None = None):
+def group_reference(q, k, v, do, b: int, kv: int, scale: float | None = None, o=None):
     """Forward and backward for one (batch, KV head) group: its g query heads.
 
     This is how full-size workloads are checked on a sample: every output of the
     sampled group is computed exactly, element by element comparable.
     Returns a dict with O [T,g,Dh], LSE [g,T], D [g,T], dQ [T,g,Dh],
-    dK [T,Dh], dV [T,Dh], all fp64.
+    dK [T,Dh], dV [T,Dh], all fp64. When o ([B,T,Hq,Dh], the output a backward
+    is handed) is given, the dict also holds "given_o": the backward's dQ, dK,
+    dV and D with D = rowsum(dO * o) instead of the exact output.
     """
     _, t, hq, hkv, dh = _check_shapes(q, k, v)
     scale = default_scale(dh) if scale is None else scale
@@ -203,6 +212,9 @@ def group_reference(q, k, v, do, b: int, kv: int, scale: float | None = None):
         "dK": np.zeros((t, dh)),
         "dV": np.zeros((t, dh)),
     }
+    if o is not None:
+        out["given_o"] = {"D": np.empty((g, t)), "dQ": np.empty((t, g, dh)), "dK": np.zeros((t, dh)),
+                          "dV": np.zeros((t, dh))}
     for r in range(g):
         h = kv * g + r
         qh = np.asarray(q[b, :, h], dtype=np.float64)
@@ -214,4 +226,12 @@ def group_reference(q, k, v, do, b: int, kv: int, scale: float | None = None):
         out["dQ"][:, r] = dqh
         out["dK"] += dkh
         out["dV"] += dvh
+        if o is not None:
+            go = out["given_o"]
+            dqh, dkh, dvh, d = head_backward(qh, kh, vh, np.asarray(o[b, :, h], dtype=np.float64), do[b, :, h],
+                                             p, scale)
+            go["D"][r] = d
+            go["dQ"][:, r] = dqh
+            go["dK"] += dkh
+            go["dV"] += dvh
     return out

@@ -312,6 +312,42 @@ def test_group_reference_matches_whole_tensor():
             assert np.allclose(r["dV"], dv[b, :, kv], atol=1e-14)
 
 
+def test_backward_of_a_given_output():
+    """The backward handed an output o reads it only through D = rowsum(dO * o).
+    With the exact output it is the exact VJP; with o = O + E every row's D
+    moves by delta_i = sum_d dO[i,d] E[i,d], so dS loses P[i,j] delta_i: dQ
+    moves by -scale * delta_i * (P K)_i, dK by -scale * sum_i P[i,j] delta_i
+    Q_i, and dV not at all."""
+    q, k, v, do = rand_qkv(2, 17, 4, 2, 8, seed=16)
+    o, _ = oracle.attention_forward(q, k, v)
+    dq, dk, dv = oracle.attention_backward(q, k, v, do)
+    same = oracle.attention_backward(q, k, v, do, o=o)
+    for a, b in zip(same, (dq, dk, dv)):
+        assert np.allclose(a, b, atol=1e-14)
+    e = np.random.default_rng(17).standard_normal(o.shape) * 1e-2
+    dq2, dk2, dv2 = oracle.attention_backward(q, k, v, do, o=o + e)
+    sc = oracle.default_scale(8)
+    assert np.allclose(dv2, dv, atol=1e-14)
+    for b in range(2):
+        for h in range(4):
+            kv = h // 2
+            _, _, p = oa.head_forward(q[b, :, h], k[b, :, kv], v[b, :, kv], sc)
+            delta = np.sum(do[b, :, h] * e[b, :, h], axis=1)
+            assert np.allclose(dq2[b, :, h] - dq[b, :, h], -sc * delta[:, None] * (p @ k[b, :, kv]), atol=1e-12)
+    for b in range(2):
+        for kv in range(2):
+            want = np.zeros((17, 8))
+            for h in (2 * kv, 2 * kv + 1):
+                _, _, p = oa.head_forward(q[b, :, h], k[b, :, kv], v[b, :, kv], sc)
+                delta = np.sum(do[b, :, h] * e[b, :, h], axis=1)
+                want += -sc * (p * delta[:, None]).T @ q[b, :, h]
+            assert np.allclose(dk2[b, :, kv] - dk[b, :, kv], want, atol=1e-12)
+    r = oracle.group_reference(q, k, v, do, 1, 1, o=o + e)
+    assert np.allclose(r["given_o"]["dQ"], dq2[1, :, 2:4], atol=1e-14)
+    assert np.allclose(r["given_o"]["dK"], dk2[1, :, 1], atol=1e-14)
+    assert np.allclose(r["dQ"], dq[1, :, 2:4], atol=1e-14)
+
+
 def test_gqa_divisibility_rejected():
     q, k, v, _ = rand_qkv(1, 4, 3, 2, 4, seed=15)
     with pytest.raises(ValueError):
