@@ -704,7 +704,12 @@ def bench_materialized(w, dev, stream, steps, warmup, P):
     full = E * T * T * 4
     sm_bytes = tri + full + E * T * 4       # read the kept entries, write whole rows and LSE
     smb_bytes = 2 * tri + full              # read P and dP where kept, write whole rows
-    gemm_flops = 2.0 * E * T * T * w.Dh * (2 + 4)  # full-square products: 2 forward, 4 backward
+    # The products over the kept triangle: 2 forward (S, O), 4 backward (dP, dQ, dK, dV),
+    # each 2 * Dh FLOPs per kept score; each streams one [T, T] triangle once (S and
+    # dP written, P or dS read), the [B,T,H,Dh] operands being small beside it.
+    prod_flops = 2.0 * w.Dh * (E * T * (T + 1) / 2) * (2 + 4)
+    prod_bytes = 6 * tri
+    prod_ms = (fwd_ms - sm_ms) + (bwd_ms - smb_ms)
 
     def roof(nbytes, ms):
         a = nbytes / (ms * 1e-3) / 1e9
@@ -714,12 +719,14 @@ def bench_materialized(w, dev, stream, steps, warmup, P):
     return {
         "workload": w.describe(), "name": w.name, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
         "probs_bytes": full,
-        "gemm_tflops_incl_softmax": gemm_flops / ((fwd_ms + bwd_ms) * 1e-3) / 1e12,
+        "products": {"ms": prod_ms, "tflops": prod_flops / (prod_ms * 1e-3) / 1e12,
+                     "gbs": prod_bytes / (prod_ms * 1e-3) / 1e9, "frac_hbm": prod_bytes / (prod_ms * 1e-3) / 1e9
+                     / P["hbm_gbs"], "bytes": prod_bytes,
+                     "how": "fwd + bwd call time minus the two softmax kernels timed alone"},
         "causal_softmax": roof(sm_bytes, sm_ms), "causal_softmax_bwd": roof(smb_bytes, smb_ms),
-        "note": "GEMMs in cuBLAS (full T x T squares, masked half included); the softmax kernels are this library's",
-        "gpu_launches": {"own_kernels_per_fwd": 4 if w.dtype == "bf16" else 2,
-                         "own_kernels_per_bwd": 8 if w.dtype == "bf16" else 4,
-                         "cublas_gemms_per_fwd": 2, "cublas_gemms_per_bwd": 4},
+        "note": "all kernels are this library's: tensor-core products over the kept triangle of tiles only, "
+                "the fused causal softmax and its VJP",
+        "gpu_launches": {"per_fwd": 3 if w.dtype == "bf16" else 6, "per_bwd": 5 if w.dtype == "bf16" else 9},
     }
 
 

@@ -61,7 +61,7 @@ def build(force: bool = False, verbose: bool = False, extra: tuple = ()) -> str:
     for r in results:
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed ({r.returncode}):\n{r.stdout}\n{r.stderr}")
-    r = _run([nvcc, ARCH, "-shared", "-o", LIB + ".tmp", *objs, "-lcublas"], verbose)
+    r = _run([nvcc, ARCH, "-shared", "-o", LIB + ".tmp", *objs], verbose)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed ({r.returncode}):\n{r.stdout}\n{r.stderr}")
     os.replace(LIB + ".tmp", LIB)

@@ -12,24 +12,22 @@
 //             dS = scale * P * (dP - rowsum(P * dP));  dQ = dS K;
 //             dK = dS^T Q;  dV = P^T dO  (dK, dV summed over the group)
 //
-// The five products are plain batched GEMMs and run in cuBLAS, one batch
-// entry per (b, h) with pointer arrays built on the device: the two that
-// contract over Dh (Q K^T, dO V^T) read the stored operands directly (bf16
-// tensor cores with fp32 accumulation, or fp32), the three that contract over
-// the T positions take fp32 P or dS and run in full fp32. The fused causal
-// softmax and its VJP are the kernels written here (one warp per row, bound by
-// HBM traffic of the [T, T] rows), with small conversion and group-sum
-// kernels around the GEMMs. The full T x T rows are computed (the masked half
-// included): this path exists for the probabilities and as an independent
-// check of the memory-linear kernels, not for speed.
-#include <cublas_v2.h>
+// The five products are this library's tensor-core kernels (mat_gemm.cuh),
+// computed over the causal triangle only: score tiles above the diagonal are
+// never formed, and the products over T read only the kept triangle of P or
+// dS. The fused causal softmax and its VJP are the kernels below (one warp per
+// row, bound by HBM traffic of the [T, T] rows). fp32 storage: Q, K, V and dO
+// are first split into three bf16 parts each (split3_kernel), so that the
+// scores keep fp32 accuracy.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <cstdio>
 #include <mutex>
 
+#include "mat_gemm.cuh"
 #include "materialized.h"
 #include "tc.cuh"
 
@@ -40,79 +38,24 @@ constexpr unsigned FULL = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 
-// Pointer arrays of the batched GEMMs: entry e = b * Hq + h of array a is
-// base[a] + b * bstride[a] + (h, or its KV head) * hstride[a] bytes.
-enum Arr { A_Q, A_K, A_V, A_DO, A_QF, A_KF, A_VF, A_DOF, A_P, A_DP, A_OF, A_DQF, A_DKH, A_DVH, NARR };
-struct PtrBuild {
-  const char* base[NARR];
-  int64_t bstride[NARR];
-  int64_t hstride[NARR];
-  int kv[NARR];
-};
-
-__global__ void build_ptrs_kernel(PtrBuild pb, void** out, int E, int Hq, int g) {
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= E) return;
-  const int b = e / Hq, h = e - b * Hq;
-  for (int a = 0; a < NARR; ++a) {
-    const int hh = pb.kv[a] ? h / g : h;
-    out[int64_t(a) * E + e] =
-        pb.base[a] ? const_cast<char*>(pb.base[a] + b * pb.bstride[a] + hh * pb.hstride[a]) : nullptr;
-  }
-}
-
-// bf16 -> fp32, 8 elements a thread (n is a multiple of 8).
-__global__ void to_f32_kernel(const __nv_bfloat16* __restrict__ src, float* __restrict__ dst, int64_t n8) {
-  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n8; i += int64_t(gridDim.x) * blockDim.x) {
-    const uint4 w = reinterpret_cast<const uint4*>(src)[i];
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-    float4 lo, hi;
-    lo.x = __uint_as_float(u[0] << 16); lo.y = __uint_as_float(u[0] & 0xffff0000u);
-    lo.z = __uint_as_float(u[1] << 16); lo.w = __uint_as_float(u[1] & 0xffff0000u);
-    hi.x = __uint_as_float(u[2] << 16); hi.y = __uint_as_float(u[2] & 0xffff0000u);
-    hi.z = __uint_as_float(u[3] << 16); hi.w = __uint_as_float(u[3] & 0xffff0000u);
-    reinterpret_cast<float4*>(dst)[2 * i] = lo;
-    reinterpret_cast<float4*>(dst)[2 * i + 1] = hi;
-  }
-}
-
-// fp32 -> bf16 (round to nearest even), 4 elements a thread (n a multiple of 4).
-__global__ void to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst, int64_t n4) {
+// fp32 -> three bf16 parts x = x0 + x1 + x2 (x0 = bf16(x), x1 = bf16(x - x0),
+// x2 = bf16(x - x0 - x1); both differences are exact in fp32), 4 elements a
+// thread; n is a multiple of 4.
+__global__ void split3_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ p0,
+                              __nv_bfloat16* __restrict__ p1, __nv_bfloat16* __restrict__ p2, int64_t n4) {
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n4; i += int64_t(gridDim.x) * blockDim.x) {
     const float4 f = reinterpret_cast<const float4*>(src)[i];
-    uint2 w;
-    w.x = pack_bf16(f.x, f.y);
-    w.y = pack_bf16(f.z, f.w);
-    reinterpret_cast<uint2*>(dst)[i] = w;
-  }
-}
-
-// dst[b, t, kv, d] = sum over the g query heads of the group of src[b, h, t, d]
-// (src per query head [B, Hq, T, Dh] fp32; dst in the storage dtype).
-template <bool BF16>
-__global__ void group_sum_kernel(const float* __restrict__ src, void* __restrict__ dst, int B, int T, int Hq,
-                                 int Hkv, int Dh) {
-  const int g = Hq / Hkv;
-  const int64_t n4 = int64_t(B) * T * Hkv * Dh / 4;
-  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n4; i += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t o = i * 4;  // element index in [B, T, Hkv, Dh]
-    const int d = int(o % Dh);
-    const int kv = int((o / Dh) % Hkv);
-    const int64_t bt = o / (int64_t(Dh) * Hkv);
-    const int t = int(bt % T), b = int(bt / T);
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int r = 0; r < g; ++r) {
-      const float4 x = *reinterpret_cast<const float4*>(src + ((int64_t(b) * Hq + kv * g + r) * T + t) * Dh + d);
-      s.x += x.x; s.y += x.y; s.z += x.z; s.w += x.w;
-    }
-    if constexpr (BF16) {
-      uint2 w;
-      w.x = pack_bf16(s.x, s.y);
-      w.y = pack_bf16(s.z, s.w);
-      reinterpret_cast<uint2*>(dst)[i] = w;
-    } else {
-      reinterpret_cast<float4*>(dst)[i] = s;
-    }
+    uint32_t h01, l01, h23, l23;
+    split_bf16x2(f.x, f.y, h01, l01);
+    split_bf16x2(f.z, f.w, h23, l23);
+    // residuals after the first two parts
+    const float r0 = f.x - __uint_as_float(h01 << 16) - __uint_as_float(l01 << 16);
+    const float r1 = f.y - __uint_as_float(h01 & 0xffff0000u) - __uint_as_float(l01 & 0xffff0000u);
+    const float r2 = f.z - __uint_as_float(h23 << 16) - __uint_as_float(l23 << 16);
+    const float r3 = f.w - __uint_as_float(h23 & 0xffff0000u) - __uint_as_float(l23 & 0xffff0000u);
+    reinterpret_cast<uint2*>(p0)[i] = make_uint2(h01, h23);
+    reinterpret_cast<uint2*>(p1)[i] = make_uint2(l01, l23);
+    reinterpret_cast<uint2*>(p2)[i] = make_uint2(pack_bf16(r0, r1), pack_bf16(r2, r3));
   }
 }
 
@@ -239,38 +182,30 @@ __global__ void causal_softmax_bwd_kernel(const float* __restrict__ p, float* __
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// [dP (backward) | fp32 storage: three bf16 parts each of Q, K, V, dO]
 struct Layout {
-  size_t ptrs, qf, kf, vf, dof, of, dp, dqf, dkh, dvh, total;
+  size_t dp, parts[4][3], total;
 };
+enum { P_Q = 0, P_K = 1, P_V = 2, P_DO = 3 };
 
-// [ptr arrays | Qf Kf Vf dOf Of (bf16 only) | dP | dQf (bf16 only) | dKh | dVh]
 Layout layout(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, bool bf16) {
   Layout L{};
   const size_t E = size_t(B) * Hq;
   const size_t nq = size_t(B) * T * Hq * Dh, nkv = size_t(B) * T * Hkv * Dh;
   size_t at = 0;
-  L.ptrs = at;
-  at += round256(NARR * E * sizeof(void*));
-  auto take = [&](size_t bytes) {
-    const size_t o = at;
-    at += round256(bytes);
-    return o;
-  };
-  L.qf = bf16 ? take(nq * 4) : 0;
-  L.kf = bf16 ? take(nkv * 4) : 0;
-  L.vf = bf16 ? take(nkv * 4) : 0;
-  L.dof = bf16 ? take(nq * 4) : 0;
-  L.of = bf16 ? take(nq * 4) : 0;
-  L.dp = take(E * size_t(T) * T * 4);
-  L.dqf = bf16 ? take(nq * 4) : 0;
-  L.dkh = take(E * size_t(T) * Dh * 4);
-  L.dvh = take(E * size_t(T) * Dh * 4);
+  L.dp = at;
+  at += round256(E * size_t(T) * T * 4);
+  if (!bf16) {
+    const size_t n[4] = {nq, nkv, nkv, nq};
+    for (int t = 0; t < 4; ++t)
+      for (int p = 0; p < 3; ++p) {
+        L.parts[t][p] = at;
+        at += round256(n[t] * 2);
+      }
+  }
   L.total = at;
   return L;
 }
-
-std::mutex g_cublas_mu;
-cublasHandle_t g_cublas[256] = {};
 
 bool cuda_ok(cudaError_t e, const char* what, std::string& err) {
   if (e == cudaSuccess) return true;
@@ -278,27 +213,43 @@ bool cuda_ok(cudaError_t e, const char* what, std::string& err) {
   return false;
 }
 
-bool cublas_ok(cublasStatus_t s, const char* what, std::string& err) {
-  if (s == CUBLAS_STATUS_SUCCESS) return true;
-  char buf[160];
-  snprintf(buf, sizeof(buf), "%s: cuBLAS status %d", what, int(s));
-  err = buf;
-  return false;
+int grid_for(int64_t work, int per_block) {
+  const int64_t g = (work + per_block - 1) / per_block;
+  return int(g < 1 ? 1 : (g > 65535 * 8 ? 65535 * 8 : g));
 }
 
-// One cuBLAS handle per device, used under g_cublas_mu (the stream is set per call).
-bool handle_for_device(cublasHandle_t* h, std::string& err) {
+int g_sms[256] = {};
+std::mutex g_mu;
+
+bool sm_count(int* out, std::string& err) {
   int dev = 0;
   if (!cuda_ok(cudaGetDevice(&dev), "cudaGetDevice", err)) return false;
   if (dev < 0 || dev >= 256) {
     err = "device ordinal out of range";
     return false;
   }
-  if (!g_cublas[dev]) {
-    if (!cublas_ok(cublasCreate(&g_cublas[dev]), "cublasCreate", err)) return false;
-    if (!cublas_ok(cublasSetMathMode(g_cublas[dev], CUBLAS_DEFAULT_MATH), "cublasSetMathMode", err)) return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_sms[dev] <= 0) {
+    int n = 0;
+    if (!cuda_ok(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute", err))
+      return false;
+    g_sms[dev] = n;
   }
-  *h = g_cublas[dev];
+  *out = g_sms[dev];
+  return true;
+}
+
+// Opt a kernel into its dynamic shared memory once per device.
+template <typename K>
+bool ensure_smem(K kernel, int bytes, std::atomic<unsigned long long>& mask, std::string& err) {
+  int dev = 0;
+  if (!cuda_ok(cudaGetDevice(&dev), "cudaGetDevice", err)) return false;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (mask.load(std::memory_order_acquire) & bit) return true;
+  if (!cuda_ok(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
+               "cudaFuncSetAttribute(materialized)", err))
+    return false;
+  mask.fetch_or(bit, std::memory_order_acq_rel);
   return true;
 }
 
@@ -306,68 +257,111 @@ struct Ctx {
   const MatParams& p;
   cudaStream_t st;
   Layout L;
-  int E, g, T, Dh;
-  void** arr;  // device pointer arrays, NARR x E
-  cudaDataType_t st_type;
-  size_t es;
+  int E, g, T, Dh, DHP;
+  char* ws;
 };
 
-void** arr_of(const Ctx& c, Arr a) { return c.arr + size_t(a) * c.E; }
+const void* part(const Ctx& c, int t, int k) { return c.ws + c.L.parts[t][k]; }
 
-// Row-major X[r][c] with leading dimension ld is the column-major X^T: every
-// product below is written for the column-major views.
-bool gemm(cublasHandle_t h, const Ctx& c, cublasOperation_t ta, cublasOperation_t tb, int m, int n, int k,
-          float alpha, Arr a, cudaDataType_t at, int lda, Arr b, cudaDataType_t bt, int ldb, Arr cc, int ldc,
-          const char* what, std::string& err) {
-  const float beta = 0.f;
-  return cublas_ok(cublasGemmBatchedEx(h, ta, tb, m, n, k, &alpha, const_cast<const void* const*>(arr_of(c, a)),
-                                       at, lda, const_cast<const void* const*>(arr_of(c, b)), bt, ldb, &beta,
-                                       arr_of(c, cc), CUDA_R_32F, ldc, c.E, CUBLAS_COMPUTE_32F,
-                                       CUBLAS_GEMM_DEFAULT),
-                   what, err);
+bool split3(const Ctx& c, const void* src, int t, int64_t n, std::string& err) {
+  split3_kernel<<<grid_for(n / 4, 256), 256, 0, c.st>>>(
+      static_cast<const float*>(src), reinterpret_cast<__nv_bfloat16*>(c.ws + c.L.parts[t][0]),
+      reinterpret_cast<__nv_bfloat16*>(c.ws + c.L.parts[t][1]), reinterpret_cast<__nv_bfloat16*>(c.ws + c.L.parts[t][2]),
+      n / 4);
+  return cuda_ok(cudaGetLastError(), "launch split3_kernel", err);
 }
 
-int grid_for(int64_t work, int per_block) {
-  const int64_t g = (work + per_block - 1) / per_block;
-  return int(g < 1 ? 1 : (g > 65535 * 8 ? 65535 * 8 : g));
-}
-
-bool build(Ctx& c, std::string& err) {
+// out[e] (tiles j <= i) = A_e B_e^T: a (tensor ia, query heads) against b
+// (tensor ib, KV heads); bf16 storage reads the tensors themselves, fp32
+// storage their three bf16 parts.
+template <int NP, int DHP>
+bool launch_scores(const Ctx& c, const void* a_src, int ia, const void* b_src, int ib, float* out, int* status,
+                   unsigned long long timeout_ns, std::string& err) {
+  using C = ScoresCfg<NP, DHP>;
   const MatParams& p = c.p;
-  char* ws = static_cast<char*>(p.workspace);
-  const int64_t es = int64_t(c.es);
-  const int64_t Hq = p.Hq, Hkv = p.Hkv, T = p.T, Dh = p.Dh;
-  PtrBuild pb{};
-  auto set = [&](Arr a, const void* base, int64_t bstride, int64_t hstride, bool kv) {
-    pb.base[a] = static_cast<const char*>(base);
-    pb.bstride[a] = bstride;
-    pb.hstride[a] = hstride;
-    pb.kv[a] = kv ? 1 : 0;
-  };
-  const int64_t qb = T * Hq * Dh, kb = T * Hkv * Dh;  // elements per batch index
-  set(A_Q, p.q, qb * es, Dh * es, false);
-  set(A_K, p.k, kb * es, Dh * es, true);
-  set(A_V, p.v, kb * es, Dh * es, true);
-  set(A_DO, p.dout, qb * es, Dh * es, false);
-  // fp32 operands: copies for bf16 storage, the caller's tensors for fp32.
-  set(A_QF, p.bf16 ? ws + c.L.qf : p.q, qb * 4, Dh * 4, false);
-  set(A_KF, p.bf16 ? ws + c.L.kf : p.k, kb * 4, Dh * 4, true);
-  set(A_VF, p.bf16 ? ws + c.L.vf : p.v, kb * 4, Dh * 4, true);
-  set(A_DOF, p.bf16 ? ws + c.L.dof : p.dout, qb * 4, Dh * 4, false);
-  set(A_P, p.probs, Hq * T * T * 4, T * T * 4, false);
-  set(A_DP, ws + c.L.dp, Hq * T * T * 4, T * T * 4, false);
-  set(A_OF, p.bf16 ? ws + c.L.of : p.out, qb * 4, Dh * 4, false);
-  set(A_DQF, p.bf16 ? ws + c.L.dqf : p.dq, qb * 4, Dh * 4, false);
-  set(A_DKH, ws + c.L.dkh, Hq * T * Dh * 4, T * Dh * 4, false);
-  set(A_DVH, ws + c.L.dvh, Hq * T * Dh * 4, T * Dh * 4, false);
-  build_ptrs_kernel<<<(c.E + 127) / 128, 128, 0, c.st>>>(pb, c.arr, c.E, int(Hq), c.g);
-  return cuda_ok(cudaGetLastError(), "launch build_ptrs_kernel", err);
+  ScoresMaps maps{};
+  for (int k = 0; k < NP; ++k) {
+    const void* av = NP == 1 ? a_src : part(c, ia, k);
+    const void* bv = NP == 1 ? b_src : part(c, ib, k);
+    if (!encode_rows_map(&maps.a[k], av, p.B, p.T, p.Hq, p.Dh, 128, err)) return false;
+    if (!encode_rows_map(&maps.b[k], bv, p.B, p.T, p.Hkv, p.Dh, 128, err)) return false;
+  }
+  ScoresArgs a{};
+  a.out = out;
+  a.status = status;
+  a.timeout_ns = timeout_ns;
+  a.B = int(p.B); a.Hq = int(p.Hq); a.Hkv = int(p.Hkv); a.T = int(p.T);
+  a.group = c.g;
+  a.n_t = int((p.T + 127) / 128);
+  a.n_tri = (long long)a.n_t * (a.n_t + 1) / 2;
+  a.n_items = a.n_tri * c.E;
+  int sms = 0;
+  if (!sm_count(&sms, err)) return false;
+  const unsigned grid = unsigned(a.n_items < sms ? a.n_items : sms);
+  static std::atomic<unsigned long long> set[2] = {};
+  if (p.T % 4 == 0) {
+    auto k = mat_scores_kernel<NP, DHP, true>;
+    if (!ensure_smem(k, C::SMEM_BYTES, set[0], err)) return false;
+    k<<<grid, C::NTHREADS, C::SMEM_BYTES, c.st>>>(maps, a);
+  } else {
+    auto k = mat_scores_kernel<NP, DHP, false>;
+    if (!ensure_smem(k, C::SMEM_BYTES, set[1], err)) return false;
+    k<<<grid, C::NTHREADS, C::SMEM_BYTES, c.st>>>(maps, a);
+  }
+  return cuda_ok(cudaGetLastError(), "launch mat_scores_kernel", err);
 }
 
-bool convert(const void* src, size_t off, int64_t n, const Ctx& c, std::string& err) {
-  float* dst = reinterpret_cast<float*>(static_cast<char*>(c.p.workspace) + off);
-  to_f32_kernel<<<grid_for(n / 8, 256), 256, 0, c.st>>>(static_cast<const __nv_bfloat16*>(src), dst, n / 8);
-  return cuda_ok(cudaGetLastError(), "launch to_f32_kernel", err);
+// out = X Y over the kept triangle (rows) or X^T Y summed over each group
+// (columns); Y is tensor iy (KV heads for rows, query heads for columns).
+template <bool TRANS, int NPY, int DHP>
+bool launch_reduce(const Ctx& c, const float* x, const void* y_src, int iy, void* out, int* status,
+                   unsigned long long timeout_ns, std::string& err) {
+  using C = ReduceCfg<TRANS, NPY, DHP>;
+  const MatParams& p = c.p;
+  ReduceMaps maps{};
+  const int64_t H = TRANS ? p.Hq : p.Hkv;
+  for (int k = 0; k < NPY; ++k) {
+    const void* yv = NPY == 1 ? y_src : part(c, iy, k);
+    if (!encode_rows_map(&maps.y[k], yv, p.B, p.T, H, p.Dh, 64, err)) return false;
+  }
+  if (NPY == 1) maps.y[1] = maps.y[0];
+  ReduceArgs a{};
+  a.x = x;
+  a.out = out;
+  a.status = status;
+  a.timeout_ns = timeout_ns;
+  a.B = int(p.B); a.Hq = int(p.Hq); a.Hkv = int(p.Hkv); a.T = int(p.T); a.Dh = int(p.Dh);
+  a.group = c.g;
+  a.n_t = int((p.T + 127) / 128);
+  a.n_items = int((TRANS ? p.B * p.Hkv : p.B * p.Hq) * a.n_t);
+  a.out_f32 = p.bf16 ? 0 : 1;
+  int sms = 0;
+  if (!sm_count(&sms, err)) return false;
+  const unsigned grid = unsigned(a.n_items < sms ? a.n_items : sms);
+  static std::atomic<unsigned long long> set = {};
+  auto k = mat_reduce_kernel<TRANS, NPY, DHP>;
+  if (!ensure_smem(k, C::SMEM_BYTES, set, err)) return false;
+  k<<<grid, C::NTHREADS, C::SMEM_BYTES, c.st>>>(maps, a);
+  return cuda_ok(cudaGetLastError(), "launch mat_reduce_kernel", err);
+}
+
+bool scores(const Ctx& c, const void* a_src, int ia, const void* b_src, int ib, float* out, std::string& err) {
+  const MatParams& p = c.p;
+  if (p.bf16)
+    return c.DHP == 64 ? launch_scores<1, 64>(c, a_src, ia, b_src, ib, out, p.status, p.timeout_ns, err)
+                       : launch_scores<1, 128>(c, a_src, ia, b_src, ib, out, p.status, p.timeout_ns, err);
+  return c.DHP == 64 ? launch_scores<3, 64>(c, a_src, ia, b_src, ib, out, p.status, p.timeout_ns, err)
+                     : launch_scores<3, 128>(c, a_src, ia, b_src, ib, out, p.status, p.timeout_ns, err);
+}
+
+template <bool TRANS>
+bool reduce(const Ctx& c, const float* x, const void* y_src, int iy, void* out, std::string& err) {
+  const MatParams& p = c.p;
+  if (p.bf16)
+    return c.DHP == 64 ? launch_reduce<TRANS, 1, 64>(c, x, y_src, iy, out, p.status, p.timeout_ns, err)
+                       : launch_reduce<TRANS, 1, 128>(c, x, y_src, iy, out, p.status, p.timeout_ns, err);
+  return c.DHP == 64 ? launch_reduce<TRANS, 2, 64>(c, x, y_src, iy, out, p.status, p.timeout_ns, err)
+                     : launch_reduce<TRANS, 2, 128>(c, x, y_src, iy, out, p.status, p.timeout_ns, err);
 }
 
 bool launch_softmax(float* s, float* lse, int64_t rows, int T, float scale, cudaStream_t st, std::string& err) {
@@ -385,6 +379,11 @@ bool launch_softmax_bwd(const float* p, float* dp, const float* dp_up, int64_t r
   else
     causal_softmax_bwd_kernel<false><<<grid_for(rows, 8), 256, 0, st>>>(p, dp, dp_up, rows, T, scale);
   return cuda_ok(cudaGetLastError(), "launch causal_softmax_bwd_kernel", err);
+}
+
+Ctx make_ctx(const MatParams& p, cudaStream_t st) {
+  return Ctx{p, st, layout(p.B, p.Hq, p.Hkv, p.T, p.Dh, p.bf16), int(p.B * p.Hq), int(p.Hq / p.Hkv), int(p.T),
+             int(p.Dh), p.Dh > 64 ? 128 : 64, static_cast<char*>(p.workspace)};
 }
 
 }  // namespace mat
@@ -405,87 +404,38 @@ size_t materialized_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t T
 
 bool materialized_fwd(const MatParams& p, cudaStream_t st, std::string& err) {
   using namespace mat;
-  Ctx c{p, st, layout(p.B, p.Hq, p.Hkv, p.T, p.Dh, p.bf16), int(p.B * p.Hq), int(p.Hq / p.Hkv), int(p.T),
-        int(p.Dh), nullptr, p.bf16 ? CUDA_R_16BF : CUDA_R_32F, size_t(p.bf16 ? 2 : 4)};
-  c.arr = reinterpret_cast<void**>(static_cast<char*>(p.workspace) + c.L.ptrs);
-  if (!build(c, err)) return false;
+  const Ctx c = make_ctx(p, st);
   const int64_t nkv = p.B * p.T * p.Hkv * p.Dh, nq = p.B * p.T * p.Hq * p.Dh;
-  if (p.bf16 && !convert(p.v, c.L.vf, nkv, c, err)) return false;
-  const int T = c.T, Dh = c.Dh, ldq = int(p.Hq * p.Dh), ldk = int(p.Hkv * p.Dh);
-  const float scale = float(1.0 / __builtin_sqrt(double(p.Dh)));
-  std::lock_guard<std::mutex> lk(g_cublas_mu);
-  cublasHandle_t h;
-  if (!handle_for_device(&h, err)) return false;
-  if (!cublas_ok(cublasSetStream(h, st), "cublasSetStream", err)) return false;
-  // S^T (col-major, = row-major S) = K Q^T: m = n = T, k = Dh.
-  if (!gemm(h, c, CUBLAS_OP_T, CUBLAS_OP_N, T, T, Dh, 1.f, A_K, c.st_type, ldk, A_Q, c.st_type, ldq, A_P, T,
-            "GEMM S = Q K^T", err))
-    return false;
-  if (!launch_softmax(p.probs, p.lse, int64_t(c.E) * T, T, scale, st, err)) return false;
-  // O^T (col-major view of row-major O) = V^T P^T: m = Dh, n = T, k = T.
-  if (!gemm(h, c, CUBLAS_OP_N, CUBLAS_OP_N, Dh, T, T, 1.f, A_VF, CUDA_R_32F, ldk, A_P, CUDA_R_32F, T, A_OF, ldq,
-            "GEMM O = P V", err))
-    return false;
-  if (p.bf16) {
-    to_bf16_kernel<<<grid_for(nq / 4, 256), 256, 0, st>>>(
-        reinterpret_cast<const float*>(static_cast<char*>(p.workspace) + c.L.of), static_cast<__nv_bfloat16*>(p.out),
-        nq / 4);
-    if (!cuda_ok(cudaGetLastError(), "launch to_bf16_kernel", err)) return false;
+  if (!p.bf16) {
+    if (!split3(c, p.q, P_Q, nq, err) || !split3(c, p.k, P_K, nkv, err) || !split3(c, p.v, P_V, nkv, err))
+      return false;
   }
-  return true;
+  const float scale = float(1.0 / __builtin_sqrt(double(p.Dh)));
+  // S = Q K^T into the probability rows (kept tiles only), then the softmax in place.
+  if (!scores(c, p.q, P_Q, p.k, P_K, p.probs, err)) return false;
+  if (!launch_softmax(p.probs, p.lse, int64_t(c.E) * c.T, c.T, scale, st, err)) return false;
+  // O = P V.
+  return reduce<false>(c, p.probs, p.v, P_V, p.out, err);
 }
 
 bool materialized_bwd(const MatParams& p, cudaStream_t st, std::string& err) {
   using namespace mat;
-  Ctx c{p, st, layout(p.B, p.Hq, p.Hkv, p.T, p.Dh, p.bf16), int(p.B * p.Hq), int(p.Hq / p.Hkv), int(p.T),
-        int(p.Dh), nullptr, p.bf16 ? CUDA_R_16BF : CUDA_R_32F, size_t(p.bf16 ? 2 : 4)};
-  c.arr = reinterpret_cast<void**>(static_cast<char*>(p.workspace) + c.L.ptrs);
-  if (!build(c, err)) return false;
+  const Ctx c = make_ctx(p, st);
   const int64_t nkv = p.B * p.T * p.Hkv * p.Dh, nq = p.B * p.T * p.Hq * p.Dh;
-  if (p.bf16) {
-    if (!convert(p.q, c.L.qf, nq, c, err) || !convert(p.k, c.L.kf, nkv, c, err) ||
-        !convert(p.dout, c.L.dof, nq, c, err))
+  if (!p.bf16) {
+    if (!split3(c, p.q, P_Q, nq, err) || !split3(c, p.k, P_K, nkv, err) || !split3(c, p.v, P_V, nkv, err) ||
+        !split3(c, p.dout, P_DO, nq, err))
       return false;
   }
-  const int T = c.T, Dh = c.Dh, ldq = int(p.Hq * p.Dh), ldk = int(p.Hkv * p.Dh);
   const float scale = float(1.0 / __builtin_sqrt(double(p.Dh)));
-  float* dp = reinterpret_cast<float*>(static_cast<char*>(p.workspace) + c.L.dp);
-  std::lock_guard<std::mutex> lk(g_cublas_mu);
-  cublasHandle_t h;
-  if (!handle_for_device(&h, err)) return false;
-  if (!cublas_ok(cublasSetStream(h, st), "cublasSetStream", err)) return false;
-  // dP^T (col-major) = V dO^T: m = n = T, k = Dh.
-  if (!gemm(h, c, CUBLAS_OP_T, CUBLAS_OP_N, T, T, Dh, 1.f, A_V, c.st_type, ldk, A_DO, c.st_type, ldq, A_DP, T,
-            "GEMM dP = dO V^T", err))
-    return false;
-  // dS (with respect to the unscaled scores, so the scale is inside).
-  if (!launch_softmax_bwd(p.probs, dp, p.dprobs, int64_t(c.E) * T, T, scale, st, err)) return false;
-  // dQ^T = K^T dS^T: m = Dh, n = T, k = T.
-  if (!gemm(h, c, CUBLAS_OP_N, CUBLAS_OP_N, Dh, T, T, 1.f, A_KF, CUDA_R_32F, ldk, A_DP, CUDA_R_32F, T, A_DQF, ldq,
-            "GEMM dQ = dS K", err))
-    return false;
-  // dK^T (per query head) = Q^T dS: m = Dh, n = T, k = T.
-  if (!gemm(h, c, CUBLAS_OP_N, CUBLAS_OP_T, Dh, T, T, 1.f, A_QF, CUDA_R_32F, ldq, A_DP, CUDA_R_32F, T, A_DKH, Dh,
-            "GEMM dK = dS^T Q", err))
-    return false;
-  // dV^T (per query head) = dO^T P: m = Dh, n = T, k = T.
-  if (!gemm(h, c, CUBLAS_OP_N, CUBLAS_OP_T, Dh, T, T, 1.f, A_DOF, CUDA_R_32F, ldq, A_P, CUDA_R_32F, T, A_DVH, Dh,
-            "GEMM dV = P^T dO", err))
-    return false;
-  const float* dkh = reinterpret_cast<const float*>(static_cast<char*>(p.workspace) + c.L.dkh);
-  const float* dvh = reinterpret_cast<const float*>(static_cast<char*>(p.workspace) + c.L.dvh);
-  const int gs = grid_for(nkv / 4, 256);
-  if (p.bf16) {
-    group_sum_kernel<true><<<gs, 256, 0, st>>>(dkh, p.dk, int(p.B), T, int(p.Hq), int(p.Hkv), Dh);
-    group_sum_kernel<true><<<gs, 256, 0, st>>>(dvh, p.dv, int(p.B), T, int(p.Hq), int(p.Hkv), Dh);
-    to_bf16_kernel<<<grid_for(nq / 4, 256), 256, 0, st>>>(
-        reinterpret_cast<const float*>(static_cast<char*>(p.workspace) + c.L.dqf), static_cast<__nv_bfloat16*>(p.dq),
-        nq / 4);
-  } else {
-    group_sum_kernel<false><<<gs, 256, 0, st>>>(dkh, p.dk, int(p.B), T, int(p.Hq), int(p.Hkv), Dh);
-    group_sum_kernel<false><<<gs, 256, 0, st>>>(dvh, p.dv, int(p.B), T, int(p.Hq), int(p.Hkv), Dh);
-  }
-  return cuda_ok(cudaGetLastError(), "launch group_sum / to_bf16 kernels", err);
+  float* dp = reinterpret_cast<float*>(c.ws + c.L.dp);
+  // dP = dO V^T (kept tiles), then dS (with respect to the unscaled scores) in place.
+  if (!scores(c, p.dout, P_DO, p.v, P_V, dp, err)) return false;
+  if (!launch_softmax_bwd(p.probs, dp, p.dprobs, int64_t(c.E) * c.T, c.T, scale, st, err)) return false;
+  // dQ = dS K;  dK = dS^T Q;  dV = P^T dO  (the last two summed over each group).
+  if (!reduce<false>(c, dp, p.k, P_K, p.dq, err)) return false;
+  if (!reduce<true>(c, dp, p.q, P_Q, p.dk, err)) return false;
+  return reduce<true>(c, p.probs, p.dout, P_DO, p.dv, err);
 }
 
 }  // namespace rca

@@ -2,6 +2,7 @@
 // attention path (materialized.cu). Not installed; callers use include/rca_attn.h.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -26,13 +27,22 @@ struct MatParams {
   bool bf16;
   void* workspace;
   size_t workspace_bytes;
+  int* status;                    // the library's device status word (bounded waits)
+  unsigned long long timeout_ns;  // device-side wait limit
 };
+
+// TMA descriptor of a [B, T, H, Dh] bf16 tensor, boxes of one 64-element
+// (128-byte, swizzled) panel x one head x box_rows positions; positions past T
+// and columns past Dh read as zero. Defined with the library's other
+// descriptors (rca_attn.cu).
+bool encode_rows_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t H, int64_t Dh,
+                     unsigned box_rows, std::string& err);
 
 // Bytes of scratch the materialized backward needs (the forward needs less).
 size_t materialized_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, bool bf16);
 
 // Enqueue the forward / backward on `st`. Arguments are validated by the
-// caller. Returns false and fills `err` on a CUDA or cuBLAS failure.
+// caller. Returns false and fills `err` on a CUDA failure.
 bool materialized_fwd(const MatParams& p, cudaStream_t st, std::string& err);
 bool materialized_bwd(const MatParams& p, cudaStream_t st, std::string& err);
 

@@ -108,6 +108,21 @@ rca_status make_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64
   return RCA_OK;
 }
 
+}  // namespace
+
+namespace rca {
+bool encode_rows_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t H, int64_t Dh,
+                     unsigned box_rows, std::string& err) {
+  if (make_map(m, ptr, B, T, H, Dh, false, "materialized operand", box_rows) != RCA_OK) {
+    err = g_err;
+    return false;
+  }
+  return true;
+}
+}  // namespace rca
+
+namespace {
+
 // ---------------------------------------------------------------------------
 // Per-device status word (device timeouts), allocated on first use.
 // ---------------------------------------------------------------------------
@@ -900,6 +915,8 @@ rca_status rca_attn_materialized_fwd(const void* q, const void* k, const void* v
   p.bf16 = dt == RCA_BF16;
   p.workspace = workspace;
   p.workspace_bytes = workspace_bytes;
+  RCA_CHECK(status_word(&p.status));
+  p.timeout_ns = g_timeout_ns.load();
   std::string err;
   if (!rca::materialized_fwd(p, static_cast<cudaStream_t>(cuda_stream), err))
     return fail(RCA_ERR_CUDA, "rca_attn_materialized_fwd: %s", err.c_str());
@@ -938,6 +955,8 @@ rca_status rca_attn_materialized_bwd(const void* q, const void* k, const void* v
   p.bf16 = dt == RCA_BF16;
   p.workspace = workspace;
   p.workspace_bytes = workspace_bytes;
+  RCA_CHECK(status_word(&p.status));
+  p.timeout_ns = g_timeout_ns.load();
   std::string err;
   if (!rca::materialized_bwd(p, static_cast<cudaStream_t>(cuda_stream), err))
     return fail(RCA_ERR_CUDA, "rca_attn_materialized_bwd: %s", err.c_str());

@@ -245,13 +245,19 @@ rca_status rca_attn_bwd_qkv(const void* qkv, const void* out, const float* lse, 
  * Layouts: q, out, dout, dq [B,T,Hq,Dh] and k, v, dk, dv [B,T,Hkv,Dh] in the
  * storage dtype (as rca_attn_fwd); probs, dprobs [B,Hq,T,T] float32 (4*B*Hq*T*T
  * bytes: 1 GiB for B=4, Hq=16, T=2048); lse [B,Hq,T] float32. Dh in {16, 32, 64,
- * 128} for both dtypes. The products over Dh use bf16 tensor cores with fp32
- * accumulation (RCA_BF16) or fp32 (RCA_F32_TF32); those over T are fp32. All
+ * 128} for both dtypes. Only the causal triangle is computed: score tiles
+ * above the diagonal are never formed and the products over T read only the
+ * kept triangle of probs (or dS). Arithmetic: tensor-core products with fp32
+ * accumulation. RCA_BF16: the products over Dh take the stored bf16 values
+ * (exact products), those over T take probs or dS as two bf16 parts hi + lo
+ * (relative representation error ~2^-17). RCA_F32_TF32: Q, K, V, dO enter as
+ * three bf16 parts each (scores to fp32 accuracy), probs or dS as two. All
  * tensors 16-byte aligned. workspace: at least
  * rca_attn_materialized_workspace_size(...) bytes (the same size serves both
  * calls), 256-byte aligned, contents on entry irrelevant. Every pointer is a
  * device pointer owned by the caller; calls validate, then only enqueue work
- * on cuda_stream (the GEMMs run in cuBLAS on that stream).
+ * on cuda_stream. Device waits are time-bounded like the other kernels'
+ * (RCA_ERR_DEVICE_TIMEOUT through rca_stream_status).
  */
 size_t rca_attn_materialized_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
                                             rca_dtype dt);

@@ -84,6 +84,36 @@ def test_small_every_output(case, with_dp):
         assert e <= GRAD_TOL[dt], f"{name} {nm}: {e:.3g}"
 
 
+# Mid-size shapes where every persistent CTA of the product kernels takes
+# several items (score tiles, 128-row output blocks, 128-key output blocks).
+MULTI = [
+    # name, B, Hq, Hkv, T, Dh, dtype      score tiles / row items / column items
+    ("bf16_dh32_gqa_multi", 4, 8, 4, 1300, 32, "bf16"),   # 2112 / 352 / 176
+    ("fp32_dh64_multi", 2, 12, 12, 1000, 64, "fp32"),     # 864 / 192 / 192
+]
+
+
+@pytest.mark.parametrize("case", MULTI, ids=[c[0] for c in MULTI])
+def test_multi_item_every_output(case):
+    name, B, Hq, Hkv, T, Dh, dt = case
+    w = small(name, B, Hq, Hkv, T, Dh, dt, seed=zlib.crc32(name.encode()) % 1000)
+    q, k, v, do = make_inputs(w)
+    out, probs, lse, dq, dk, dv = gpu_mat(q, k, v, do)
+    q64, k64, v64, do64 = (to64(x) for x in (q, k, v, do))
+    o_ref, p_ref, l_ref = oracle.attention_probs(q64, k64, v64)
+    check_probs(name, probs, lse, p_ref, l_ref)
+    o = to64(out)
+    if dt == "bf16":
+        err = np.abs(o - o_ref)
+        assert np.all(err <= 2.0 ** -8 * np.abs(o_ref) + 1e-5), f"{name}: O max err {err.max():.3g}"
+    else:
+        assert rel_fro(o, o_ref) <= GRAD_TOL["fp32"], name
+    ref = oracle.materialized_backward(q64, k64, v64, do64, None)
+    for nm, got, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        e = rel_fro(to64(got), r)
+        assert e <= GRAD_TOL[dt], f"{name} {nm}: {e:.3g}"
+
+
 def test_zero_dprobs_equals_none():
     w = small("mat_zero_dp", 1, 2, 2, 64, 64, "bf16", seed=3)
     q, k, v, do = make_inputs(w)
