@@ -39,10 +39,10 @@
 // register stores and the tensor core's operand reads all share, then carries
 // only Q, K and V. Wider heads stage P in shared memory (bf16, K-major,
 // 128-byte swizzle, one buffer per warpgroup).
-// Persistent launch (TMEM-resident P): one CTA per SM walks several work items
-// in the order that balances the SMs; the next item's Q tile, K tiles and
-// first scores are fetched and computed while the current item's epilogue
-// merges and stores its output.
+// Persistent launch (bf16 storage): one CTA per SM walks several work items
+// in the order that balances the SMs; the next item's K tiles and first
+// scores (and, with TMEM-resident P, its query tile) are fetched and computed
+// while the current item's epilogue merges and stores its output.
 // fp32 storage mode: both warpgroups take every key tile, warpgroup g keys
 // 64 g .. 64 g + 63 of it, with O_g accumulated from its half of the keys.
 // S = Q K^T runs as kind::tf32 on the fp32 tiles (the head dimension is
@@ -74,17 +74,21 @@ struct FwdCfg {
   // from TMEM), so it costs no shared-memory bandwidth, which on this part is
   // shared by TMA writes, register stores and the tensor core's operand reads.
   static constexpr bool PT = PP && DHP <= 64;
-  // Persistent CTAs hand each work item's merge and output to the epilogue
-  // warpgroup, so the softmax warpgroups go straight on to the next item.
-  static constexpr bool EPI_WG = PT;
+  // bf16 storage: persistent CTAs (one per SM) walk several work items and
+  // hand each item's merge and output to the epilogue warpgroup, so the
+  // softmax warpgroups go straight on to the next item.
+  static constexpr bool EPI_WG = PP;
   static constexpr int ES = TF32 ? 4 : 2;     // storage bytes per element
   static constexpr int PE = 128 / ES;         // elements per 128-byte swizzle row
   static constexpr int BM = 128, BN = 128;    // query rows, keys per tile
   static constexpr int PANEL = 128 * 128;     // one 128-row x 128-byte panel
   static constexpr int DPANELS = DHP / PE;    // panels across the head width
   static constexpr int Q_BYTES = DPANELS * PANEL;
-  // Persistent CTAs (TMEM-resident P) double-buffer Q so the next work item's
-  // query tile loads while the current one is still in use.
+  // Persistent CTAs with TMEM-resident P double-buffer Q so the next work
+  // item's query tile loads while the current one is still in use; at head
+  // width 128 (P staged in shared memory) only one Q buffer fits beside two
+  // K/V stages, and the next item's Q loads once the last S of the current
+  // item is done.
   static constexpr int QB = PT ? 2 : 1;
   static constexpr int KV_BYTES = DPANELS * PANEL;
   static constexpr int KSTEP = TF32 ? 8 : 16;  // K of one QK^T MMA instruction
@@ -101,13 +105,20 @@ struct FwdCfg {
   static constexpr int P_BUFS = TF32 ? 1 : 2;
   static constexpr int P_BUF = TF32 ? 2 * P_HALF : P_HALF;    // one buffer: hi (+ lo)
   static constexpr int P_BYTES = PT ? 0 : P_BUFS * P_BUF;
-  // Merge statistics m[2][128], l[2][128] (2 KB). Persistent CTAs keep two sets
-  // (by work-item parity) in a region of their own; otherwise they reuse the P
-  // buffer, dead once the CTA's only work item is finished.
-  static constexpr int STATX_BYTES = PT ? 4096 : 0;
+  // Merge statistics m[2][128], l[2][128] (2 KB per set). Persistent CTAs keep
+  // them in a region of their own: two sets (by work-item parity) with
+  // TMEM-resident P, one at head width 128; otherwise they reuse the P buffer,
+  // dead once the CTA's only work item is finished.
+  static constexpr int STAT_SETS = PT ? 2 : 1;
+  static constexpr int STATX_BYTES = EPI_WG ? 2048 * STAT_SETS : 0;
   static constexpr int SMEM_LIMIT = 232448;
-  static constexpr int BAR_BYTES = 1024;
-  static constexpr int AVAIL = SMEM_LIMIT - 1024 - BAR_BYTES - QB * Q_BYTES - P_BYTES - VHL_BYTES - STATX_BYTES;
+  static constexpr int BAR_BYTES = EPI_WG && !PT ? 512 : 1024;
+  // The dynamic shared memory of a block starts 1024-aligned (the first 1 KB
+  // of a block's shared memory is reserved by the hardware); the persistent
+  // head-width-128 layout uses the alignment slack the others keep, and the
+  // kernel checks the alignment at run time instead (error, no access).
+  static constexpr int SLACK = EPI_WG && !PT ? 0 : 1024;
+  static constexpr int AVAIL = SMEM_LIMIT - SLACK - BAR_BYTES - QB * Q_BYTES - P_BYTES - VHL_BYTES - STATX_BYTES;
   static constexpr int NS_BF = AVAIL / (2 * KV_BYTES) > 4 ? 4 : AVAIL / (2 * KV_BYTES);
   static constexpr int NSV = TF32 ? (AVAIL >= 4 * KV_BYTES ? 2 : 1) : NS_BF;
   static constexpr int NSK_FIT = TF32 ? (AVAIL - NSV * KV_BYTES) / KV_BYTES : NS_BF;
@@ -120,8 +131,8 @@ struct FwdCfg {
   static constexpr int OFF_VHL = OFF_P + P_BYTES;
   static constexpr int OFF_STATX = OFF_VHL + VHL_BYTES;
   static constexpr int OFF_BAR = OFF_STATX + STATX_BYTES;
-  static constexpr int OFF_STAT = PT ? OFF_STATX : OFF_P;
-  static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
+  static constexpr int OFF_STAT = EPI_WG ? OFF_STATX : OFF_P;
+  static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + SLACK;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
   static constexpr int TMEM_S = 0;          // two buffers: columns [0,128) and [128,256)
   static constexpr int TMEM_O = 256;        // O_0 at [256, 256+DHB), O_1 after it
@@ -153,7 +164,7 @@ struct FwdCfg {
   static constexpr int B_STATFREE = B_STAT + 2;
   static constexpr int B_FIN = B_STATFREE + 2;   // [2] exit: S issuer's / P V issuer's MMAs done
   static constexpr int NBAR = B_FIN + 2;
-  static_assert(8 * NBAR + 8 <= 512, "barrier area");
+  static_assert(8 * NBAR + 8 <= BAR_BYTES, "barrier area");
 };
 
 struct FwdArgs {
@@ -250,6 +261,13 @@ __global__ void __launch_bounds__(512, 1)
   using C = FwdCfg<TF32, DHP>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
+  if constexpr (C::SLACK == 0) {
+    // No alignment slack in this layout: a misaligned base is reported, never used.
+    if (raw & 1023u) {
+      if (threadIdx.x == 0) atomicExch(a.status, kStatusLayout);
+      return;
+    }
+  }
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * i; };
@@ -745,16 +763,18 @@ __global__ void __launch_bounds__(512, 1)
       }
       if (!ok) break;
       if constexpr (C::EPI_WG) {
-        // Publish this warpgroup's statistics of item n (set n % 2, free once
-        // the epilogue has read those of item n - 2) and go on to the next item.
-        if (n >= 2) {
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_STATFREE + (n & 1)), ((n - 2) >> 1) & 1, w));
+        // Publish this warpgroup's statistics of item n (set n % S, free once
+        // the epilogue has read those of item n - S) and go on to the next item.
+        constexpr int S = C::STAT_SETS;
+        const int set = n % S;
+        if (n >= S) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_STATFREE + set), ((n - S) / S) & 1, w));
           if (!ok) break;
         }
-        float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT) + (n & 1) * 512;
+        float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT) + set * 512;
         stat[g * 128 + row] = m;
         stat[256 + g * 128 + row] = l;
-        mbar_arrive(bar(C::B_STAT + (n & 1)));
+        mbar_arrive(bar(C::B_STAT + set));
         tb += it.nkv;
         continue;
       }
@@ -863,12 +883,14 @@ __global__ void __launch_bounds__(512, 1)
       int tb = 0;
       FwdItem it{};
       for (int n = 0; ok && fwd_item<LIST>(a, n, it); ++n) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_STAT + (n & 1)), (n >> 1) & 1, w));
+        constexpr int S = C::STAT_SETS;
+        const int set = n % S;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_STAT + set), (n / S) & 1, w));
         if (!ok) break;
-        const float* stat = reinterpret_cast<const float*>(smem + C::OFF_STAT) + (n & 1) * 512;
+        const float* stat = reinterpret_cast<const float*>(smem + C::OFF_STAT) + set * 512;
         const float m0 = stat[row], m1 = stat[128 + row];
         const float l0 = stat[256 + row], l1 = stat[384 + row];
-        mbar_arrive(bar(C::B_STATFREE + (n & 1)));
+        mbar_arrive(bar(C::B_STATFREE + set));
         const float mt = fmaxf(m0, m1);
         const float f0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - mt);
         const float f1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - mt);

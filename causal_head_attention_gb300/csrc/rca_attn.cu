@@ -358,7 +358,7 @@ rca_status launch_fwd(const void* q, const void* k, const void* v, int64_t B, in
   // kernel overlaps one item's epilogue with the next item's first products;
   // otherwise one CTA per work item.
   int grid = a.n_items;
-  if (C::PT) {
+  if (C::EPI_WG) {
     int sms = 0;
     RCA_CHECK(sm_count(&sms));
     if (grid > sms) grid = sms;
@@ -1143,6 +1143,10 @@ rca_status rca_stream_status(void* cuda_stream) {
   RCA_CHECK(noalloc_take_status(&hn));
   if (h == 0) h = hn;
   if (h != 0) {
+    if (h == rca::kStatusLayout)
+      return fail(RCA_ERR_CUDA,
+                  "a kernel found its dynamic shared memory not 1024-byte aligned and computed nothing; "
+                  "the affected results are invalid");
     if (h == rca::kStatusBadInput)
       return fail(RCA_ERR_DEVICE_INVALID_INPUT,
                   "a kernel read an invalid device-side input (a page ID outside [0, num_pages) or a "

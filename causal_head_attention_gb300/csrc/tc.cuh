@@ -13,6 +13,8 @@ namespace rca {
 constexpr int kStatusTimeout = 4;
 // A kernel read an invalid device-side input (a page ID or a length).
 constexpr int kStatusBadInput = 5;
+// A kernel found its dynamic shared memory not 1024-byte aligned and did nothing.
+constexpr int kStatusLayout = 6;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
