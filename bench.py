@@ -855,6 +855,36 @@ def bench_decode(w, dev, stream, steps, warmup, cpu_budget, P):
     }
 
 
+def profile_case(case: str, w) -> int:
+    """One small invocation of a kernel family on cuda:0, untimed, for profiler
+    captures: three forward calls (fwd), three backward calls after one
+    forward (bwd), or two materialized forward + backward calls on the
+    workload's shape cut to one batch row (materialized: [1, Hq, T, T] fp32
+    probabilities, 1 GiB at T = 8192, 256 MiB at the headline T)."""
+    from dataclasses import replace
+
+    import causal_head_attention_gb300 as rca
+
+    if case == "materialized":
+        w = replace(w, B=1)
+    q, k, v, do = (x.cuda() for x in make_inputs(w))
+    if case == "fwd":
+        for _ in range(3):
+            rca.attention_forward(q, k, v)
+    elif case == "bwd":
+        out, lse = rca.attention_forward(q, k, v)
+        for _ in range(3):
+            rca.attention_backward(q, k, v, out, lse, do)
+    else:
+        for _ in range(2):
+            out, probs, lse = rca.materialized_forward(q, k, v)
+            rca.materialized_backward(q, k, v, probs, do)
+    torch.cuda.synchronize()
+    rca.rca_stream_status()
+    print(json.dumps({"profile_case": case, "workload": w.describe()}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -873,10 +903,14 @@ def main():
                     help="skip the fused-layout, variable-length and materialized-path measurements")
     ap.add_argument("--decode-steps", type=int, default=50)
     ap.add_argument("--decode-cpu-budget", type=float, default=3.0)
+    ap.add_argument("--profile-case", choices=["fwd", "bwd", "materialized"],
+                    help="run one small untimed invocation of a kernel family (for profiler captures) and exit")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     args.metric = "causal attn fwd+bwd TFLOP/s at B4 H16 T2048 Dh64 BF16; % of GB300 tensor peak"
     w = BY_NAME[args.workload]
+    if args.profile_case:
+        return profile_case(args.profile_case, w)
     world, rank, local = dist_setup()
     if args.impl == "reference":
         rc = run_reference(args, w, world, rank)

@@ -313,7 +313,14 @@ struct BwdCfg {
   static constexpr int B_KVFREE = B_ITF + 1;  // dK, dV of a work item read (drain warpgroup)
   static constexpr int B_KVD = B_KVFREE + 1;   // dK, dV of a work item final (its last dK done)
   static constexpr int B_FIN = B_KVD + 1;
-  static constexpr int NBAR = B_FIN + 1;
+  // Aliased dQ columns: the drain stages the four 32-column blocks of a dQ
+  // partial in the P^T and dS^T buffers (idle while dQ is drained) and
+  // releases the columns as soon as they are read; this barrier (one arrival
+  // per drain warp) says the bulk reductions have finished reading them.
+  static constexpr int B_STGF = B_FIN + 1;
+  static constexpr int NBAR = B_STGF + 1;
+  static_assert(!DQ_ALIAS || (!SHARE && P_SMEM == 2 * PANEL * NPART && NPART == 1 && DHB == 128),
+                "dQ staging in the P^T / dS^T buffers assumes separate 32 KB buffers");
   // parts multiplied for one product: (hi,hi) [, (hi,lo), (lo,hi)]
   static constexpr int NPROD = HL ? 3 : 1;
   __device__ static constexpr int pa(int t) { return t == 2 ? 1 : 0; }
@@ -435,6 +442,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(bar(C::B_KVFREE), 128);  // the dQ drain warpgroup writes dK, dV
     mbar_init(bar(C::B_KVD), 1);
     mbar_init(bar(C::B_FIN), 1);
+    mbar_init(bar(C::B_STGF), 4);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -782,8 +790,11 @@ __global__ void __launch_bounds__(512, 1)
             tc_fence_before();
             mbar_arrive(bar(C::B_ITF));  // dQ(gi) read: its columns may be overwritten
           }
-          const uint32_t panel = sbase + C::OFF_DQS;
-          if (lane == 0) bulk_wait_read0();  // the previous block has been read from the slice
+          // Aliased dQ columns: block c goes to its own slice of the P^T / dS^T
+          // buffers (no wait between blocks); otherwise the one staging panel,
+          // rewritten once the previous block's reduction has read it.
+          const uint32_t panel = C::DQ_ALIAS ? sbase + C::OFF_P + c * 16384 : sbase + C::OFF_DQS;
+          if (!C::DQ_ALIAS && lane == 0) bulk_wait_read0();
           __syncwarp();
 #pragma unroll
           for (int k = 0; k < 8; ++k)
@@ -799,6 +810,15 @@ __global__ void __launch_bounds__(512, 1)
               tma_reduce_add_4d(&maps.dq, panel + quarter * 4096, 32 * c, h, i * 128 + quarter * 32, itm.b);
             bulk_commit();
           }
+        }
+        if constexpr (C::DQ_ALIAS) {
+          // The next iteration's P^T and dS^T may overwrite the slices once
+          // these reductions have read them.
+          if (lane == 0) {
+            bulk_wait_read0();
+            mbar_arrive(bar(C::B_STGF));
+          }
+          __syncwarp();
         }
       }
     }
@@ -883,6 +903,13 @@ __global__ void __launch_bounds__(512, 1)
             tmem_st16(tl + C::TM_P + 32 * g + 16 * hh, pk);
           }
         } else {
+          if constexpr (C::DQ_ALIAS) {
+            // The P^T / dS^T buffers held dQ(gi - 1) blocks for its reductions.
+            if (gi > 0) {
+              ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_STGF), (gi - 1) & 1, w));
+              if (!ok) break;
+            }
+          }
           store_half_row_bf16<HL>(sbase + C::OFF_P + g * C::PANEL, rl, p, C::PT_HALF);
           fence_async_smem();
         }
