@@ -353,30 +353,42 @@ def run_gpu(args, w, world, rank, local):
     n_warm = args.warmup
     rca.rca_stream_status(stream)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    # Timed region: exactly K steps with nothing between the launches, so each
+    # kernel's launch overlaps the tail of the one before (the library launches
+    # them with programmatic dependent launch; an event recorded between two
+    # kernels would serialise them again).
     barrier(world)
     torch.cuda.synchronize(dev)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
-        step(n_warm + i, evs[i])
+        step(n_warm + i)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
+    # Per-kernel durations: the same K steps once more, with an event between
+    # every two launches on the launching stream. These intervals include each
+    # kernel's full launch gap (events take away the overlap), so they are
+    # upper bounds on the kernels' own durations.
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        step(n_warm + args.steps + i, evs[i])
+    torch.cuda.synchronize(dev)
     # The same step again, untimed, for at least min_warmup_s: clock samples
     # under load (the timed steps alone last only milliseconds).
     t_c = time.perf_counter()
     n_clock = 0
     while time.perf_counter() - t_c < args.min_warmup_s:
-        step(n_warm + args.steps + n_clock)
+        step(n_warm + 2 * args.steps + n_clock)
         n_clock += 1
         if n_clock % 64 == 0:
             torch.cuda.synchronize(dev)
     torch.cuda.synchronize(dev)
     clocks = clk.stop()
     if clocks is not None:
-        clocks["window"] = (f"{args.warmup} warm-up + {args.steps} timed steps + {n_clock} more steps "
+        clocks["window"] = (f"{args.warmup} warm-up + {args.steps} timed steps + {args.steps} steps with "
+                            f"per-kernel events + {n_clock} more steps "
                             f"({time.perf_counter() - t_c:.1f} s) after the timed region")
     rca.rca_stream_status(stream)
     total_ms = t_start.elapsed_time(t_end)
@@ -387,6 +399,7 @@ def run_gpu(args, w, world, rank, local):
             per[n].append(e[j].elapsed_time(e[j + 1]))
     avg = {n: sum(v) / len(v) for n, v in per.items()}
     step_spread = spread([e[0].elapsed_time(e[4]) for e in evs])
+    step_spread["pass"] = "per-kernel pass (an event between every two launches)"
 
     ms = max_over_ranks(total_ms, world) / args.steps
     F = fwd_flops(w)
@@ -560,6 +573,8 @@ def run_gpu(args, w, world, rank, local):
             },
             "kernels": {n: {k2: (round(v2, 6) if isinstance(v2, float) else v2) for k2, v2 in d.items()}
                         for n, d in kern.items()},
+            "kernels_timing": ("second pass of the same K steps with an event between every two launches; "
+                               "each interval includes the kernel's launch gap"),
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": clocks,

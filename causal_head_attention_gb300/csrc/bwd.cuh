@@ -52,6 +52,7 @@ struct PreArgs {
 // fits (the divisions are then far cheaper), 64-bit otherwise.
 template <bool F32, typename IT>
 __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const PreArgs a) {
+  grid_dep_sync();
   constexpr int ES = F32 ? 4 : 2;
   constexpr int EPL = 16 / ES;  // elements per lane
   const unsigned lpr = static_cast<unsigned>(a.Dh / EPL);  // lanes per row: power of two in [2, 32]
@@ -120,6 +121,7 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const PreArgs 
 // kernel (lpr lanes per row, a power of two).
 template <bool F32>
 __global__ void __launch_bounds__(256) attn_bwd_preprocess_varlen_kernel(const PreArgs a) {
+  grid_dep_sync();
   constexpr int ES = F32 ? 4 : 2;
   constexpr int EPL = 16 / ES;
   const int b = blockIdx.y;
@@ -179,6 +181,7 @@ template <bool F32, bool STRIDED>
 __global__ void __launch_bounds__(256)
     attn_bwd_dq_convert_kernel(const float* __restrict__ acc, void* __restrict__ dq, long long n4,
                                float scale, long long row4, long long dq_row4) {
+  grid_dep_sync();
   constexpr int U = 4;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += U * stride) {
@@ -211,6 +214,7 @@ template <bool STRIDED>
 __global__ void __launch_bounds__(256)
     split_hilo_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ hi,
                       __nv_bfloat16* __restrict__ lo, long long n4, long long row4, long long src_row4) {
+  grid_dep_sync();
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
     const long long si = STRIDED ? (i / row4) * src_row4 + i % row4 : i;
@@ -405,6 +409,7 @@ template <bool HL, int DHB, bool LIST>
 __global__ void __launch_bounds__(512, 1)
     attn_bwd_main_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   using C = BwdCfg<HL, DHB>;
+  grid_dep_sync();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);

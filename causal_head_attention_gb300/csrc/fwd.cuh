@@ -259,6 +259,7 @@ __global__ void __launch_bounds__(512, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
   using C = FwdCfg<TF32, DHP>;
+  grid_dep_sync();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   if constexpr (C::SLACK == 0) {

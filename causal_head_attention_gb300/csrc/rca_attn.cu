@@ -11,6 +11,7 @@
 #include <cstdio>
 #include <mutex>
 #include <string>
+#include <utility>
 
 #include "rca_attn.h"
 #include "bwd.cuh"
@@ -171,6 +172,28 @@ rca_status sm_count(int* out) {
   }
   *out = g_sms[dev];
   return RCA_OK;
+}
+
+// Launch with programmatic dependent launch allowed: the kernel may be
+// scheduled while the kernel before it in the stream is still finishing, which
+// hides most of the gap between the kernels of a training step (~4 us each
+// otherwise). Every kernel launched this way calls rca::grid_dep_sync() before
+// it touches global memory, so it still sees everything earlier in the
+// stream. A failed launch is reported through cudaGetLastError() like a
+// <<<>>> launch.
+template <typename... KA, typename... A>
+void launch_dep(void (*kern)(KA...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, A&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  (void)cudaLaunchKernelEx(&cfg, kern, std::forward<A>(args)...);
 }
 
 template <typename K>
@@ -363,7 +386,7 @@ rca_status launch_fwd(const void* q, const void* k, const void* v, int64_t B, in
     RCA_CHECK(sm_count(&sms));
     if (grid > sms) grid = sms;
   }
-  kern<<<unsigned(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(mq, mk, mv, a);
+  launch_dep(kern, dim3(unsigned(grid)), dim3(C::NTHREADS), C::SMEM_BYTES, st, mq, mk, mv, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch attn_fwd_kernel");
   return RCA_OK;
@@ -380,10 +403,10 @@ rca_status launch_split(const void* src, void* hi, void* lo, size_t n, int64_t r
   const long long want = (n4 + 255) / 256, cap = (long long)sms * 8;
   const unsigned grid = unsigned(want < cap ? (want > 0 ? want : 1) : cap);
   if (src_row == row_len)
-    rca::split_hilo_kernel<false><<<grid, 256, 0, st>>>(static_cast<const float*>(src), static_cast<__nv_bfloat16*>(hi),
+    launch_dep(rca::split_hilo_kernel<false>, dim3(grid), dim3(256), 0, st, static_cast<const float*>(src), static_cast<__nv_bfloat16*>(hi),
                                                          static_cast<__nv_bfloat16*>(lo), n4, row_len / 4, src_row / 4);
   else
-    rca::split_hilo_kernel<true><<<grid, 256, 0, st>>>(static_cast<const float*>(src), static_cast<__nv_bfloat16*>(hi),
+    launch_dep(rca::split_hilo_kernel<true>, dim3(grid), dim3(256), 0, st, static_cast<const float*>(src), static_cast<__nv_bfloat16*>(hi),
                                                         static_cast<__nv_bfloat16*>(lo), n4, row_len / 4, src_row / 4);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch split_hilo_kernel");
@@ -479,7 +502,7 @@ rca_status launch_bwd_main(const void* q, const void* k, const void* v, const vo
     RCA_CHECK(sm_count(&sms));
     if (grid > sms) grid = sms;
   }
-  kern<<<unsigned(grid), C::NTHREADS, C::SMEM_BYTES, st>>>(maps, a);
+  launch_dep(kern, dim3(unsigned(grid)), dim3(C::NTHREADS), C::SMEM_BYTES, st, maps, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch attn_bwd_main_kernel");
   return RCA_OK;
@@ -564,7 +587,7 @@ rca_status plan_varlen(const int* lens, int64_t B, int64_t Hq, int64_t Hkv, int6
   a.T = int(T);
   a.n_qt = int((T + 127) / 128);
   const size_t smem = (2 * size_t(B) + 3 * (size_t(a.n_qt) + 1)) * sizeof(int);
-  rca::varlen_plan_kernel<<<1, rca::kVarlenPlanThreads, smem, st>>>(a);
+  launch_dep(rca::varlen_plan_kernel, dim3(1), dim3(rca::kVarlenPlanThreads), smem, st, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch varlen_plan_kernel");
   *fwd_items = a.fwd_items;
@@ -585,9 +608,9 @@ rca_status zero_padding(void* x, float* lse, const int* lens, int64_t B, int64_t
   const int64_t want = (per_seq + 1023) / 1024, cap = std::max<int64_t>(1, int64_t(sms) * 8 / B);
   const dim3 grid(unsigned(std::max<int64_t>(1, std::min(want, cap))), unsigned(B), x2 ? 2u : 1u);
   if (dt == RCA_BF16)
-    rca::varlen_zero_kernel<2><<<grid, 256, 0, st>>>(x, x2, lse, lens, int(T), int(H), int(Dh));
+    launch_dep(rca::varlen_zero_kernel<2>, dim3(grid), dim3(256), 0, st, x, x2, lse, lens, int(T), int(H), int(Dh));
   else
-    rca::varlen_zero_kernel<4><<<grid, 256, 0, st>>>(x, x2, lse, lens, int(T), int(H), int(Dh));
+    launch_dep(rca::varlen_zero_kernel<4>, dim3(grid), dim3(256), 0, st, x, x2, lse, lens, int(T), int(H), int(Dh));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch varlen_zero_kernel");
   return RCA_OK;
@@ -605,9 +628,9 @@ rca_status varlen_convert(void* dq, const int* lens, int64_t B, int64_t Hq, int6
   const dim3 grid(unsigned(std::max<int64_t>(1, std::min(want, cap))), unsigned(B));
   const float scale = float(1.0 / std::sqrt(double(Dh)));
   if (dt == RCA_BF16)
-    rca::varlen_dq_convert_kernel<false><<<grid, 256, 0, st>>>(acc, dq, lens, int(T), row4, scale);
+    launch_dep(rca::varlen_dq_convert_kernel<false>, dim3(grid), dim3(256), 0, st, acc, dq, lens, int(T), row4, scale);
   else
-    rca::varlen_dq_convert_kernel<true><<<grid, 256, 0, st>>>(acc, dq, lens, int(T), row4, scale);
+    launch_dep(rca::varlen_dq_convert_kernel<true>, dim3(grid), dim3(256), 0, st, acc, dq, lens, int(T), row4, scale);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch varlen_dq_convert_kernel");
   return RCA_OK;
@@ -636,9 +659,9 @@ rca_status do_preprocess(const void* out, const float* lse, const void* dout, in
     const int64_t want = (L.Tpad * Hq * lpr + 255) / 256, cap = std::max<int64_t>(1, int64_t(sms) * 8 / B);
     const dim3 grid(unsigned(std::max<int64_t>(1, std::min(want, cap))), unsigned(B));
     if (dt == RCA_BF16)
-      rca::attn_bwd_preprocess_varlen_kernel<false><<<grid, 256, 0, st>>>(a);
+      launch_dep(rca::attn_bwd_preprocess_varlen_kernel<false>, dim3(grid), dim3(256), 0, st, a);
     else
-      rca::attn_bwd_preprocess_varlen_kernel<true><<<grid, 256, 0, st>>>(a);
+      launch_dep(rca::attn_bwd_preprocess_varlen_kernel<true>, dim3(grid), dim3(256), 0, st, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch attn_bwd_preprocess_varlen_kernel");
     return RCA_OK;
@@ -647,11 +670,11 @@ rca_status do_preprocess(const void* out, const float* lse, const void* dout, in
   const unsigned grid = unsigned((threads + 255) / 256);
   const bool narrow = (int64_t(grid) * 256) < (int64_t(1) << 31);  // 32-bit thread indices suffice
   if (dt == RCA_BF16) {
-    if (narrow) rca::attn_bwd_preprocess_kernel<false, uint32_t><<<grid, 256, 0, st>>>(a);
-    else rca::attn_bwd_preprocess_kernel<false, unsigned long long><<<grid, 256, 0, st>>>(a);
+    if (narrow) launch_dep(rca::attn_bwd_preprocess_kernel<false, uint32_t>, dim3(grid), dim3(256), 0, st, a);
+    else launch_dep(rca::attn_bwd_preprocess_kernel<false, unsigned long long>, dim3(grid), dim3(256), 0, st, a);
   } else {
-    if (narrow) rca::attn_bwd_preprocess_kernel<true, uint32_t><<<grid, 256, 0, st>>>(a);
-    else rca::attn_bwd_preprocess_kernel<true, unsigned long long><<<grid, 256, 0, st>>>(a);
+    if (narrow) launch_dep(rca::attn_bwd_preprocess_kernel<true, uint32_t>, dim3(grid), dim3(256), 0, st, a);
+    else launch_dep(rca::attn_bwd_preprocess_kernel<true, unsigned long long>, dim3(grid), dim3(256), 0, st, a);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch attn_bwd_preprocess_kernel");
@@ -672,11 +695,11 @@ rca_status do_convert(void* dq, int64_t B, int64_t Hq, int64_t T, int64_t Dh, rc
   const long long row4 = Hq * Dh / 4, dq_row4 = dqs / 4;
   const bool strided = dqs != Hq * Dh;
   if (dt == RCA_BF16) {
-    if (strided) rca::attn_bwd_dq_convert_kernel<false, true><<<grid, 256, 0, st>>>(acc, dq, n4, scale, row4, dq_row4);
-    else rca::attn_bwd_dq_convert_kernel<false, false><<<grid, 256, 0, st>>>(acc, dq, n4, scale, row4, dq_row4);
+    if (strided) launch_dep(rca::attn_bwd_dq_convert_kernel<false, true>, dim3(grid), dim3(256), 0, st, acc, dq, n4, scale, row4, dq_row4);
+    else launch_dep(rca::attn_bwd_dq_convert_kernel<false, false>, dim3(grid), dim3(256), 0, st, acc, dq, n4, scale, row4, dq_row4);
   } else {
-    if (strided) rca::attn_bwd_dq_convert_kernel<true, true><<<grid, 256, 0, st>>>(acc, dq, n4, scale, row4, dq_row4);
-    else rca::attn_bwd_dq_convert_kernel<true, false><<<grid, 256, 0, st>>>(acc, dq, n4, scale, row4, dq_row4);
+    if (strided) launch_dep(rca::attn_bwd_dq_convert_kernel<true, true>, dim3(grid), dim3(256), 0, st, acc, dq, n4, scale, row4, dq_row4);
+    else launch_dep(rca::attn_bwd_dq_convert_kernel<true, false>, dim3(grid), dim3(256), 0, st, acc, dq, n4, scale, row4, dq_row4);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch attn_bwd_dq_convert_kernel");

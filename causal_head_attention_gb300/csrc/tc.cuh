@@ -326,6 +326,18 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64
 // ----------------------------------------------------------------------------
 // Small arithmetic helpers (hardware instructions, no library math).
 // ----------------------------------------------------------------------------
+// Programmatic dependent launch. The library launches the kernels of a
+// training step so that each may be scheduled while the kernel before it in
+// the stream is still finishing; every such kernel calls this first, before it
+// reads or writes global memory: griddepcontrol.wait returns once all earlier
+// kernels of the stream have completed and their writes are visible, and
+// launch_dependents then lets the next kernel of the stream be scheduled. In a
+// kernel launched without the attribute both are no-ops.
+__device__ __forceinline__ void grid_dep_sync() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -36,6 +36,7 @@ struct VarlenPlanArgs {
 // Dynamic shared memory: nq[B], order[B], cnt[n_qt + 1] (#sequences with
 // nq_b > l for level l), fwd_off[n_qt + 1], bwd_off[n_qt + 1].
 __global__ void __launch_bounds__(kVarlenPlanThreads) varlen_plan_kernel(const VarlenPlanArgs a) {
+  grid_dep_sync();
   extern __shared__ int sm[];
   int* nq = sm;
   int* order = nq + a.B;
@@ -120,6 +121,7 @@ template <int ES>
 __global__ void __launch_bounds__(256)
     varlen_zero_kernel(void* __restrict__ x, void* __restrict__ x2, float* __restrict__ lse,
                        const int* __restrict__ lens, int T, int H, int Dh) {
+  grid_dep_sync();
   if (blockIdx.z == 1) {
     x = x2;
     lse = nullptr;
@@ -149,6 +151,7 @@ template <bool F32>
 __global__ void __launch_bounds__(256)
     varlen_dq_convert_kernel(const float* __restrict__ acc, void* __restrict__ dq, const int* __restrict__ lens,
                              int T, long long row4, float scale) {
+  grid_dep_sync();
   constexpr int U = 4;
   const int b = blockIdx.y;
   int L = __ldg(lens + b);

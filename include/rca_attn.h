@@ -45,6 +45,14 @@
  * return; they never synchronise. Inputs are never written. Outputs are fully
  * overwritten. The library keeps, per device, a small cache of TMA descriptors
  * and one device status word used by the bounded-wait timeout described below.
+ * The kernels of the Flash forward and backward (and of the fused-QKV and
+ * variable-length calls) are launched with programmatic dependent launch: one
+ * may be scheduled onto the GPU while the kernel before it on cuda_stream is
+ * still finishing, which hides most of the launch gap between the kernels of a
+ * training step. Stream order is unchanged: each such kernel waits, before it
+ * reads or writes any memory, until all work queued before it on cuda_stream
+ * has completed, and nothing queued after it touches memory before it has
+ * completed.
  *
  * Errors. Every argument is validated before anything is launched; on a
  * validation failure nothing is enqueued. No C++ exception crosses this
