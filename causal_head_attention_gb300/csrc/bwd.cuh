@@ -543,35 +543,47 @@ __global__ void __launch_bounds__(512, 1)
    } else if (warp == 13) {
     // ---------------- tcgen05 MMA issuer (one elected thread) ----------------
     if (elect_one()) {
-      const uint32_t dsb = sbase + C::OFF_DS;
-      const uint32_t pb = sbase + C::OFF_P;
+      // Shared-memory descriptors are built once and moved by constant
+      // offsets (desc_add): the issuing thread shares its sub-partition with
+      // compute warps, so every instruction it saves shortens the gaps
+      // between products. K-major operands (16-byte leading offset) and
+      // MN-major ones (a 64-column panel apart) of each buffer:
+      const uint64_t k_km = make_sdesc(sbase + C::OFF_K, 16, 1024);        // K: A of S^T
+      const uint64_t v_km = make_sdesc(sbase + C::OFF_V, 16, 1024);        // V: A of dP^T
+      const uint64_t k_mn = make_sdesc(sbase + C::OFF_K, C::PANEL, 1024);  // K: B of dQ
+      const uint64_t q_km = make_sdesc(stage(0), 16, 1024);                // Q: B of S^T
+      const uint64_t q_mn = make_sdesc(stage(0), C::PANEL, 1024);          // Q: B of dK
+      const uint64_t do_km = make_sdesc(stage(0) + C::OPND, 16, 1024);     // dO: B of dP^T
+      const uint64_t do_mn = make_sdesc(stage(0) + C::OPND, C::PANEL, 1024);  // dO: B of dV
+      const uint64_t ds_km = make_sdesc(sbase + C::OFF_DS, 16, 1024);      // dS^T: A of dK
+      const uint64_t ds_mn = make_sdesc(sbase + C::OFF_DS, C::PANEL, 1024);  // dS: A of dQ
+      const uint64_t p_km = make_sdesc(sbase + C::OFF_P, 16, 1024);        // P^T in shared memory: A of dV
       // S^T = K Q^T (M = keys, N = queries, K = head dim) into TMEM_S, for
       // iteration gi2 whose item uses K/V buffer x2.
       auto issue_s = [&](int gi2, int x2) {
-        const uint32_t qb = stage(gi2 % C::NQS);
-        const uint32_t kb = sbase + C::OFF_K + x2 * 2 * C::OPND;
+        const uint64_t db = desc_add(q_km, (gi2 % C::NQS) * C::STAGE_BYTES);
+        const uint64_t da = desc_add(k_km, x2 * 2 * C::OPND);
 #pragma unroll
         for (int t = 0; t < C::NPROD; ++t)
 #pragma unroll
           for (int k = 0; k < DHB / 16; ++k) {
             const uint32_t off = (k / 4) * C::PANEL + (k % 4) * 32;
-            mma_ss<false>(tmem + C::TM_S, make_sdesc(kb + C::pa(t) * C::TILE + off, 16, 1024),
-                          make_sdesc(qb + C::pb(t) * C::TILE + off, 16, 1024), C::IDESC_T, (t > 0 || k > 0) ? 1u : 0u);
+            mma_ss<false>(tmem + C::TM_S, desc_add(da, C::pa(t) * C::TILE + off),
+                          desc_add(db, C::pb(t) * C::TILE + off), C::IDESC_T, (t > 0 || k > 0) ? 1u : 0u);
           }
         tc_commit(bar(C::B_SR));
       };
       // dP^T = V dO^T into TMEM_DP
       auto issue_dp = [&](int gi2, int x2) {
-        const uint32_t dob = stage(gi2 % C::NQS) + C::OPND;
-        const uint32_t vb = sbase + C::OFF_V + x2 * 2 * C::OPND;
+        const uint64_t db = desc_add(do_km, (gi2 % C::NQS) * C::STAGE_BYTES);
+        const uint64_t da = desc_add(v_km, x2 * 2 * C::OPND);
 #pragma unroll
         for (int t = 0; t < C::NPROD; ++t)
 #pragma unroll
           for (int k = 0; k < DHB / 16; ++k) {
             const uint32_t off = (k / 4) * C::PANEL + (k % 4) * 32;
-            mma_ss<false>(tmem + C::TM_DP, make_sdesc(vb + C::pa(t) * C::TILE + off, 16, 1024),
-                          make_sdesc(dob + C::pb(t) * C::TILE + off, 16, 1024), C::IDESC_T,
-                          (t > 0 || k > 0) ? 1u : 0u);
+            mma_ss<false>(tmem + C::TM_DP, desc_add(da, C::pa(t) * C::TILE + off),
+                          desc_add(db, C::pb(t) * C::TILE + off), C::IDESC_T, (t > 0 || k > 0) ? 1u : 0u);
           }
         tc_commit(bar(C::B_DPR));
       };
@@ -586,12 +598,12 @@ __global__ void __launch_bounds__(512, 1)
       }
       while (ok) {
         const int x = n % C::KVB;
-        const uint32_t kb = sbase + C::OFF_K + x * 2 * C::OPND;
+        const uint64_t kx_mn = desc_add(k_mn, x * 2 * C::OPND);  // this item's K as the B operand of dQ
         BwdItem nxt{};
         const bool has_next = bwd_item<LIST>(a, n + 1, nxt);
         for (int it = 0; ok && it < itm.n_it; ++it, ++gi) {
           const int s = gi % C::NQS;
-          const uint32_t qb = stage(s), dob = stage(s) + C::OPND;
+          const uint64_t qs_mn = desc_add(q_mn, s * C::STAGE_BYTES), dos_mn = desc_add(do_mn, s * C::STAGE_BYTES);
           // The next iteration: in this item, or the first of the next item.
           const bool more_here = it + 1 < itm.n_it;
           const bool more = more_here || (C::KVB > 1 && has_next);
@@ -634,13 +646,12 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
               for (int k = 4 * g; k < 4 * g + 4; ++k) {
                 const uint32_t acc = (it > 0 || g > 0 || t > 0 || k > 0) ? 1u : 0u;
-                const uint64_t bd = make_sdesc(dob + C::pb(t) * C::TILE + k * 16 * 128, C::PANEL, 1024);
+                const uint64_t bd = desc_add(dos_mn, C::pb(t) * C::TILE + k * 16 * 128);
                 if constexpr (C::PTB) {
                   mma_ts(tmem + C::TM_DV, tmem + C::TM_P + 8 * k, bd, C::IDESC_KV, acc);
                 } else {
                   const uint32_t aoff = (k / 4) * C::PANEL + (k % 4) * 32;
-                  mma_ss<false>(tmem + C::TM_DV, make_sdesc(pb + C::pa(t) * C::PT_HALF + aoff, 16, 1024), bd,
-                                C::IDESC_KV, acc);
+                  mma_ss<false>(tmem + C::TM_DV, desc_add(p_km, C::pa(t) * C::PT_HALF + aoff), bd, C::IDESC_KV, acc);
                 }
               }
             // P^T half g is free again once this product is done (it no longer
@@ -661,8 +672,8 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
               for (int k = 4 * g; k < 4 * g + 4; ++k) {
                 const uint32_t aoff = (k / 4) * C::PANEL + (k % 4) * 32;
-                mma_ss<false>(tmem + C::TM_DK, make_sdesc(dsb + C::pa(t) * C::PT_HALF + aoff, 16, 1024),
-                              make_sdesc(qb + C::pb(t) * C::TILE + k * 16 * 128, C::PANEL, 1024), C::IDESC_KV,
+                mma_ss<false>(tmem + C::TM_DK, desc_add(ds_km, C::pa(t) * C::PT_HALF + aoff),
+                              desc_add(qs_mn, C::pb(t) * C::TILE + k * 16 * 128), C::IDESC_KV,
                               (it > 0 || g > 0 || t > 0 || k > 0) ? 1u : 0u);
               }
           }
@@ -687,9 +698,8 @@ __global__ void __launch_bounds__(512, 1)
           for (int t = 0; t < C::NPROD; ++t)
 #pragma unroll
             for (int k = 0; k < 128 / 16; ++k)
-              mma_ss<false>(tmem + C::TM_DQ, make_sdesc(dsb + C::pa(t) * C::PT_HALF + k * 16 * 128, C::PANEL, 1024),
-                            make_sdesc(kb + C::pb(t) * C::TILE + k * 16 * 128, C::PANEL, 1024), C::IDESC_Q,
-                            (t > 0 || k > 0) ? 1u : 0u);
+              mma_ss<false>(tmem + C::TM_DQ, desc_add(ds_mn, C::pa(t) * C::PT_HALF + k * 16 * 128),
+                            desc_add(kx_mn, C::pb(t) * C::TILE + k * 16 * 128), C::IDESC_Q, (t > 0 || k > 0) ? 1u : 0u);
           tc_commit(bar(C::B_DQF));
           if (!more_here) tc_commit(bar(C::B_KVE + x));  // the item's last read of K and V
           if constexpr (!C::PREFETCH) {

@@ -246,6 +246,15 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uin
   return d;
 }
 
+// A descriptor moved by `bytes` (a multiple of 16). The start-address field
+// holds address / 16 in its low 14 bits; every shared-memory address here is
+// below 256 KB, so the sum never carries out of the field and only the low
+// 32-bit word changes (one integer add per operand in the MMA issue loops).
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
+  const uint32_t lo = static_cast<uint32_t>(d) + (bytes >> 4);
+  return (d & 0xFFFFFFFF00000000ull) | lo;
+}
+
 // ----------------------------------------------------------------------------
 // TMEM <-> registers, 32 lanes x 32 consecutive 32-bit columns per warp
 // (thread i of the warp holds lane base+i). The wait is inside the same asm
