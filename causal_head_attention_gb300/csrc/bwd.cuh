@@ -113,27 +113,27 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const PreArgs 
   }
 }
 
-// Variable-length batch: blockIdx.y is the sequence b, and only the rows the
-// backward reads are visited: positions t < 128 * ceil(L_b / 128) (the query
-// tiles that hold real rows). Real rows (t < L_b) get D and LSE2 and a zeroed
-// accumulator row; the rest of their last tile gets D = 0, LSE2 = -inf. Rows
-// past it are never read and not written. Same lane groups as the dense
-// kernel (lpr lanes per row, a power of two).
+// Variable-length batch, one block of the gx blocks (bx = 0 .. gx - 1) given to
+// sequence b: only the rows the backward reads are visited, positions
+// t < 128 * ceil(L_b / 128) (the query tiles that hold real rows). Real rows
+// (t < L_b) get D and LSE2 and a zeroed accumulator row; the rest of their
+// last tile gets D = 0, LSE2 = -inf. Rows past it are never read and not
+// written. Same lane groups as the dense kernel (lpr lanes per row, a power
+// of two); row indices are 32-bit (the caller checks they fit). Run as part of
+// the variable-length backward's prologue launch.
 template <bool F32>
-__global__ void __launch_bounds__(256) attn_bwd_preprocess_varlen_kernel(const PreArgs a) {
-  grid_dep_sync();
+__device__ __forceinline__ void preprocess_varlen_block(const PreArgs& a, int b, unsigned bx, unsigned gx) {
   constexpr int ES = F32 ? 4 : 2;
   constexpr int EPL = 16 / ES;
-  const int b = blockIdx.y;
   int L = __ldg(a.lens + b);
   if (L < 0 || L > a.T) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) atomicExch(a.status, kStatusBadInput);
+    if (threadIdx.x == 0 && bx == 0) atomicExch(a.status, kStatusBadInput);
     L = L < 0 ? 0 : a.T;
   }
   const unsigned lpr = static_cast<unsigned>(a.Dh / EPL);
   const unsigned rows = static_cast<unsigned>((L + 127) / 128 * 128) * a.Hq;  // (t, h) rows of real tiles
-  const unsigned stride = gridDim.x * blockDim.x;
-  for (unsigned i0 = blockIdx.x * blockDim.x; i0 < rows * lpr; i0 += stride) {  // uniform per block
+  const unsigned stride = gx * blockDim.x;
+  for (unsigned i0 = bx * blockDim.x; i0 < rows * lpr; i0 += stride) {  // uniform per block
     const unsigned gid = i0 + threadIdx.x;
     const unsigned row = gid / lpr, part = gid % lpr;
     const bool in = row < rows;

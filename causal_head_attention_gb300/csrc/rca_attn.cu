@@ -570,11 +570,10 @@ rca_status check_varlen(int64_t B, int64_t T) {
 }
 
 // Builds both work lists from the lengths; returns their device pointers.
-rca_status plan_varlen(const int* lens, int64_t B, int64_t Hq, int64_t Hkv, int64_t T, void* ws, const VarlenLayout& V,
-                       cudaStream_t st, const int4** fwd_items, const int** fwd_count, const int4** bwd_items,
-                       const int** bwd_count) {
+rca_status plan_args(rca::VarlenPlanArgs& a, size_t& smem, const int* lens, int64_t B, int64_t Hq, int64_t Hkv,
+                     int64_t T, void* ws, const VarlenLayout& V) {
   char* w = static_cast<char*>(ws);
-  rca::VarlenPlanArgs a{};
+  a = rca::VarlenPlanArgs{};
   a.lens = lens;
   a.fwd_items = reinterpret_cast<int4*>(w + V.fwd_items);
   a.bwd_items = reinterpret_cast<int4*>(w + V.bwd_items);
@@ -586,7 +585,16 @@ rca_status plan_varlen(const int* lens, int64_t B, int64_t Hq, int64_t Hkv, int6
   a.Hkv = int(Hkv);
   a.T = int(T);
   a.n_qt = int((T + 127) / 128);
-  const size_t smem = (2 * size_t(B) + 3 * (size_t(a.n_qt) + 1)) * sizeof(int);
+  smem = (2 * size_t(B) + 3 * (size_t(a.n_qt) + 1)) * sizeof(int);
+  return RCA_OK;
+}
+
+rca_status plan_varlen(const int* lens, int64_t B, int64_t Hq, int64_t Hkv, int64_t T, void* ws, const VarlenLayout& V,
+                       cudaStream_t st, const int4** fwd_items, const int** fwd_count, const int4** bwd_items,
+                       const int** bwd_count) {
+  rca::VarlenPlanArgs a{};
+  size_t smem = 0;
+  RCA_CHECK(plan_args(a, smem, lens, B, Hq, Hkv, T, ws, V));
   launch_dep(rca::varlen_plan_kernel, dim3(1), dim3(rca::kVarlenPlanThreads), smem, st, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch varlen_plan_kernel");
@@ -600,6 +608,55 @@ rca_status plan_varlen(const int* lens, int64_t B, int64_t Hq, int64_t Hkv, int6
 // Zero the rows at or past each sequence's length (and -inf LSE) of x [B, T, H, Dh]
 // and, if given, of x2 of the same shape: one grid column per sequence (and
 // tensor), covering only its padding.
+// The variable-length prologue launch (varlen.cuh): the work lists, the zero
+// fill of the padding rows of x (and x2; lse -inf with x), and with `pre`
+// the backward preprocess, in one launch ahead of the attention kernel. Its
+// preprocess part indexes rows with 32 bits: callers check
+// varlen_pre_fits() first.
+bool varlen_pre_fits(int64_t Hq, int64_t Dh, rca_dtype dt, const WsLayout& L) {
+  return L.Tpad * Hq * (Dh / (dt == RCA_BF16 ? 8 : 4)) < (int64_t(1) << 31);
+}
+rca_status varlen_prologue(const int* lens, int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt,
+                           void* ws, const VarlenLayout& V, void* x, void* x2, float* lse, int64_t H,
+                           const rca::PreArgs* pre, const WsLayout* L, cudaStream_t st, const int4** fwd_items,
+                           const int** fwd_count, const int4** bwd_items, const int** bwd_count) {
+  rca::VarlenPrologue p{};
+  size_t smem = 0;
+  RCA_CHECK(plan_args(p.plan, smem, lens, B, Hq, Hkv, T, ws, V));
+  int sms = 0;
+  RCA_CHECK(sm_count(&sms));
+  const int64_t cap = std::max<int64_t>(1, int64_t(sms) * 8 / B);
+  const int64_t per_seq = T * H * Dh * (dt == RCA_BF16 ? 2 : 4) / 16;  // 16-byte vectors
+  p.zx = x;
+  p.zx2 = x2;
+  p.zlse = lse;
+  p.zH = int(H);
+  p.Dh = int(Dh);
+  p.zgx = int(std::max<int64_t>(1, std::min((per_seq + 1023) / 1024, cap)));
+  int64_t blocks = 1 + int64_t(p.zgx) * B * (x2 ? 2 : 1);
+  if (pre) {
+    p.pre = *pre;
+    const int64_t lpr = Dh / (dt == RCA_BF16 ? 8 : 4);
+    p.pgx = int(std::max<int64_t>(1, std::min((L->Tpad * Hq * lpr + 255) / 256, cap)));
+    blocks += int64_t(p.pgx) * B;
+  }
+  const dim3 grid = dim3(static_cast<unsigned>(blocks));
+  if (dt == RCA_BF16) {
+    if (pre) launch_dep(rca::varlen_prologue_kernel<2, 1>, grid, dim3(256), smem, st, p);
+    else launch_dep(rca::varlen_prologue_kernel<2, 0>, grid, dim3(256), smem, st, p);
+  } else {
+    if (pre) launch_dep(rca::varlen_prologue_kernel<4, 2>, grid, dim3(256), smem, st, p);
+    else launch_dep(rca::varlen_prologue_kernel<4, 0>, grid, dim3(256), smem, st, p);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch varlen_prologue_kernel");
+  *fwd_items = p.plan.fwd_items;
+  *fwd_count = p.plan.fwd_count;
+  *bwd_items = p.plan.bwd_items;
+  *bwd_count = p.plan.bwd_count;
+  return RCA_OK;
+}
+
 rca_status zero_padding(void* x, float* lse, const int* lens, int64_t B, int64_t T, int64_t H, int64_t Dh,
                         rca_dtype dt, cudaStream_t st, void* x2 = nullptr) {
   const int64_t per_seq = T * H * Dh * (dt == RCA_BF16 ? 2 : 4) / 16;  // 16-byte vectors
@@ -636,11 +693,10 @@ rca_status varlen_convert(void* dq, const int* lens, int64_t B, int64_t Hq, int6
   return RCA_OK;
 }
 
-rca_status do_preprocess(const void* out, const float* lse, const void* dout, int64_t B, int64_t Hq, int64_t T,
-                         int64_t Dh, rca_dtype dt, void* ws, const WsLayout& L, cudaStream_t st,
-                         const int* lens = nullptr) {
+rca_status pre_args(rca::PreArgs& a, const void* out, const float* lse, const void* dout, int64_t B, int64_t Hq,
+                    int64_t T, int64_t Dh, void* ws, const WsLayout& L, const int* lens) {
   uint8_t* w = static_cast<uint8_t*>(ws);
-  rca::PreArgs a{};
+  a = rca::PreArgs{};
   a.lens = lens;
   if (lens) RCA_CHECK(status_word(&a.status));
   a.out = out;
@@ -650,22 +706,15 @@ rca_status do_preprocess(const void* out, const float* lse, const void* dout, in
   a.lse2 = reinterpret_cast<float*>(w + L.lse2_off);
   a.dvec = reinterpret_cast<float*>(w + L.d_off);
   a.B = int(B); a.Hq = int(Hq); a.T = int(T); a.Dh = int(Dh); a.Tpad = int(L.Tpad);
+  return RCA_OK;
+}
+
+rca_status do_preprocess(const void* out, const float* lse, const void* dout, int64_t B, int64_t Hq, int64_t T,
+                         int64_t Dh, rca_dtype dt, void* ws, const WsLayout& L, cudaStream_t st,
+                         const int* lens = nullptr) {
+  rca::PreArgs a{};
+  RCA_CHECK(pre_args(a, out, lse, dout, B, Hq, T, Dh, ws, L, lens));
   const int64_t lpr = Dh / (dt == RCA_BF16 ? 8 : 4);
-  if (lens && L.Tpad * Hq * lpr < (int64_t(1) << 31)) {
-    // Variable-length batch: one grid column per sequence, over the rows of
-    // its real tiles only.
-    int sms = 0;
-    RCA_CHECK(sm_count(&sms));
-    const int64_t want = (L.Tpad * Hq * lpr + 255) / 256, cap = std::max<int64_t>(1, int64_t(sms) * 8 / B);
-    const dim3 grid(unsigned(std::max<int64_t>(1, std::min(want, cap))), unsigned(B));
-    if (dt == RCA_BF16)
-      launch_dep(rca::attn_bwd_preprocess_varlen_kernel<false>, dim3(grid), dim3(256), 0, st, a);
-    else
-      launch_dep(rca::attn_bwd_preprocess_varlen_kernel<true>, dim3(grid), dim3(256), 0, st, a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "launch attn_bwd_preprocess_varlen_kernel");
-    return RCA_OK;
-  }
   const int64_t threads = B * L.Tpad * Hq * lpr;
   const unsigned grid = unsigned((threads + 255) / 256);
   const bool narrow = (int64_t(grid) * 256) < (int64_t(1) << 31);  // 32-bit thread indices suffice
@@ -1096,9 +1145,11 @@ rca_status rca_attn_fwd_varlen(const void* q, const void* k, const void* v, cons
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   const int4 *fi = nullptr, *bi = nullptr;
   const int *fc = nullptr, *bc = nullptr;
-  RCA_CHECK(plan_varlen(seq_lens, B, Hq, Hkv, T, workspace, V, st, &fi, &fc, &bi, &bc));
-  RCA_CHECK(do_fwd(q, k, v, B, Hq, Hkv, T, Dh, out, lse, dt, st, 0, 0, seq_lens, fi, fc));
-  return zero_padding(out, lse, seq_lens, B, T, Hq, Dh, dt, st);
+  // Work lists and the zero fill of tiles made only of padding, then the
+  // forward over the listed tiles (which writes its own padding rows too).
+  RCA_CHECK(varlen_prologue(seq_lens, B, Hq, Hkv, T, Dh, dt, workspace, V, out, nullptr, lse, Hq, nullptr, nullptr,
+                            st, &fi, &fc, &bi, &bc));
+  return do_fwd(q, k, v, B, Hq, Hkv, T, Dh, out, lse, dt, st, 0, 0, seq_lens, fi, fc);
   RCA_GUARD_END
 }
 
@@ -1124,6 +1175,18 @@ rca_status rca_attn_bwd_varlen(const void* q, const void* k, const void* v, cons
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   const int4 *fi = nullptr, *bi = nullptr;
   const int *fc = nullptr, *bc = nullptr;
+  if (varlen_pre_fits(Hq, Dh, dt, L)) {
+    // One prologue launch (work lists, dK / dV padding zeroed, preprocess),
+    // the main kernel over the listed items, the dQ conversion.
+    rca::PreArgs pa{};
+    RCA_CHECK(pre_args(pa, out, lse, dout, B, Hq, T, Dh, workspace, L, seq_lens));
+    RCA_CHECK(varlen_prologue(seq_lens, B, Hq, Hkv, T, Dh, dt, workspace, V, dk, dv, nullptr, Hkv, &pa, &L, st, &fi,
+                              &fc, &bi, &bc));
+    RCA_CHECK(do_bwd_main(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, dt, workspace, L, st, nullptr, 0, 0, 0, bi, bc));
+    return varlen_convert(dq, seq_lens, B, Hq, T, Dh, dt, workspace, L, st);
+  }
+  // Rows past 32-bit indexing: separate launches, the dense preprocess
+  // skipping padding rows.
   RCA_CHECK(plan_varlen(seq_lens, B, Hq, Hkv, T, workspace, V, st, &fi, &fc, &bi, &bc));
   RCA_CHECK(do_preprocess(out, lse, dout, B, Hq, T, Dh, dt, workspace, L, st, seq_lens));
   RCA_CHECK(do_bwd_main(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, dt, workspace, L, st, nullptr, 0, 0, 0, bi, bc));

@@ -17,6 +17,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "bwd.cuh"
 #include "tc.cuh"
 
 namespace rca {
@@ -33,11 +34,10 @@ struct VarlenPlanArgs {
   int B, Hq, Hkv, T, n_qt;
 };
 
-// Dynamic shared memory: nq[B], order[B], cnt[n_qt + 1] (#sequences with
-// nq_b > l for level l), fwd_off[n_qt + 1], bwd_off[n_qt + 1].
-__global__ void __launch_bounds__(kVarlenPlanThreads) varlen_plan_kernel(const VarlenPlanArgs a) {
-  grid_dep_sync();
-  extern __shared__ int sm[];
+// Shared memory sm: nq[B], order[B], cnt[n_qt + 1] (#sequences with
+// nq_b > l for level l), fwd_off[n_qt + 1], bwd_off[n_qt + 1]. One block, any
+// number of threads.
+__device__ __forceinline__ void varlen_plan_block(const VarlenPlanArgs& a, int* sm) {
   int* nq = sm;
   int* order = nq + a.B;
   int* cnt = order + a.B;           // cnt[l] = #{b : nq_b > l}, l = 0 .. n_qt
@@ -110,13 +110,39 @@ __global__ void __launch_bounds__(kVarlenPlanThreads) varlen_plan_kernel(const V
   }
 }
 
+__global__ void __launch_bounds__(kVarlenPlanThreads) varlen_plan_kernel(const VarlenPlanArgs a) {
+  grid_dep_sync();
+  extern __shared__ int sm[];
+  varlen_plan_block(a, sm);
+}
+
 // Zero the rows of positions t >= L_b of a [B, T, H, Dh] tensor (storage
-// dtype, ES bytes) and, if lse is given, set lse[b, h, t] = -inf there.
-// blockIdx.y is the sequence b; its padding is one contiguous range of
-// 16-byte vectors, [L_b * vpr, T * vpr) of its slab, so no thread divides to
-// find its row and none touches a real row.
-// blockIdx.z = 1 (when x2 is given) zeroes the padding of x2 instead, a
-// second tensor of the same shape, in the same launch.
+// dtype, ES bytes) and, if lse is given, set lse[b, h, t] = -inf there: block
+// bx of the gx blocks given to sequence b. The padding is one contiguous range
+// of 16-byte vectors, [L_b * vpr, T * vpr) of the sequence's slab, so no
+// thread divides to find its row and none touches a real row.
+template <int ES>
+__device__ __forceinline__ void varlen_zero_block(void* __restrict__ x, float* __restrict__ lse,
+                                                  const int* __restrict__ lens, int T, int H, int Dh, int b,
+                                                  unsigned bx, unsigned gx) {
+  int L = __ldg(lens + b);
+  L = L < 0 ? 0 : (L > T ? T : L);
+  const long long vpr = static_cast<long long>(H) * Dh * ES / 16;  // vectors per position
+  uint4* slab = reinterpret_cast<uint4*>(x) + static_cast<long long>(b) * T * vpr;
+  const long long stride = static_cast<long long>(gx) * blockDim.x;
+  const long long first = static_cast<long long>(bx) * blockDim.x + threadIdx.x;
+  for (long long i = L * vpr + first; i < T * vpr; i += stride) slab[i] = make_uint4(0, 0, 0, 0);
+  if (lse) {
+    const int np = T - L;  // padding positions of each head's LSE row
+    for (long long k = first; k < static_cast<long long>(H) * np; k += stride) {
+      const int h = static_cast<int>(k / np), t = L + static_cast<int>(k - static_cast<long long>(h) * np);
+      lse[(static_cast<long long>(b) * H + h) * T + t] = -INFINITY;
+    }
+  }
+}
+
+// The same as a kernel: blockIdx.y is the sequence; blockIdx.z = 1 (when x2 is
+// given) zeroes the padding of x2 instead, a second tensor of the same shape.
 template <int ES>
 __global__ void __launch_bounds__(256)
     varlen_zero_kernel(void* __restrict__ x, void* __restrict__ x2, float* __restrict__ lse,
@@ -126,20 +152,51 @@ __global__ void __launch_bounds__(256)
     x = x2;
     lse = nullptr;
   }
-  const int b = blockIdx.y;
-  int L = __ldg(lens + b);
-  L = L < 0 ? 0 : (L > T ? T : L);
-  const long long vpr = static_cast<long long>(H) * Dh * ES / 16;  // vectors per position
-  uint4* slab = reinterpret_cast<uint4*>(x) + static_cast<long long>(b) * T * vpr;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  const long long first = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (long long i = L * vpr + first; i < T * vpr; i += stride) slab[i] = make_uint4(0, 0, 0, 0);
-  if (lse) {
-    const int np = T - L;  // padding positions of each head's LSE row
-    for (long long k = first; k < static_cast<long long>(H) * np; k += stride) {
-      const int h = static_cast<int>(k / np), t = L + static_cast<int>(k - static_cast<long long>(h) * np);
-      lse[(static_cast<long long>(b) * H + h) * T + t] = -INFINITY;
-    }
+  varlen_zero_block<ES>(x, lse, lens, T, H, Dh, blockIdx.y, blockIdx.x, gridDim.x);
+}
+
+// One launch ahead of a variable-length call's attention kernel, 256 threads a
+// block: block 0 builds the work lists; the next nz = zgx * B * (x2 ? 2 : 1)
+// blocks zero the padding rows of x (and x2; LSE -inf with x) as above, zgx
+// blocks a sequence; the last pgx * B blocks (backward only) run the
+// preprocess over the rows of real tiles, pgx blocks a sequence. The three
+// parts touch disjoint memory and none reads what another writes, so they
+// share one launch; the attention kernel after it waits for all of it
+// (programmatic launch: its griddepcontrol.wait).
+struct VarlenPrologue {
+  VarlenPlanArgs plan;
+  void* zx;
+  void* zx2;
+  float* zlse;
+  int zH, Dh, zgx;
+  PreArgs pre;
+  int pgx;  // 0: no preprocess part
+};
+
+template <int ES, int PRE>  // PRE: 0 none, 1 bf16 storage, 2 fp32 storage
+__global__ void __launch_bounds__(256) varlen_prologue_kernel(const VarlenPrologue p) {
+  grid_dep_sync();
+  extern __shared__ int sm[];
+  unsigned blk = blockIdx.x;
+  if (blk == 0) {
+    varlen_plan_block(p.plan, sm);
+    return;
+  }
+  blk -= 1;
+  const unsigned B = static_cast<unsigned>(p.plan.B);
+  const unsigned nz = static_cast<unsigned>(p.zgx) * B * (p.zx2 ? 2u : 1u);
+  if (blk < nz) {
+    const unsigned per = static_cast<unsigned>(p.zgx) * B;
+    const bool second = blk >= per;
+    const unsigned r = second ? blk - per : blk;
+    varlen_zero_block<ES>(second ? p.zx2 : p.zx, second ? nullptr : p.zlse, p.plan.lens, p.plan.T, p.zH, p.Dh,
+                          static_cast<int>(r / p.zgx), r % p.zgx, p.zgx);
+    return;
+  }
+  if constexpr (PRE != 0) {
+    blk -= nz;
+    const unsigned pg = static_cast<unsigned>(p.pgx);
+    preprocess_varlen_block<PRE == 2>(p.pre, static_cast<int>(blk / pg), blk % pg, pg);
   }
 }
 
