@@ -66,7 +66,7 @@ def peaks():
 # device helpers and its host launcher).
 KERNEL_SOURCES = {
     "fwd": ("fwd.cuh", "tc.cuh", "rca_attn.cu"),
-    "bwd_main": ("bwd.cuh", "tc.cuh", "rca_attn.cu"),
+    "bwd_main": ("bwd.cuh", "bwd_sub.cuh", "tc.cuh", "rca_attn.cu"),
     "bwd_preprocess": ("bwd.cuh", "tc.cuh", "rca_attn.cu"),
     "bwd_dq_convert": ("bwd.cuh", "tc.cuh", "rca_attn.cu"),
     "decode": ("decode.cu", "decode.h", "tc.cuh"),

@@ -15,6 +15,7 @@
 
 #include "rca_attn.h"
 #include "bwd.cuh"
+#include "bwd_sub.cuh"
 #include "decode.h"
 #include "fwd.cuh"
 #include "materialized.h"
@@ -413,11 +414,72 @@ rca_status launch_split(const void* src, void* hi, void* lo, size_t n, int64_t r
   return RCA_OK;
 }
 
+// bf16 storage, head width 128: the 64-row query sub-tile kernel (bwd_sub.cuh),
+// one CTA per work item.
+rca_status launch_bwd_sub(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
+                          int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, void* ws, const WsLayout& L,
+                          cudaStream_t st, int* status_override, int64_t qs, int64_t kvs, int64_t dkvs,
+                          const int4* items, const int* n_items_dev) {
+  using C = rca::BwdSubCfg;
+  static std::atomic<unsigned long long> smem_set[2] = {};
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  rca::BwdMaps maps;
+  RCA_CHECK(make_map(&maps.q[0], q, B, T, Hq, Dh, false, "q", 64, qs));
+  RCA_CHECK(make_map(&maps.k[0], k, B, T, Hkv, Dh, false, "k", 128, kvs));
+  RCA_CHECK(make_map(&maps.v[0], v, B, T, Hkv, Dh, false, "v", 128, kvs));
+  RCA_CHECK(make_map(&maps.dO[0], dout, B, T, Hq, Dh, false, "dout", 64));
+  maps.q[1] = maps.q[0];
+  maps.k[1] = maps.k[0];
+  maps.v[1] = maps.v[0];
+  maps.dO[1] = maps.dO[0];
+  RCA_CHECK(make_map(&maps.dq, w + L.dq_off, B, T, Hq, Dh, true, "dq accumulator", 32));
+  int* status = status_override;
+  if (!status) RCA_CHECK(status_word(&status));
+  const int li = items ? 1 : 0;
+  auto kern = items ? rca::attn_bwd_sub_kernel<true> : rca::attn_bwd_sub_kernel<false>;
+  cudaError_t e = ensure_smem(kern, C::SMEM_BYTES, smem_set[li]);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd sub-tile)");
+  static std::atomic<int> launch_regs[2] = {};
+  if (launch_regs[li].load(std::memory_order_acquire) == 0) {
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(bwd sub-tile)");
+    launch_regs[li].store(fa.numRegs, std::memory_order_release);
+  }
+  if (launch_regs[li].load(std::memory_order_acquire) != C::LAUNCH_REGS)
+    return fail(RCA_ERR_UNSUPPORTED, "backward kernel built with %d registers per thread, its warpgroup split needs %d",
+                launch_regs[li].load(), C::LAUNCH_REGS);
+  rca::BwdArgs a{};
+  a.dk = dk;
+  a.dv = dv;
+  a.dkv_row = dkvs;
+  a.items = items;
+  a.n_items_dev = n_items_dev;
+  a.lse2 = reinterpret_cast<const float*>(w + L.lse2_off);
+  a.dvec = reinterpret_cast<const float*>(w + L.d_off);
+  a.status = status;
+  a.timeout_ns = g_timeout_ns.load();
+  a.B = int(B); a.Hq = int(Hq); a.Hkv = int(Hkv); a.T = int(T); a.Dh = int(Dh);
+  a.group = int(Hq / Hkv);
+  a.n_t = int((T + 127) / 128);
+  a.Tpad = int(L.Tpad);
+  a.scale = float(1.0 / std::sqrt(double(Dh)));
+  a.scale_log2 = float(1.4426950408889634 / std::sqrt(double(Dh)));
+  a.n_items = int(int64_t(a.n_t) * B * Hkv);
+  launch_dep(kern, dim3(unsigned(a.n_items)), dim3(C::NTHREADS), C::SMEM_BYTES, st, maps, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch attn_bwd_sub_kernel");
+  return RCA_OK;
+}
+
 template <bool HL, int DHB>
 rca_status launch_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
                            int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, void* ws,
                            const WsLayout& L, cudaStream_t st, int* status_override, int64_t qs, int64_t kvs,
                            int64_t dkvs, const int4* items, const int* n_items_dev) {
+  if constexpr (!HL && DHB == 128)
+    return launch_bwd_sub(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, ws, L, st, status_override, qs, kvs, dkvs, items,
+                          n_items_dev);
   using C = rca::BwdCfg<HL, DHB>;
   static std::atomic<unsigned long long> smem_set[2] = {};
   uint8_t* w = static_cast<uint8_t*>(ws);
