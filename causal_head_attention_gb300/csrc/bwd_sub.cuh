@@ -9,8 +9,10 @@
 // waited for its loads. Here an iteration takes 64 query rows: a Q + dO stage
 // is 32 KB and two of them fit, so the next sub-tile loads while the current
 // one is computed. dQ is computed transposed, dQ^T = K^T dS^T (M = head width,
-// N = 64 queries), so it has TMEM columns of its own:
-//   S^T [0, 64)  dP^T [64, 128)  dV [128, 256)  dK [256, 384)  dQ^T [384, 448)
+// N = 64 queries), so it has TMEM columns of its own, and the last 64 columns
+// hold the item's K tile, copied there once (tcgen05.cp), so that S^T reads
+// its A operand from TMEM instead of shared memory every iteration:
+//   S^T [0, 64)  dP^T [64, 128)  dV [128, 256)  dK [256, 384)  dQ^T [384, 448)  K [448, 512)
 // Products per iteration (M = 128 each): S^T = K Q^T and dP^T = V dO^T
 // (N = 64 queries, K = head width), dV += P^T dO and dK += dS^T Q (N = head
 // width, K = 64 queries), dQ^T = K^T dS^T (N = 64 queries, K = 128 keys; A and
@@ -44,7 +46,7 @@ struct BwdSubCfg {
   static constexpr int BAR_BYTES = 1024;
   static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static constexpr int TM_S = 0, TM_DP = 64, TM_DV = 128, TM_DK = 256, TM_DQ = 384;
+  static constexpr int TM_S = 0, TM_DP = 64, TM_DV = 128, TM_DK = 256, TM_DQ = 384, TM_K = 448;
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_T = make_idesc(false, 128, 64, false, false);   // S^T, dP^T
   static constexpr uint32_t IDESC_KV = make_idesc(false, 128, 128, false, true);  // dV, dK
@@ -177,7 +179,7 @@ __global__ void __launch_bounds__(512, 1)
    } else if (warp == 13) {
     // ---------------- tcgen05 MMA issuer (one elected thread) ----------------
     if (elect_one()) {
-      const uint64_t k_km = make_sdesc(sbase + C::OFF_K, 16, 1024);            // K: A of S^T
+      const uint64_t k_km = make_sdesc(sbase + C::OFF_K, 16, 1024);            // K: copied to TMEM (A of S^T)
       const uint64_t v_km = make_sdesc(sbase + C::OFF_V, 16, 1024);            // V: A of dP^T
       const uint64_t k_mn = make_sdesc(sbase + C::OFF_K, C::PANEL, 1024);      // K^T: A of dQ^T (MN-major)
       const uint64_t q_km = make_sdesc(stage(0), 16, 1024);                    // Q: B of S^T
@@ -191,8 +193,8 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t so = (it2 % C::NQS) * C::STAGE_BYTES;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint32_t ko = (k / 4) * C::PANEL + (k % 4) * 32, qo = so + (k / 4) * C::QPANEL + (k % 4) * 32;
-          mma_ss<false>(tmem + C::TM_S, desc_add(k_km, ko), desc_add(q_km, qo), C::IDESC_T, k > 0 ? 1u : 0u);
+          const uint32_t qo = so + (k / 4) * C::QPANEL + (k % 4) * 32;
+          mma_ts(tmem + C::TM_S, tmem + C::TM_K + 8 * k, desc_add(q_km, qo), C::IDESC_T, k > 0 ? 1u : 0u);
         }
         tc_commit(bar(C::B_SR));
 #pragma unroll
@@ -205,6 +207,10 @@ __global__ void __launch_bounds__(512, 1)
       bool ok = mbar_wait(bar(C::B_KVF), 0, w) && mbar_wait(bar(C::B_QF), 0, w);
       if (ok) {
         tc_fence_after();
+        // K into TMEM: eight K = 16 slices of the K-major tile.
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          tmem_cp_128x256b(tmem + C::TM_K + 8 * k, desc_add(k_km, (k / 4) * C::PANEL + (k % 4) * 32));
         issue_s_dp(0);
       }
       for (int it = 0; ok && it < n_it; ++it) {

@@ -223,6 +223,16 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// Shared memory -> TMEM copy of a 128-row x 32-byte block (128 lanes x 8
+// 32-bit columns) described by a shared-memory matrix descriptor: with a
+// K-major operand descriptor it lays out one K = 16 slice of a bf16 A operand
+// the way tcgen05.mma reads A from TMEM (row = lane, element pairs in
+// consecutive columns). Asynchronous, ordered before the issuing thread's
+// later tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Instruction descriptor for kind::f16 (bf16 operands) / kind::tf32 with an
 // fp32 accumulator. a_mn / b_mn select MN-major (1) or K-major (0) operands.
 __host__ __device__ constexpr uint32_t make_idesc(bool tf32, int M, int N, bool a_mn, bool b_mn) {
