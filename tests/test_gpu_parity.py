@@ -50,6 +50,11 @@ SMALL = [
     ("bf16_t128", 1, 2, 2, 128, 128, "bf16"),
     ("bf16_t129", 1, 2, 2, 129, 64, "bf16"),
     ("bf16_gqa8", 1, 8, 1, 260, 64, "bf16"),
+    # head width 128 (64-row query sub-tiles): one row; a length ending just inside the second
+    # sub-tile (group of 2); a second tile whose second sub-tile is partly real
+    ("bf16_dh128_t1", 1, 2, 2, 1, 128, "bf16"),
+    ("bf16_dh128_t65", 1, 2, 1, 65, 128, "bf16"),
+    ("bf16_dh128_t200", 2, 2, 2, 200, 128, "bf16"),
 ]
 
 

@@ -39,6 +39,9 @@ CASES = [
     # name, B, Hq, Hkv, T, Dh, dtype, lens
     ("vl_bf16_dh64_gqa", 4, 4, 2, 300, 64, "bf16", [300, 129, 1, 0]),
     ("vl_bf16_dh128", 3, 2, 2, 257, 128, "bf16", [128, 256, 200]),
+    # head width 128 with a group of 4: the 64-row sub-tile backward over a planned work list
+    # (a length ending inside the first and inside the second half of a 128-row tile)
+    ("vl_bf16_dh128_gqa", 3, 8, 2, 600, 128, "bf16", [600, 129, 65]),
     ("vl_bf16_dh32", 2, 4, 1, 130, 32, "bf16", [127, 65]),
     ("vl_fp32_dh64", 3, 2, 2, 200, 64, "fp32", [200, 77, 128]),
     ("vl_fp32_dh16_gqa", 2, 4, 2, 140, 16, "fp32", [3, 140]),
