@@ -27,6 +27,8 @@
 //                               for the main kernel (see BwdCfg).
 #pragma once
 
+#include <type_traits>
+
 #include "tc.cuh"
 
 namespace rca {
@@ -44,72 +46,129 @@ struct PreArgs {
   const int* lens;  // per-sequence lengths (right padding), or null
   int* status;
   int B, Hq, T, Dh, Tpad;
+  int lg_lpr;     // log2 of the 16-byte segments per row (Dh * element size / 16)
+  uint32_t hq_m;  // n / Hq = (umulhi(hq_m, n) + n) >> hq_l for n < 2^31
+  int hq_l;
+  int bpb;        // dense kernel: blocks per batch entry
 };
 
-// A group of LPR consecutive lanes handles one (b, t, h) row of Dh elements,
-// each lane 16 bytes, so every load instruction is fully coalesced. IT is the
-// index type of the row decomposition: 32-bit whenever every thread index
-// fits (the divisions are then far cheaper), 64-bit otherwise.
-template <bool F32, typename IT>
+// Segments (16 bytes of O and of dO) per thread in the dense kernel.
+constexpr int kPreSegs = 1;
+
+// Row r = t * Hq + h of one batch entry split into (t, h). For r < 2^31 the
+// quotient is a multiply-high by a constant the host derives from Hq
+// (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994); the sum below stays under 2^32 there.
+__device__ __forceinline__ void pre_split_row(const PreArgs& a, uint32_t r, int& t, int& h) {
+  const uint32_t q = (__umulhi(a.hq_m, r) + r) >> a.hq_l;
+  t = static_cast<int>(q);
+  h = static_cast<int>(r - q * static_cast<uint32_t>(a.Hq));
+}
+__device__ __forceinline__ void pre_split_row(const PreArgs& a, unsigned long long r, int& t, int& h) {
+  t = static_cast<int>(r / static_cast<unsigned>(a.Hq));
+  h = static_cast<int>(r - static_cast<unsigned long long>(t) * a.Hq);
+}
+
+// The share of rowsum(dO * O) held in one 16-byte segment of each.
+template <bool F32>
+__device__ __forceinline__ float pre_dot(const uint4 o, const uint4 g) {
+  const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+  const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (F32) {
+      acc = fmaf(__uint_as_float(ow[i]), __uint_as_float(gw[i]), acc);
+    } else {
+      const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[i]));
+      const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[i]));
+      acc = fmaf(of.x, gf.x, acc);
+      acc = fmaf(of.y, gf.y, acc);
+    }
+  }
+  return acc;
+}
+
+// -D and base-2 -LSE of row (b, t, h); a padding row gets 0 and -inf, which
+// keeps it out of the backward (its recomputed probabilities are exactly 0).
+__device__ __forceinline__ void pre_write_row(const PreArgs& a, int b, int t, int h, bool real, float acc) {
+  const size_t so = (static_cast<size_t>(b) * a.Hq + h) * a.Tpad + t;
+  a.dvec[so] = real ? -acc : 0.f;
+  a.lse2[so] = real ? -(a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.T + t] * 1.4426950408889634f) : -INFINITY;
+}
+
+// Dense preprocess. The rows of batch entry b, r = t * Hq + h for t < Tpad,
+// are 2^lg_lpr consecutive 16-byte segments each, and segment s of the entry
+// sits at 16-byte index s of its O and dO rows (contiguous [T, Hq, Dh]). Each
+// block takes bpb-th of one entry: kPreSegs * 256 consecutive segments, one
+// per thread per 256, all loads issued before any arithmetic. The lanes of a
+// row are a power-of-two group of one warp, so its sum is a shuffle tree; the
+// first lane of the row splits r into (t, h) and writes D and LSE2. Rows at
+// or past T (or past the sequence's length) are padding: not read, their
+// accumulator rows not zeroed (the conversion writes those dQ rows as zeros).
+// WIDE: 64-bit segment indices (an entry with 2^31 or more segments).
+template <bool F32, bool WIDE>
 __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const PreArgs a) {
   grid_dep_sync();
+  using IT = typename std::conditional<WIDE, unsigned long long, uint32_t>::type;
   constexpr int ES = F32 ? 4 : 2;
-  constexpr int EPL = 16 / ES;  // elements per lane
-  const unsigned lpr = static_cast<unsigned>(a.Dh / EPL);  // lanes per row: power of two in [2, 32]
-  const IT gid = static_cast<IT>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const IT rows = static_cast<IT>(a.B) * a.Tpad * a.Hq;
-  const IT row = gid / lpr;
-  const int part = static_cast<int>(gid % lpr);
-  const bool in = row < rows;
-  int b = 0, t = 0, h = 0;
-  if (in) {
-    h = static_cast<int>(row % static_cast<IT>(a.Hq));
-    const IT bt = row / static_cast<IT>(a.Hq);
-    t = static_cast<int>(bt % static_cast<IT>(a.Tpad));
-    b = static_cast<int>(bt / static_cast<IT>(a.Tpad));
-  }
-  const bool live = in && t < a.T;
-  // A padding row of a variable-length batch is kept out of the backward:
-  // LSE2 = -inf makes its recomputed probabilities exactly 0, and D = 0.
-  bool real = live;
-  if (live && a.lens) {
+  constexpr int Z4 = 16 / ES / 4;  // float4 groups of the accumulator per segment
+  constexpr int U = kPreSegs;
+  const int lg = a.lg_lpr;
+  const IT pmask = (IT(1) << lg) - 1;
+  const int b = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.bpb));
+  const IT blk = blockIdx.x - static_cast<unsigned>(b) * static_cast<unsigned>(a.bpb);
+  const IT nseg = (static_cast<IT>(a.Tpad) * static_cast<IT>(a.Hq)) << lg;
+  IT real_rows = static_cast<IT>(a.T) * static_cast<IT>(a.Hq);
+  if (a.lens) {
     int L = __ldg(a.lens + b);
     if (L < 0 || L > a.T) {
-      atomicExch(a.status, kStatusBadInput);
+      if (threadIdx.x == 0) atomicExch(a.status, kStatusBadInput);
       L = L < 0 ? 0 : a.T;
     }
-    real = t < L;
+    real_rows = static_cast<IT>(L) * static_cast<IT>(a.Hq);
   }
-  float acc = 0.f;
-  // Padding rows of a variable-length batch are neither read nor zeroed in
-  // the accumulator: their dQ rows are written as zeros by the conversion.
-  if (real) {
-    const size_t off = ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * a.Dh + part * EPL;
-    const uint4 o = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.out) + off * ES);
-    const uint4 g = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.dout) + off * ES);
-    const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
-    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+  const size_t seg0 = static_cast<size_t>(b) * a.T * a.Hq << lg;  // the entry's first segment
+  const uint4* ob = reinterpret_cast<const uint4*>(a.out) + seg0;
+  const uint4* gb = reinterpret_cast<const uint4*>(a.dout) + seg0;
+  float4* zb = reinterpret_cast<float4*>(a.dq_acc) + seg0 * Z4;
+  const IT s0 = blk * static_cast<IT>(256 * U) + threadIdx.x;
+
+  uint4 o[U], g[U];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if constexpr (F32) {
-        acc = fmaf(__uint_as_float(ow[i]), __uint_as_float(gw[i]), acc);
-      } else {
-        const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[i]));
-        const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[i]));
-        acc = fmaf(of.x, gf.x, acc);
-        acc = fmaf(of.y, gf.y, acc);
-      }
+  for (int k = 0; k < U; ++k) {
+    const IT s = s0 + static_cast<IT>(k * 256);
+    if (s < nseg && (s >> lg) < real_rows) {
+      o[k] = ob[s];
+      g[k] = gb[s];
+    } else {
+      o[k] = make_uint4(0u, 0u, 0u, 0u);
+      g[k] = o[k];
     }
-    float4* z = reinterpret_cast<float4*>(a.dq_acc + off);
-#pragma unroll
-    for (int i = 0; i < EPL / 4; ++i) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  for (int o = lpr >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, lpr);
-  if (in && part == 0) {
-    const size_t so = (static_cast<size_t>(b) * a.Hq + h) * a.Tpad + t;
-    a.dvec[so] = real ? -acc : 0.f;
-    a.lse2[so] = real ? -(a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.T + t] * 1.4426950408889634f)
-                      : -INFINITY;
+  float acc[U];
+#pragma unroll
+  for (int k = 0; k < U; ++k) {
+    const IT s = s0 + static_cast<IT>(k * 256);
+    acc[k] = pre_dot<F32>(o[k], g[k]);
+    if (s < nseg && (s >> lg) < real_rows) {
+#pragma unroll
+      for (int z = 0; z < Z4; ++z) zb[s * Z4 + z] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  const int lpr = 1 << lg;
+#pragma unroll
+  for (int k = 0; k < U; ++k)
+    for (int x = lpr >> 1; x > 0; x >>= 1) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], x, lpr);
+#pragma unroll
+  for (int k = 0; k < U; ++k) {
+    const IT s = s0 + static_cast<IT>(k * 256);
+    if (s < nseg && (s & pmask) == 0) {
+      const IT r = s >> lg;
+      int t, h;
+      pre_split_row(a, r, t, h);
+      pre_write_row(a, b, t, h, r < real_rows, acc[k]);
+    }
   }
 }
 
@@ -118,55 +177,44 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const PreArgs 
 // t < 128 * ceil(L_b / 128) (the query tiles that hold real rows). Real rows
 // (t < L_b) get D and LSE2 and a zeroed accumulator row; the rest of their
 // last tile gets D = 0, LSE2 = -inf. Rows past it are never read and not
-// written. Same lane groups as the dense kernel (lpr lanes per row, a power
-// of two); row indices are 32-bit (the caller checks they fit). Run as part of
-// the variable-length backward's prologue launch.
+// written. Segments as in the dense kernel, one per thread per pass; indices
+// are 32-bit (the caller checks they fit). Run as part of the
+// variable-length backward's prologue launch.
 template <bool F32>
 __device__ __forceinline__ void preprocess_varlen_block(const PreArgs& a, int b, unsigned bx, unsigned gx) {
   constexpr int ES = F32 ? 4 : 2;
-  constexpr int EPL = 16 / ES;
+  constexpr int Z4 = 16 / ES / 4;
   int L = __ldg(a.lens + b);
   if (L < 0 || L > a.T) {
     if (threadIdx.x == 0 && bx == 0) atomicExch(a.status, kStatusBadInput);
     L = L < 0 ? 0 : a.T;
   }
-  const unsigned lpr = static_cast<unsigned>(a.Dh / EPL);
+  const int lg = a.lg_lpr;
+  const unsigned pmask = (1u << lg) - 1u;
   const unsigned rows = static_cast<unsigned>((L + 127) / 128 * 128) * a.Hq;  // (t, h) rows of real tiles
+  const unsigned real_rows = static_cast<unsigned>(L) * a.Hq;
+  const size_t seg0 = static_cast<size_t>(b) * a.T * a.Hq << lg;
+  const uint4* ob = reinterpret_cast<const uint4*>(a.out) + seg0;
+  const uint4* gb = reinterpret_cast<const uint4*>(a.dout) + seg0;
+  float4* zb = reinterpret_cast<float4*>(a.dq_acc) + seg0 * Z4;
   const unsigned stride = gx * blockDim.x;
-  for (unsigned i0 = bx * blockDim.x; i0 < rows * lpr; i0 += stride) {  // uniform per block
-    const unsigned gid = i0 + threadIdx.x;
-    const unsigned row = gid / lpr, part = gid % lpr;
-    const bool in = row < rows;
-    const int t = static_cast<int>(row / a.Hq), h = static_cast<int>(row % a.Hq);
-    const bool real = in && t < L;
+  const int lpr = 1 << lg;
+  for (unsigned i0 = bx * blockDim.x; i0 < (rows << lg); i0 += stride) {  // uniform per block
+    const unsigned s = i0 + threadIdx.x;
+    const unsigned r = s >> lg;
+    const bool in = r < rows;
+    const bool real = r < real_rows;
     float acc = 0.f;
     if (real) {
-      const size_t off = ((static_cast<size_t>(b) * a.T + t) * a.Hq + h) * a.Dh + part * EPL;
-      const uint4 o = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.out) + off * ES);
-      const uint4 g = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.dout) + off * ES);
-      const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
-      const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+      acc = pre_dot<F32>(ob[s], gb[s]);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if constexpr (F32) {
-          acc = fmaf(__uint_as_float(ow[i]), __uint_as_float(gw[i]), acc);
-        } else {
-          const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[i]));
-          const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[i]));
-          acc = fmaf(of.x, gf.x, acc);
-          acc = fmaf(of.y, gf.y, acc);
-        }
-      }
-      float4* z = reinterpret_cast<float4*>(a.dq_acc + off);
-#pragma unroll
-      for (int i = 0; i < EPL / 4; ++i) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int z = 0; z < Z4; ++z) zb[static_cast<size_t>(s) * Z4 + z] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    for (unsigned o = lpr >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, lpr);
-    if (in && part == 0) {
-      const size_t so = (static_cast<size_t>(b) * a.Hq + h) * a.Tpad + t;
-      a.dvec[so] = real ? -acc : 0.f;
-      a.lse2[so] = real ? -(a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.T + t] * 1.4426950408889634f)
-                        : -INFINITY;
+    for (int x = lpr >> 1; x > 0; x >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, x, lpr);
+    if (in && (s & pmask) == 0) {
+      int t, h;
+      pre_split_row(a, r, t, h);
+      pre_write_row(a, b, t, h, real, acc);
     }
   }
 }

@@ -756,7 +756,7 @@ rca_status varlen_convert(void* dq, const int* lens, int64_t B, int64_t Hq, int6
 }
 
 rca_status pre_args(rca::PreArgs& a, const void* out, const float* lse, const void* dout, int64_t B, int64_t Hq,
-                    int64_t T, int64_t Dh, void* ws, const WsLayout& L, const int* lens) {
+                    int64_t T, int64_t Dh, rca_dtype dt, void* ws, const WsLayout& L, const int* lens) {
   uint8_t* w = static_cast<uint8_t*>(ws);
   a = rca::PreArgs{};
   a.lens = lens;
@@ -768,6 +768,15 @@ rca_status pre_args(rca::PreArgs& a, const void* out, const float* lse, const vo
   a.lse2 = reinterpret_cast<float*>(w + L.lse2_off);
   a.dvec = reinterpret_cast<float*>(w + L.d_off);
   a.B = int(B); a.Hq = int(Hq); a.T = int(T); a.Dh = int(Dh); a.Tpad = int(L.Tpad);
+  const int64_t lpr = Dh / (dt == RCA_BF16 ? 8 : 4);  // 16-byte segments per row, a power of two
+  a.lg_lpr = 0;
+  while ((int64_t(1) << a.lg_lpr) < lpr) ++a.lg_lpr;
+  // n / Hq for n < 2^31 as a multiply-high (Granlund and Montgomery, 1994):
+  // l = ceil(log2 Hq), m = floor(2^32 (2^l - Hq) / Hq) + 1 (below 2^32).
+  int l = 0;
+  while ((int64_t(1) << l) < Hq) ++l;
+  a.hq_l = l;
+  a.hq_m = uint32_t(((uint64_t(1) << 32) * ((uint64_t(1) << l) - uint64_t(Hq))) / uint64_t(Hq) + 1);
   return RCA_OK;
 }
 
@@ -775,17 +784,21 @@ rca_status do_preprocess(const void* out, const float* lse, const void* dout, in
                          int64_t Dh, rca_dtype dt, void* ws, const WsLayout& L, cudaStream_t st,
                          const int* lens = nullptr) {
   rca::PreArgs a{};
-  RCA_CHECK(pre_args(a, out, lse, dout, B, Hq, T, Dh, ws, L, lens));
-  const int64_t lpr = Dh / (dt == RCA_BF16 ? 8 : 4);
-  const int64_t threads = B * L.Tpad * Hq * lpr;
-  const unsigned grid = unsigned((threads + 255) / 256);
-  const bool narrow = (int64_t(grid) * 256) < (int64_t(1) << 31);  // 32-bit thread indices suffice
+  RCA_CHECK(pre_args(a, out, lse, dout, B, Hq, T, Dh, dt, ws, L, lens));
+  const int64_t seg = (L.Tpad * Hq) << a.lg_lpr;  // 16-byte segments of one batch entry
+  const int64_t per_block = 256 * rca::kPreSegs;
+  const int64_t bpb = (seg + per_block - 1) / per_block;
+  if (bpb * B >= (int64_t(1) << 31))
+    return fail(RCA_ERR_UNSUPPORTED, "rca_attn_bwd_preprocess: B x T x Hq x Dh too large for one launch");
+  a.bpb = int(bpb);
+  const dim3 grid = dim3(static_cast<unsigned>(bpb * B));
+  const bool narrow = seg < (int64_t(1) << 31);  // 32-bit segment indices within an entry suffice
   if (dt == RCA_BF16) {
-    if (narrow) launch_dep(rca::attn_bwd_preprocess_kernel<false, uint32_t>, dim3(grid), dim3(256), 0, st, a);
-    else launch_dep(rca::attn_bwd_preprocess_kernel<false, unsigned long long>, dim3(grid), dim3(256), 0, st, a);
+    if (narrow) launch_dep(rca::attn_bwd_preprocess_kernel<false, false>, grid, dim3(256), 0, st, a);
+    else launch_dep(rca::attn_bwd_preprocess_kernel<false, true>, grid, dim3(256), 0, st, a);
   } else {
-    if (narrow) launch_dep(rca::attn_bwd_preprocess_kernel<true, uint32_t>, dim3(grid), dim3(256), 0, st, a);
-    else launch_dep(rca::attn_bwd_preprocess_kernel<true, unsigned long long>, dim3(grid), dim3(256), 0, st, a);
+    if (narrow) launch_dep(rca::attn_bwd_preprocess_kernel<true, false>, grid, dim3(256), 0, st, a);
+    else launch_dep(rca::attn_bwd_preprocess_kernel<true, true>, grid, dim3(256), 0, st, a);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch attn_bwd_preprocess_kernel");
@@ -1241,7 +1254,7 @@ rca_status rca_attn_bwd_varlen(const void* q, const void* k, const void* v, cons
     // One prologue launch (work lists, dK / dV padding zeroed, preprocess),
     // the main kernel over the listed items, the dQ conversion.
     rca::PreArgs pa{};
-    RCA_CHECK(pre_args(pa, out, lse, dout, B, Hq, T, Dh, workspace, L, seq_lens));
+    RCA_CHECK(pre_args(pa, out, lse, dout, B, Hq, T, Dh, dt, workspace, L, seq_lens));
     RCA_CHECK(varlen_prologue(seq_lens, B, Hq, Hkv, T, Dh, dt, workspace, V, dk, dv, nullptr, Hkv, &pa, &L, st, &fi,
                               &fc, &bi, &bc));
     RCA_CHECK(do_bwd_main(q, k, v, dout, dk, dv, B, Hq, Hkv, T, Dh, dt, workspace, L, st, nullptr, 0, 0, 0, bi, bc));
