@@ -53,7 +53,9 @@ def build(force: bool = False, verbose: bool = False, extra: tuple = ()) -> str:
     from concurrent.futures import ThreadPoolExecutor
 
     nvcc = nvcc_path()
-    common = [nvcc, ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}", *extra]
+    # Hidden visibility: only the calls include/rca_attn.h marks RCA_API are exported.
+    common = [nvcc, ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
+              f"-I{INCLUDE}", *extra]
     objs = [os.path.join(PKG, u[:-3] + ".o") for u in UNITS]
     cmds = [common + ["-c", "-o", o, os.path.join(CSRC, u)] for u, o in zip(UNITS, objs)]
     with ThreadPoolExecutor(len(cmds)) as ex:

@@ -69,6 +69,15 @@
 #include <stddef.h>
 #include <stdint.h>
 
+/* The library is built with hidden symbol visibility; the calls declared here
+ * are its only exported symbols, so two copies of it (or a program that
+ * defines the same internal names) can share a process without interfering. */
+#if defined(__GNUC__) && !defined(RCA_API)
+#define RCA_API __attribute__((visibility("default")))
+#elif !defined(RCA_API)
+#define RCA_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -88,18 +97,18 @@ typedef enum { RCA_F32_TF32 = 0, RCA_BF16 = 1 } rca_dtype;
 
 /* ABI version: upper 16 bits major, lower 16 bits minor (0x00010007 = 1.7). */
 #define RCA_ABI_VERSION 0x00010007u
-uint32_t rca_abi_version(void);
+RCA_API uint32_t rca_abi_version(void);
 
 /* Message of the last failed call on this thread ("" if none). The pointer is
  * owned by the library and valid until the next call on this thread. */
-const char* rca_last_error(void);
+RCA_API const char* rca_last_error(void);
 
 /*
  * Forward. Writes out [B,T,Hq,Dh] (storage dtype) and lse [B,Hq,T] (float32).
  * Requires B, Hq, Hkv, T >= 1 (T = 0 would be a fully masked row: rejected),
  * Hq % Hkv == 0, and 16-byte aligned q, k, v, out, lse.
  */
-rca_status rca_attn_fwd(const void* q, const void* k, const void* v,
+RCA_API rca_status rca_attn_fwd(const void* q, const void* k, const void* v,
                         int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
                         void* out, float* lse, rca_dtype dt, void* cuda_stream);
 
@@ -109,7 +118,7 @@ rca_status rca_attn_fwd(const void* q, const void* k, const void* v,
  * T rounded up to 128), and for RCA_F32_TF32 bf16 hi/lo copies of Q, dout, K
  * and V. Returns 0 for invalid sizes.
  */
-size_t rca_attn_bwd_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
+RCA_API size_t rca_attn_bwd_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
                                    rca_dtype dt);
 
 /*
@@ -120,7 +129,7 @@ size_t rca_attn_bwd_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t T
  * clobbered. Runs rca_attn_bwd_preprocess, rca_attn_bwd_main and
  * rca_attn_bwd_dq_convert in order on cuda_stream.
  */
-rca_status rca_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+RCA_API rca_status rca_attn_bwd(const void* q, const void* k, const void* v, const void* out,
                         const float* lse, const void* dout, void* dq, void* dk, void* dv,
                         int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
                         rca_dtype dt, void* workspace, size_t workspace_bytes,
@@ -137,16 +146,16 @@ rca_status rca_attn_bwd(const void* q, const void* k, const void* v, const void*
  *              For RCA_F32_TF32 it first writes the bf16 hi/lo operand copies.
  *  dq_convert: dq = scale * accumulator, cast to the storage dtype.
  */
-rca_status rca_attn_bwd_preprocess(const void* out, const float* lse, const void* dout,
+RCA_API rca_status rca_attn_bwd_preprocess(const void* out, const float* lse, const void* dout,
                                    int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
                                    rca_dtype dt, void* workspace, size_t workspace_bytes,
                                    void* cuda_stream);
-rca_status rca_attn_bwd_main(const void* q, const void* k, const void* v, const void* dout,
+RCA_API rca_status rca_attn_bwd_main(const void* q, const void* k, const void* v, const void* dout,
                              void* dk, void* dv,
                              int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
                              rca_dtype dt, void* workspace, size_t workspace_bytes,
                              void* cuda_stream);
-rca_status rca_attn_bwd_dq_convert(void* dq, int64_t B, int64_t Hq, int64_t Hkv, int64_t T,
+RCA_API rca_status rca_attn_bwd_dq_convert(void* dq, int64_t B, int64_t Hq, int64_t Hkv, int64_t T,
                                    int64_t Dh, rca_dtype dt, const void* workspace,
                                    size_t workspace_bytes, void* cuda_stream);
 
@@ -176,7 +185,7 @@ rca_status rca_attn_bwd_dq_convert(void* dq, int64_t B, int64_t Hq, int64_t Hkv,
  *    the library's other status word. The kernels end within the wait limit.
  * Never calls cudaMalloc, cudaFree or any allocating routine.
  */
-rca_status rca_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* out,
+RCA_API rca_status rca_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* out,
                                 const float* lse, const void* dout, void* dq, void* dk, void* dv,
                                 int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
                                 rca_dtype dt, void* cuda_stream);
@@ -202,12 +211,12 @@ rca_status rca_attn_bwd_noalloc(const void* q, const void* k, const void* v, con
  * entry irrelevant. B <= 4096 and T <= 131072 (else RCA_ERR_UNSUPPORTED). Same
  * layouts, dtypes, head widths and errors as rca_attn_fwd / rca_attn_bwd otherwise.
  */
-size_t rca_attn_varlen_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt);
-rca_status rca_attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* seq_lens,
+RCA_API size_t rca_attn_varlen_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt);
+RCA_API rca_status rca_attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* seq_lens,
                                int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
                                void* out, float* lse, rca_dtype dt,
                                void* workspace, size_t workspace_bytes, void* cuda_stream);
-rca_status rca_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* out, const float* lse,
+RCA_API rca_status rca_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* out, const float* lse,
                                const void* dout, const int32_t* seq_lens, void* dq, void* dk, void* dv,
                                int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, rca_dtype dt,
                                void* workspace, size_t workspace_bytes, void* cuda_stream);
@@ -226,9 +235,9 @@ rca_status rca_attn_bwd_varlen(const void* q, const void* k, const void* v, cons
  * Same computation, dtypes, head widths, errors and workspace
  * (rca_attn_bwd_workspace_size) as rca_attn_fwd / rca_attn_bwd. 16-byte aligned.
  */
-rca_status rca_attn_fwd_qkv(const void* qkv, int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t Dh,
+RCA_API rca_status rca_attn_fwd_qkv(const void* qkv, int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t Dh,
                             void* out, float* lse, rca_dtype dt, void* cuda_stream);
-rca_status rca_attn_bwd_qkv(const void* qkv, const void* out, const float* lse, const void* dout, void* dqkv,
+RCA_API rca_status rca_attn_bwd_qkv(const void* qkv, const void* out, const float* lse, const void* dout, void* dqkv,
                             int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t Dh, rca_dtype dt,
                             void* workspace, size_t workspace_bytes, void* cuda_stream);
 
@@ -267,13 +276,13 @@ rca_status rca_attn_bwd_qkv(const void* qkv, const void* out, const float* lse, 
  * on cuda_stream. Device waits are time-bounded like the other kernels'
  * (RCA_ERR_DEVICE_TIMEOUT through rca_stream_status).
  */
-size_t rca_attn_materialized_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
+RCA_API size_t rca_attn_materialized_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
                                             rca_dtype dt);
-rca_status rca_attn_materialized_fwd(const void* q, const void* k, const void* v,
+RCA_API rca_status rca_attn_materialized_fwd(const void* q, const void* k, const void* v,
                                      int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
                                      void* out, float* probs, float* lse, rca_dtype dt,
                                      void* workspace, size_t workspace_bytes, void* cuda_stream);
-rca_status rca_attn_materialized_bwd(const void* q, const void* k, const void* v, const float* probs,
+RCA_API rca_status rca_attn_materialized_bwd(const void* q, const void* k, const void* v, const float* probs,
                                      const void* dout, const float* dprobs,
                                      void* dq, void* dk, void* dv,
                                      int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh,
@@ -294,8 +303,8 @@ rca_status rca_attn_materialized_bwd(const void* q, const void* k, const void* v
  *             for j <= i, 0 for j > i (the gradient of the unscaled scores).
  * Device pointers, 16-byte aligned; lse is [N, T]; 1 <= T <= 65536; scale finite.
  */
-rca_status rca_causal_softmax(float* scores, float* lse, int64_t N, int64_t T, float scale, void* cuda_stream);
-rca_status rca_causal_softmax_bwd(const float* probs, float* grad, const float* grad_extra, int64_t N, int64_t T,
+RCA_API rca_status rca_causal_softmax(float* scores, float* lse, int64_t N, int64_t T, float scale, void* cuda_stream);
+RCA_API rca_status rca_causal_softmax_bwd(const float* probs, float* grad, const float* grad_extra, int64_t N, int64_t T,
                                   float scale, void* cuda_stream);
 
 /*
@@ -347,9 +356,9 @@ rca_status rca_causal_softmax_bwd(const float* probs, float* grad, const float* 
  * pointers owned by the caller; the call validates its host arguments (nothing
  * is enqueued on failure) and then only enqueues work on cuda_stream.
  */
-size_t rca_paged_decode_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t Dh,
+RCA_API size_t rca_paged_decode_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t Dh,
                                        int64_t page_size, int64_t max_pages, rca_dtype dt);
-rca_status rca_paged_decode(const void* q, const void* k_pool, const void* v_pool,
+RCA_API rca_status rca_paged_decode(const void* q, const void* k_pool, const void* v_pool,
                             const int32_t* page_table, const int32_t* seq_lens,
                             int64_t B, int64_t Hq, int64_t Hkv, int64_t Dh,
                             int64_t page_size, int64_t max_pages, int64_t num_pages,
@@ -363,7 +372,7 @@ rca_status rca_paged_decode(const void* q, const void* k_pool, const void* v_poo
  * library on the current device, the allocation-free backward's included.
  * RCA_OK if none happened.
  */
-rca_status rca_stream_status(void* cuda_stream);
+RCA_API rca_status rca_stream_status(void* cuda_stream);
 
 /*
  * Failure-detection self-test (no counterpart on the pages). Enqueues a small
@@ -373,7 +382,7 @@ rca_status rca_stream_status(void* cuda_stream);
  * next rca_stream_status() on this stream returns RCA_ERR_DEVICE_TIMEOUT (and
  * clears it); the CUDA context remains usable. Nothing faults or hangs.
  */
-rca_status rca_selftest_device_timeout(void* cuda_stream);
+RCA_API rca_status rca_selftest_device_timeout(void* cuda_stream);
 
 /*
  * The same self-test for the allocation-free backward's status word: the
@@ -381,14 +390,14 @@ rca_status rca_selftest_device_timeout(void* cuda_stream);
  * and the next rca_stream_status() returns RCA_ERR_DEVICE_TIMEOUT. Sets up the
  * built-in region on the current device like a first rca_attn_bwd_noalloc call.
  */
-rca_status rca_selftest_noalloc_timeout(void* cuda_stream);
+RCA_API rca_status rca_selftest_noalloc_timeout(void* cuda_stream);
 
 /*
  * Sets the device-side wait limit in nanoseconds for subsequent launches from
  * any thread (default 2e9 = 2 s; values < 1e6 are raised to 1e6). Returns the
  * previous value.
  */
-uint64_t rca_set_wait_timeout_ns(uint64_t ns);
+RCA_API uint64_t rca_set_wait_timeout_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }

@@ -1,10 +1,12 @@
 """Host-side checks of the C ABI (no GPU needed): the library builds and loads,
-exports every function include/rca_attn.h declares, and rejects invalid
+exports exactly the functions include/rca_attn.h declares, and rejects invalid
 arguments before touching any pointer or launching anything."""
 
 import ctypes
 import os
 import re
+import shutil
+import subprocess
 
 import pytest
 
@@ -38,6 +40,21 @@ def test_every_declared_symbol_is_exported(lib):
     for n in declared_functions():
         assert hasattr(lib, n), f"{n} declared in rca_attn.h but not exported"
         assert n in _native._SIG, f"{n} has no binding signature"
+
+
+def test_only_declared_symbols_are_exported(lib):
+    """The library is built with hidden visibility: its dynamic symbol table
+    holds the calls the header declares and nothing of its internals (which
+    would let a second copy of the library, or a host program defining the
+    same names, interfere with it)."""
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm (binutils) not installed")
+    out = subprocess.run([nm, "-D", "--defined-only", lib._name], capture_output=True, text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if ln.strip()}
+    linker = {"_init", "_fini", "__bss_start", "_edata", "_end", "__bss_start__", "__bss_end__", "__end__",
+              "_bss_end__"}
+    assert exported - linker == set(declared_functions())
 
 
 def test_abi_version(lib):
