@@ -715,16 +715,20 @@ def bench_materialized(w, dev, stream, steps, warmup, P):
     lse2 = torch.empty((E, T), device=dev)
     sm_ms = timed(lambda i: rca.rca_causal_softmax(s[i % 2], lse2, scale, stream), steps)
     smb_ms = timed(lambda i: rca.rca_causal_softmax_bwd(s[i % 2], g[i % 2], None, scale, stream), steps)
+    # The backward call runs the VJP tiled by 128 columns (dS only where its products read it).
+    smbt_ms = timed(lambda i: rca.rca_causal_softmax_bwd_tiled(s[i % 2], g[i % 2], None, 128, scale, stream), steps)
     tri = E * T * (T + 1) // 2 * 4  # bytes of the kept (lower) half of the rows
     full = E * T * T * 4
     sm_bytes = tri + full + E * T * 4       # read the kept entries, write whole rows and LSE
     smb_bytes = 2 * tri + full              # read P and dP where kept, write whole rows
+    # tiled by 128: row i written up to the end of its diagonal tile
+    smbt_bytes = 2 * tri + E * sum(min(T, 128 * (i // 128 + 1)) for i in range(T)) * 4
     # The products over the kept triangle: 2 forward (S, O), 4 backward (dP, dQ, dK, dV),
     # each 2 * Dh FLOPs per kept score; each streams one [T, T] triangle once (S and
     # dP written, P or dS read), the [B,T,H,Dh] operands being small beside it.
     prod_flops = 2.0 * w.Dh * (E * T * (T + 1) / 2) * (2 + 4)
     prod_bytes = 6 * tri
-    prod_ms = (fwd_ms - sm_ms) + (bwd_ms - smb_ms)
+    prod_ms = (fwd_ms - sm_ms) + (bwd_ms - smbt_ms)
 
     def roof(nbytes, ms):
         a = nbytes / (ms * 1e-3) / 1e9
@@ -737,8 +741,10 @@ def bench_materialized(w, dev, stream, steps, warmup, P):
         "products": {"ms": prod_ms, "tflops": prod_flops / (prod_ms * 1e-3) / 1e12,
                      "gbs": prod_bytes / (prod_ms * 1e-3) / 1e9, "frac_hbm": prod_bytes / (prod_ms * 1e-3) / 1e9
                      / P["hbm_gbs"], "bytes": prod_bytes,
-                     "how": "fwd + bwd call time minus the two softmax kernels timed alone"},
+                     "how": "fwd + bwd call time minus the softmax (whole rows) and the VJP tiled by 128 "
+                            "columns, the forms the two calls run, timed alone"},
         "causal_softmax": roof(sm_bytes, sm_ms), "causal_softmax_bwd": roof(smb_bytes, smb_ms),
+        "causal_softmax_bwd_tiled128": roof(smbt_bytes, smbt_ms),
         "note": "all kernels are this library's: tensor-core products over the kept triangle of tiles only, "
                 "the fused causal softmax and its VJP",
         "gpu_launches": {"per_fwd": 3 if w.dtype == "bf16" else 6, "per_bwd": 5 if w.dtype == "bf16" else 9},

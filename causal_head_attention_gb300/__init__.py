@@ -29,6 +29,7 @@ from ._native import (  # noqa: F401  (C-ABI names)
     rca_attn_materialized_workspace_size,
     rca_causal_softmax,
     rca_causal_softmax_bwd,
+    rca_causal_softmax_bwd_tiled,
     rca_last_error,
     rca_paged_decode,
     rca_paged_decode_workspace_size,
@@ -69,6 +70,7 @@ __all__ = [
     "rca_attn_materialized_workspace_size",
     "rca_causal_softmax",
     "rca_causal_softmax_bwd",
+    "rca_causal_softmax_bwd_tiled",
     "paged_decode",
     "rca_paged_decode",
     "rca_paged_decode_workspace_size",

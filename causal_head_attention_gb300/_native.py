@@ -59,6 +59,7 @@ _SIG = {
                                                  ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "rca_causal_softmax": (ctypes.c_int, [_P, _P, _I, _I, ctypes.c_float, _P]),
     "rca_causal_softmax_bwd": (ctypes.c_int, [_P, _P, _P, _I, _I, ctypes.c_float, _P]),
+    "rca_causal_softmax_bwd_tiled": (ctypes.c_int, [_P, _P, _P, _I, _I, _I, ctypes.c_float, _P]),
     "rca_attn_fwd_qkv": (ctypes.c_int, [_P, _I, _I, _I, _I, _I, _P, _P, ctypes.c_int, _P]),
     "rca_attn_bwd_qkv": (ctypes.c_int, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_int, _P, ctypes.c_size_t,
                                         _P]),
@@ -326,6 +327,15 @@ def rca_causal_softmax_bwd(probs, grad, grad_extra, scale, stream=None):
     N = probs.numel() // (T * T)
     _check(lib().rca_causal_softmax_bwd(_ptr(probs), _ptr(grad), _ptr(grad_extra), N, T, float(scale),
                                         _stream(stream)))
+
+
+def rca_causal_softmax_bwd_tiled(probs, grad, grad_extra, tile, scale, stream=None):
+    """As rca_causal_softmax_bwd, row i read and written only for columns
+    j < min(T, tile * (i // tile + 1)); the rest of grad is left as it was."""
+    T = probs.shape[-1]
+    N = probs.numel() // (T * T)
+    _check(lib().rca_causal_softmax_bwd_tiled(_ptr(probs), _ptr(grad), _ptr(grad_extra), N, T, int(tile),
+                                              float(scale), _stream(stream)))
 
 
 def _qkv_shape(qkv, Hq, Hkv):

@@ -27,7 +27,9 @@
 // fp32 itself; 2 parts: 3 products, ~2^-17). X (P or dS) is split into two
 // parts by the converting warps as it is loaded; bf16 operands are exact.
 //
-// Scheduling: persistent CTAs (one per SM) take items c, c + G, ...; roles
+// Scheduling: persistent CTAs (one per SM) take items c, c + G, ... (the
+// reduce kernel's items differ in length and are dealt in alternating
+// directions, see reduce_deal); roles
 // are a TMA warp, a single-thread MMA issuer, a TMEM owner, four epilogue
 // warps (TMEM lanes 32 q .. 32 q + 31) and, in the reduce kernel, eight
 // converting warps that load X straight from global memory (two chunks in
@@ -328,6 +330,17 @@ __device__ __forceinline__ int reduce_chunks_per_head(const ReduceArgs& a, int t
   return (kend + 63) / 64;
 }
 
+// The n-th item of CTA c among G: items are dealt in rounds of G, even rounds
+// in CTA order and odd rounds in reverse, so that a CTA given one of the
+// longest items of a round gets one of the shortest of the next (the items
+// are ordered longest first). reduce_count is how many items CTA c gets.
+__device__ __forceinline__ int reduce_deal(int c, int n, int G) { return n * G + ((n & 1) ? G - 1 - c : c); }
+__device__ __forceinline__ int reduce_count(int c, int n_items, int G) {
+  const int full = n_items / G, rem = n_items - full * G;
+  const int pos = (full & 1) ? G - 1 - c : c;
+  return full + (pos < rem ? 1 : 0);
+}
+
 template <bool TRANS, int NPY, int DHP>
 __global__ void __launch_bounds__(512, 1)
     mat_reduce_kernel(const __grid_constant__ ReduceMaps maps, const ReduceArgs a) {
@@ -363,7 +376,7 @@ __global__ void __launch_bounds__(512, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl w{a.status, abort_flag, a.timeout_ns};
-  const int n_mine = a.n_items > static_cast<int>(blockIdx.x) ? (a.n_items - 1 - static_cast<int>(blockIdx.x)) / G + 1 : 0;
+  const int n_mine = reduce_count(static_cast<int>(blockIdx.x), a.n_items, G);
 
   if (warp == 0) {
     // ---------------- TMA producer: Y chunks ----------------
@@ -374,7 +387,7 @@ __global__ void __launch_bounds__(512, 1)
       bool ok = true;
       for (int n = 0; ok && n < n_mine; ++n) {
         int b, hd, t;
-        reduce_item<TRANS>(a, blockIdx.x + n * G, b, hd, t);
+        reduce_item<TRANS>(a, reduce_deal(blockIdx.x, n, G), b, hd, t);
         const int nch = reduce_chunks_per_head<TRANS>(a, t);
         const int nh = TRANS ? a.group : 1;
         for (int r = 0; ok && r < nh; ++r)
@@ -406,7 +419,7 @@ __global__ void __launch_bounds__(512, 1)
       bool ok = true;
       for (int n = 0; ok && n < n_mine; ++n) {
         int b, hd, t;
-        reduce_item<TRANS>(a, blockIdx.x + n * G, b, hd, t);
+        reduce_item<TRANS>(a, reduce_deal(blockIdx.x, n, G), b, hd, t);
         const int nch = reduce_chunks_per_head<TRANS>(a, t) * (TRANS ? a.group : 1);
         const int acc = n & 1;
         const uint32_t d = tmem + acc * DHP;
@@ -497,7 +510,7 @@ __global__ void __launch_bounds__(512, 1)
       q.c = 0;
       q.valid = n < n_mine;
       if (q.valid) {
-        reduce_item<TRANS>(a, blockIdx.x + n * G, q.b, q.hd, q.t);
+        reduce_item<TRANS>(a, reduce_deal(blockIdx.x, n, G), q.b, q.hd, q.t);
         q.nch = reduce_chunks_per_head<TRANS>(a, q.t);
         q.nh = TRANS ? a.group : 1;
       }
@@ -556,7 +569,7 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
     for (int n = 0; n < n_mine; ++n) {
       int b, hd, t;
-      reduce_item<TRANS>(a, blockIdx.x + n * G, b, hd, t);
+      reduce_item<TRANS>(a, reduce_deal(blockIdx.x, n, G), b, hd, t);
       const int acc = n & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(C::B_ACCF + acc), static_cast<uint32_t>((n >> 1) & 1), w))) break;
       tc_fence_after();

@@ -124,10 +124,13 @@ __global__ void causal_softmax_kernel(float* __restrict__ s, float* __restrict__
 
 // VJP of the fused causal softmax, in place on dP, one warp per row: with
 // dPt = dP + dP_up, dS[i, j] = scale P[i, j] (dPt[i, j] - sum_k P[i, k] dPt[i, k])
-// for j <= i, 0 above (the gradient with respect to the unscaled scores).
+// for j <= i, 0 above (the gradient with respect to the unscaled scores),
+// written up to the end of row i's diagonal tile of `tile` columns (tile >= T:
+// the whole row); dP and dP_up are read for j <= i only.
 template <bool VEC>
 __global__ void causal_softmax_bwd_kernel(const float* __restrict__ p, float* __restrict__ dp,
-                                          const float* __restrict__ dp_up, int64_t rows, int T, float scale) {
+                                          const float* __restrict__ dp_up, int64_t rows, int T, int tile,
+                                          float scale) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
   for (int64_t r = blockIdx.x * int64_t(blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
@@ -135,6 +138,9 @@ __global__ void causal_softmax_bwd_kernel(const float* __restrict__ p, float* __
     float* drow = dp + r * T;
     const float* urow = dp_up ? dp_up + r * T : nullptr;
     const int n = int(r % T) + 1;
+    // Columns written: the row's causal tiles of `tile` columns (the diagonal
+    // one zero past n); tile >= T writes the whole row.
+    const int wend = tile >= T ? T : min(T, ((n - 1) / tile + 1) * tile);
     float sum = 0.f;
     if constexpr (VEC) {
       for (int j = lane * 4; j < n; j += 128) {
@@ -153,7 +159,7 @@ __global__ void causal_softmax_bwd_kernel(const float* __restrict__ p, float* __
 #pragma unroll
     for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(FULL, sum, off);
     if constexpr (VEC) {
-      for (int j = lane * 4; j < T; j += 128) {
+      for (int j = lane * 4; j < wend; j += 128) {
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
         if (j < n) {
           const float4 a = *reinterpret_cast<const float4*>(prow + j);
@@ -170,7 +176,7 @@ __global__ void causal_softmax_bwd_kernel(const float* __restrict__ p, float* __
         *reinterpret_cast<float4*>(drow + j) = x;
       }
     } else {
-      for (int j = lane; j < T; j += 32)
+      for (int j = lane; j < wend; j += 32)
         drow[j] = j < n ? scale * prow[j] * (drow[j] + (urow ? urow[j] : 0.f) - sum) : 0.f;
     }
   }
@@ -372,12 +378,13 @@ bool launch_softmax(float* s, float* lse, int64_t rows, int T, float scale, cuda
   return cuda_ok(cudaGetLastError(), "launch causal_softmax_kernel", err);
 }
 
-bool launch_softmax_bwd(const float* p, float* dp, const float* dp_up, int64_t rows, int T, float scale,
+bool launch_softmax_bwd(const float* p, float* dp, const float* dp_up, int64_t rows, int T, int tile, float scale,
                         cudaStream_t st, std::string& err) {
-  if (T % 4 == 0)
-    causal_softmax_bwd_kernel<true><<<grid_for(rows, 8), 256, 0, st>>>(p, dp, dp_up, rows, T, scale);
+  // The vector form writes 4 columns at a time: T and the tile width multiples of 4.
+  if (T % 4 == 0 && (tile >= T || tile % 4 == 0))
+    causal_softmax_bwd_kernel<true><<<grid_for(rows, 8), 256, 0, st>>>(p, dp, dp_up, rows, T, tile, scale);
   else
-    causal_softmax_bwd_kernel<false><<<grid_for(rows, 8), 256, 0, st>>>(p, dp, dp_up, rows, T, scale);
+    causal_softmax_bwd_kernel<false><<<grid_for(rows, 8), 256, 0, st>>>(p, dp, dp_up, rows, T, tile, scale);
   return cuda_ok(cudaGetLastError(), "launch causal_softmax_bwd_kernel", err);
 }
 
@@ -393,9 +400,9 @@ bool causal_softmax_fwd(float* scores, float* lse, int64_t N, int64_t T, float s
   return mat::launch_softmax(scores, lse, N * T, int(T), scale, st, err);
 }
 
-bool causal_softmax_bwd(const float* probs, float* grad, const float* grad_extra, int64_t N, int64_t T, float scale,
-                        cudaStream_t st, std::string& err) {
-  return mat::launch_softmax_bwd(probs, grad, grad_extra, N * T, int(T), scale, st, err);
+bool causal_softmax_bwd(const float* probs, float* grad, const float* grad_extra, int64_t N, int64_t T, int64_t tile,
+                        float scale, cudaStream_t st, std::string& err) {
+  return mat::launch_softmax_bwd(probs, grad, grad_extra, N * T, int(T), int(tile < T ? tile : T), scale, st, err);
 }
 
 size_t materialized_workspace_size(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, bool bf16) {
@@ -431,7 +438,8 @@ bool materialized_bwd(const MatParams& p, cudaStream_t st, std::string& err) {
   float* dp = reinterpret_cast<float*>(c.ws + c.L.dp);
   // dP = dO V^T (kept tiles), then dS (with respect to the unscaled scores) in place.
   if (!scores(c, p.dout, P_DO, p.v, P_V, dp, err)) return false;
-  if (!launch_softmax_bwd(p.probs, dp, p.dprobs, int64_t(c.E) * c.T, c.T, scale, st, err)) return false;
+  // dS only where the products read it: each row's causal 128-column tiles.
+  if (!launch_softmax_bwd(p.probs, dp, p.dprobs, int64_t(c.E) * c.T, c.T, 128, scale, st, err)) return false;
   // dQ = dS K;  dK = dS^T Q;  dV = P^T dO  (the last two summed over each group).
   if (!reduce<false>(c, dp, p.k, P_K, p.dq, err)) return false;
   if (!reduce<true>(c, dp, p.q, P_Q, p.dk, err)) return false;

@@ -50,7 +50,9 @@ bool materialized_bwd(const MatParams& p, cudaStream_t st, std::string& err);
 // (in place), as used by the two calls above.
 bool causal_softmax_fwd(float* scores, float* lse, int64_t N, int64_t T, float scale, cudaStream_t st,
                         std::string& err);
-bool causal_softmax_bwd(const float* probs, float* grad, const float* grad_extra, int64_t N, int64_t T, float scale,
-                        cudaStream_t st, std::string& err);
+// The VJP writes row i for columns j < min(T, tile * (i / tile + 1)) (tile >= T:
+// whole rows).
+bool causal_softmax_bwd(const float* probs, float* grad, const float* grad_extra, int64_t N, int64_t T, int64_t tile,
+                        float scale, cudaStream_t st, std::string& err);
 
 }  // namespace rca

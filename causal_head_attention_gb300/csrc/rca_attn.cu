@@ -1135,18 +1135,33 @@ rca_status rca_causal_softmax(float* scores, float* lse, int64_t N, int64_t T, f
   RCA_GUARD_END
 }
 
+static rca_status softmax_bwd_call(const char* name, const float* probs, float* grad, const float* grad_extra,
+                                   int64_t N, int64_t T, int64_t tile, float scale, void* cuda_stream) {
+  if (!probs || !grad) return fail(RCA_ERR_INVALID_ARGUMENT, "%s: null pointer", name);
+  RCA_CHECK(check_softmax_args(N, T, scale));
+  if (tile < 1) return fail(RCA_ERR_INVALID_ARGUMENT, "%s: tile must be >= 1 (got %lld)", name, (long long)tile);
+  if (!aligned16(probs) || !aligned16(grad) || (grad_extra && !aligned16(grad_extra)))
+    return fail(RCA_ERR_INVALID_ARGUMENT, "%s: tensors must be 16-byte aligned", name);
+  std::string err;
+  if (!rca::causal_softmax_bwd(probs, grad, grad_extra, N, T, tile, scale, static_cast<cudaStream_t>(cuda_stream),
+                               err))
+    return fail(RCA_ERR_CUDA, "%s: %s", name, err.c_str());
+  return RCA_OK;
+}
+
 rca_status rca_causal_softmax_bwd(const float* probs, float* grad, const float* grad_extra, int64_t N, int64_t T,
                                   float scale, void* cuda_stream) {
   RCA_GUARD_BEGIN
   g_err.clear();
-  if (!probs || !grad) return fail(RCA_ERR_INVALID_ARGUMENT, "rca_causal_softmax_bwd: null pointer");
-  RCA_CHECK(check_softmax_args(N, T, scale));
-  if (!aligned16(probs) || !aligned16(grad) || (grad_extra && !aligned16(grad_extra)))
-    return fail(RCA_ERR_INVALID_ARGUMENT, "rca_causal_softmax_bwd: tensors must be 16-byte aligned");
-  std::string err;
-  if (!rca::causal_softmax_bwd(probs, grad, grad_extra, N, T, scale, static_cast<cudaStream_t>(cuda_stream), err))
-    return fail(RCA_ERR_CUDA, "rca_causal_softmax_bwd: %s", err.c_str());
-  return RCA_OK;
+  return softmax_bwd_call("rca_causal_softmax_bwd", probs, grad, grad_extra, N, T, T, scale, cuda_stream);
+  RCA_GUARD_END
+}
+
+rca_status rca_causal_softmax_bwd_tiled(const float* probs, float* grad, const float* grad_extra, int64_t N,
+                                        int64_t T, int64_t tile, float scale, void* cuda_stream) {
+  RCA_GUARD_BEGIN
+  g_err.clear();
+  return softmax_bwd_call("rca_causal_softmax_bwd_tiled", probs, grad, grad_extra, N, T, tile, scale, cuda_stream);
   RCA_GUARD_END
 }
 

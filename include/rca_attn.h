@@ -96,7 +96,7 @@ typedef enum {
 typedef enum { RCA_F32_TF32 = 0, RCA_BF16 = 1 } rca_dtype;
 
 /* ABI version: upper 16 bits major, lower 16 bits minor (0x00010007 = 1.7). */
-#define RCA_ABI_VERSION 0x00010007u
+#define RCA_ABI_VERSION 0x00010008u
 RCA_API uint32_t rca_abi_version(void);
 
 /* Message of the last failed call on this thread ("" if none). The pointer is
@@ -306,6 +306,18 @@ RCA_API rca_status rca_attn_materialized_bwd(const void* q, const void* k, const
 RCA_API rca_status rca_causal_softmax(float* scores, float* lse, int64_t N, int64_t T, float scale, void* cuda_stream);
 RCA_API rca_status rca_causal_softmax_bwd(const float* probs, float* grad, const float* grad_extra, int64_t N, int64_t T,
                                   float scale, void* cuda_stream);
+/*
+ * The same VJP restricted to the causal tiles of a tiled consumer: row i is
+ * read and written only for columns j < min(T, tile * (floor(i / tile) + 1)),
+ * i.e. its tiles of `tile` columns on or left of the diagonal (entries above
+ * the diagonal inside the diagonal tile are written as 0); the rest of the
+ * row, in grad and grad_extra, is neither read nor written. tile >= T is
+ * rca_causal_softmax_bwd. The materialized backward applies it with tile 128
+ * to its dP workspace, whose products read only those tiles. tile >= 1, else
+ * RCA_ERR_INVALID_ARGUMENT; other arguments and errors as above. (ABI 1.8)
+ */
+RCA_API rca_status rca_causal_softmax_bwd_tiled(const float* probs, float* grad, const float* grad_extra, int64_t N,
+                                                int64_t T, int64_t tile, float scale, void* cuda_stream);
 
 /*
  * Paged decode attention ("Execution Backends and the Python ABI",

@@ -202,6 +202,29 @@ def test_materialized_bwd_validation(lib):
     assert st == 1 and "null" in lib.rca_last_error().decode()
 
 
+@pytest.mark.parametrize(
+    "kw,needle",
+    [
+        (dict(probs=NULL), "null"),
+        (dict(grad=NULL), "null"),
+        (dict(tile=0), "tile must be >= 1"),
+        (dict(tile=-128), "tile must be >= 1"),
+        (dict(T=0), ">= 1"),
+        (dict(T=70000), "too large"),
+        (dict(scale=float("nan")), "finite"),
+        (dict(grad=ctypes.c_void_p(4100)), "aligned"),
+    ],
+)
+def test_softmax_bwd_tiled_validation(lib, kw, needle):
+    a = dict(probs=FAKE, grad=FAKE, extra=NULL, N=2, T=256, tile=128, scale=0.125)
+    a.update(kw)
+    st = lib.rca_causal_softmax_bwd_tiled(a["probs"], a["grad"], a["extra"], a["N"], a["T"], a["tile"], a["scale"],
+                                          NULL)
+    assert st == 1
+    assert needle in lib.rca_last_error().decode()
+    assert "rca_causal_softmax_bwd_tiled" in lib.rca_last_error().decode() or needle != "null"
+
+
 def test_materialized_workspace_size(lib):
     n = lib.rca_attn_materialized_workspace_size(4, 16, 16, 2048, 64, 1)
     # bf16 storage: dP [B,Hq,T,T] fp32 only

@@ -145,6 +145,34 @@ def test_headline_cross_check_with_flash():
         assert np.all(err <= 2.0 ** -8 * np.abs(o_ref) + 1e-5)
 
 
+@pytest.mark.parametrize("T,tile", [(37, 1), (37, 5), (256, 128), (300, 128), (300, 1000), (130, 64)])
+def test_causal_softmax_bwd_tiled(T, tile):
+    """The tiled VJP: row i written for j < min(T, tile (i // tile + 1)), equal
+    there to the whole-row VJP bit for bit and to the oracle within its bound;
+    every other entry of grad left exactly as it was."""
+    g = torch.Generator().manual_seed(1000 + T + tile)
+    s = torch.randn((2, T, T), generator=g) * 3
+    grad = torch.randn((2, T, T), generator=g)
+    extra = torch.randn((2, T, T), generator=g)
+    dev = torch.device("cuda:0")
+    pd = s.to(dev)
+    lse = torch.empty((2, T), device=dev)
+    rca.rca_causal_softmax(pd, lse, 0.3)
+    full, tiled, ed = grad.to(dev), grad.to(dev), extra.to(dev)
+    rca.rca_causal_softmax_bwd(pd, full, ed, 0.3)
+    rca.rca_causal_softmax_bwd_tiled(pd, tiled, ed, tile, 0.3)
+    rca.rca_stream_status()
+    i = torch.arange(T).view(T, 1)
+    j = torch.arange(T).view(1, T)
+    written = (j < torch.clamp((i // tile + 1) * tile, max=T)).expand(2, T, T)
+    tc, fc = tiled.cpu(), full.cpu()
+    assert torch.equal(tc[written], fc[written])
+    assert torch.equal(tc[~written], grad[~written])
+    d_ref = oracle.causal_softmax_vjp(to64(pd), (grad + extra).double().numpy(), 0.3)
+    err = np.abs(to64(tc) - d_ref)[written.numpy()]
+    assert np.all(err <= 1e-6 + 1e-4 * np.abs(d_ref[written.numpy()]))
+
+
 @pytest.mark.parametrize("T", [1, 37, 256])
 def test_causal_softmax_entries(T):
     """The fused causal softmax and its VJP on their own (in place)."""
