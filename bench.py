@@ -723,12 +723,16 @@ def bench_materialized(w, dev, stream, steps, warmup, P):
     smb_bytes = 2 * tri + full              # read P and dP where kept, write whole rows
     # tiled by 128: row i written up to the end of its diagonal tile
     smbt_bytes = 2 * tri + E * sum(min(T, 128 * (i // 128 + 1)) for i in range(T)) * 4
-    # The products over the kept triangle: 2 forward (S, O), 4 backward (dP, dQ, dK, dV),
-    # each 2 * Dh FLOPs per kept score; each streams one [T, T] triangle once (S and
-    # dP written, P or dS read), the [B,T,H,Dh] operands being small beside it.
-    prod_flops = 2.0 * w.Dh * (E * T * (T + 1) / 2) * (2 + 4)
-    prod_bytes = 6 * tri
-    prod_ms = (fwd_ms - sm_ms) + (bwd_ms - smbt_ms)
+    # Forward call: the probabilities written once as whole rows and read once by
+    # P V (S is formed twice on the tensor cores and never stored); the
+    # [B,T,H,Dh] operands are small beside them.
+    fwd_bytes = full + tri
+    # Backward products over the kept triangle (dP, dQ, dK, dV), each 2 * Dh FLOPs
+    # per kept score and one [T, T] triangle streamed once (dP written; dS, dS, P
+    # read): the backward call minus the tiled VJP it runs, timed alone.
+    prod_flops = 2.0 * w.Dh * (E * T * (T + 1) / 2) * 4
+    prod_bytes = 4 * tri
+    prod_ms = bwd_ms - smbt_ms
 
     def roof(nbytes, ms):
         a = nbytes / (ms * 1e-3) / 1e9
@@ -738,16 +742,18 @@ def bench_materialized(w, dev, stream, steps, warmup, P):
     return {
         "workload": w.describe(), "name": w.name, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
         "probs_bytes": full,
-        "products": {"ms": prod_ms, "tflops": prod_flops / (prod_ms * 1e-3) / 1e12,
-                     "gbs": prod_bytes / (prod_ms * 1e-3) / 1e9, "frac_hbm": prod_bytes / (prod_ms * 1e-3) / 1e9
-                     / P["hbm_gbs"], "bytes": prod_bytes,
-                     "how": "fwd + bwd call time minus the softmax (whole rows) and the VJP tiled by 128 "
-                            "columns, the forms the two calls run, timed alone"},
+        "fwd": dict(roof(fwd_bytes, fwd_ms), how="whole forward call: probabilities written once (whole rows), "
+                    "read once by P V; row statistics from a first pass over recomputed S"),
+        "bwd_products": {"ms": prod_ms, "tflops": prod_flops / (prod_ms * 1e-3) / 1e12,
+                         "gbs": prod_bytes / (prod_ms * 1e-3) / 1e9,
+                         "frac_hbm": prod_bytes / (prod_ms * 1e-3) / 1e9 / P["hbm_gbs"], "bytes": prod_bytes,
+                         "how": "backward call time minus the VJP tiled by 128 columns (the form it runs), "
+                                "timed alone"},
         "causal_softmax": roof(sm_bytes, sm_ms), "causal_softmax_bwd": roof(smb_bytes, smb_ms),
         "causal_softmax_bwd_tiled128": roof(smbt_bytes, smbt_ms),
         "note": "all kernels are this library's: tensor-core products over the kept triangle of tiles only, "
                 "the fused causal softmax and its VJP",
-        "gpu_launches": {"per_fwd": 3 if w.dtype == "bf16" else 6, "per_bwd": 5 if w.dtype == "bf16" else 9},
+        "gpu_launches": {"per_fwd": 4 if w.dtype == "bf16" else 7, "per_bwd": 5 if w.dtype == "bf16" else 9},
     }
 
 

@@ -8,7 +8,9 @@
 //
 //   mat_scores_kernel     C[i, j] = A[i] . B[j]   for 128 x 128 tiles j <= i
 //                         (S = Q K^T in the forward, dP = dO V^T in the
-//                         backward), fp32 into the [E, T, T] rows
+//                         backward); the epilogue writes C (fp32 into the
+//                         [E, T, T] rows), or per-row statistics of C, or
+//                         the probabilities 2^(c C - LSE2) (see MODE)
 //   mat_reduce_kernel<0>  R[i] = sum_{j <= i} X[i, j] Y[j]
 //                         (O = P V, dQ = dS K): one item per 128 query rows
 //   mat_reduce_kernel<1>  R[j] = sum_h sum_{i >= j} X_h[i, j] Y_h[i]
@@ -29,9 +31,10 @@
 //
 // Scheduling: persistent CTAs (one per SM) take items c, c + G, ... (the
 // reduce kernel's items differ in length and are dealt in alternating
-// directions, see reduce_deal); roles
-// are a TMA warp, a single-thread MMA issuer, a TMEM owner, four epilogue
-// warps (TMEM lanes 32 q .. 32 q + 31) and, in the reduce kernel, eight
+// directions, see reduce_deal); roles are a TMA warp, a single-thread MMA
+// issuer, a TMEM owner, epilogue warps (TMEM lanes 32 q .. 32 q + 31: four in
+// the reduce kernel; eight in the scores kernel, two per lane quarter, each
+// with one 64-column half of the tile) and, in the reduce kernel, eight
 // converting warps that load X straight from global memory (two chunks in
 // flight per thread) and store its bf16 parts in the swizzled layout the MMA
 // reads. Two TMEM accumulators alternate between items so one item's
@@ -63,11 +66,11 @@ struct Products {
 // ---------------------------------------------------------------------------
 template <int NP, int DHP>
 struct ScoresCfg {
-  static constexpr int NTHREADS = 256;
+  static constexpr int NTHREADS = 384;                 // warps 0-3 roles, 4-11 epilogue
   static constexpr int DP = DHP / 64;                  // 64-column panels across the head width
   static constexpr int PART = DP * kPanel64;           // one bf16 part of a 128-row tile
   static constexpr int STAGE = 2 * NP * PART;          // A parts then B parts
-  static constexpr int STAGING = 4 * 32 * 128;         // four warps x 32 rows x 128 bytes
+  static constexpr int STAGING = 8 * 32 * 128;         // eight warps x 32 rows x 128 bytes
   static constexpr int SMEM_LIMIT = 232448;
   static constexpr int BAR_BYTES = 256;
   static constexpr int NS_FIT = (SMEM_LIMIT - 1024 - BAR_BYTES - STAGING) / STAGE;
@@ -84,6 +87,9 @@ struct ScoresCfg {
 
 struct ScoresArgs {
   float* out;         // [E, T, T]
+  float2* part;       // row statistics mode: (max, sum) of row r, tile j, column half h at [e, r, j, h]
+  const float* lse2;  // probabilities mode: base-2 LSE of each row, [E, T]
+  float c;            // both modes: scale * log2(e)
   int* status;
   unsigned long long timeout_ns;
   int B, Hq, Hkv, T, group, n_t;
@@ -107,8 +113,17 @@ __device__ __forceinline__ void scores_item(const ScoresArgs& a, long long idx, 
   j = static_cast<int>(r - static_cast<long long>(ii) * (ii + 1) / 2);
 }
 
-template <int NP, int DHP, bool VEC>
-__global__ void __launch_bounds__(256, 1)
+// MODE (what the epilogue does with a tile's scores S = A B^T):
+//   kScoresRaw    write S (fp32) into the kept tiles; blocks of the diagonal
+//                 tile that lie wholly above a warp's rows are not written;
+//   kScoresStats  write, per row and tile, x = c S's (max m, sum of 2^(x - m))
+//                 over the row's kept columns, nothing else;
+//   kScoresProbs  write P = 2^(c S - LSE2) on and below the diagonal, 0 above it
+//                 inside the diagonal tile (the whole tile is written).
+enum { kScoresRaw = 0, kScoresStats = 1, kScoresProbs = 2 };
+
+template <int NP, int DHP, bool VEC, int MODE>
+__global__ void __launch_bounds__(384, 1)
     mat_scores_kernel(const __grid_constant__ ScoresMaps maps, const ScoresArgs a) {
   using C = ScoresCfg<NP, DHP>;
   extern __shared__ uint8_t smem_raw[];
@@ -127,7 +142,7 @@ __global__ void __launch_bounds__(256, 1)
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(bar(C::B_ACCF + k), 1);
-      mbar_init(bar(C::B_ACCE + k), 4);
+      mbar_init(bar(C::B_ACCE + k), 8);  // the eight epilogue warps
     }
     mbar_init(bar(C::B_FIN), 1);
     *abort_flag = 0;
@@ -208,9 +223,13 @@ __global__ void __launch_bounds__(256, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ---------------- epilogue: TMEM -> staging -> coalesced row stores ----------------
-    const int q = warp & 3;  // TMEM lanes 32 q .. 32 q + 31 = tile rows
+    // Warps 4 + 4 h + q read TMEM lanes 32 q .. 32 q + 31 (tile rows) and the
+    // tile's columns 64 h .. 64 h + 63: two warps per sub-partition, so one's
+    // latency hides behind the other's work.
+    const int q = warp & 3;
+    const int half = (warp - 4) >> 2;
     const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    const uint32_t stg = sbase + C::OFF_STG + q * (32 * 128);
+    const uint32_t stg = sbase + C::OFF_STG + (warp - 4) * (32 * 128);
     const int rsub = lane >> 3, cq = lane & 7;  // staging read: row within a group of 4, 16-byte chunk
     for (long long n = 0; n < n_mine; ++n) {
       int e, i, j;
@@ -219,16 +238,54 @@ __global__ void __launch_bounds__(256, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(bar(C::B_ACCF + acc), static_cast<uint32_t>((n >> 1) & 1), w))) break;
       tc_fence_after();
       float* orow = a.out + static_cast<size_t>(e) * a.T * a.T;
-      for (int c = 0; c < 4; ++c) {
+      const int my_row = i * 128 + 32 * q + lane;  // this thread's TMEM lane
+      if constexpr (MODE == kScoresStats) {
+        // The half row in one load, this warp's share of the accumulator
+        // released at once; then its maximum (of S: c > 0) and the sum of
+        // 2^(c S - m) over the kept columns k <= lim, in four chains each. A
+        // half wholly above the diagonal gives (-inf, 0).
+        uint32_t rr[64];
+        tmem_ld64(tl + acc * 128 + 64 * half, rr);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_ACCE + acc));
+        const int lim = i == j ? my_row - (j * 128 + 64 * half) : 63;
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int k = 0; k < 64; ++k)
+          if (k <= lim) mx[k & 3] = fmaxf(mx[k & 3], __uint_as_float(rr[k]));
+        const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.c;
+        float sm[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < 64; ++k)
+          if (k <= lim) sm[k & 3] += ex2(fmaf(__uint_as_float(rr[k]), a.c, -m));
+        if (my_row < a.T)
+          a.part[((static_cast<size_t>(e) * a.T + my_row) * a.n_t + j) * 2 + half] =
+              make_float2(m, (sm[0] + sm[1]) + (sm[2] + sm[3]));
+        continue;
+      }
+      float lse2_row = 0.f;  // kScoresProbs
+      if constexpr (MODE == kScoresProbs)
+        if (my_row < a.T) lse2_row = a.lse2[static_cast<size_t>(e) * a.T + my_row];
+      for (int c = 2 * half; c < 2 * half + 2; ++c) {
         uint32_t r[32];
         tmem_ld32(tl + acc * 128 + 32 * c, r);
-        if (c == 3) {
+        if (c == 2 * half + 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(C::B_ACCE + acc));
         }
-        // On a diagonal tile a block whose columns all lie above this warp's rows is skipped.
-        if (i == j && c > q) continue;
+        // On a diagonal tile a block whose columns all lie above this warp's
+        // rows is skipped (its probabilities, all 0, are still written).
+        if (MODE == kScoresRaw && i == j && c > q) continue;
+        if constexpr (MODE == kScoresProbs) {
+          // Column j 128 + 32 c + k is kept for this row unless it lies above
+          // the diagonal, which only happens in the diagonal tile.
+          const int lim = i == j ? my_row - (j * 128 + 32 * c) : 31;  // kept: k <= lim
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            r[k] = __float_as_uint(k <= lim ? ex2(fmaf(__uint_as_float(r[k]), a.c, -lse2_row)) : 0.f);
+        }
         // This thread's row (32 fp32 = 8 chunks of 16 bytes), chunk index swizzled by row.
 #pragma unroll
         for (int u = 0; u < 8; ++u)

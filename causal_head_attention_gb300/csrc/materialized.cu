@@ -189,8 +189,52 @@ __global__ void causal_softmax_bwd_kernel(const float* __restrict__ p, float* __
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // [dP (backward) | fp32 storage: three bf16 parts each of Q, K, V, dO]
+// Row statistics of the two-pass forward, one warp per row (e, i): the
+// (max, sum) pairs, in base 2, of the two column halves of each of the row's
+// tiles j <= i / 128 (a half wholly above the diagonal holds -inf) merged into
+// LSE2 = m + log2 l (and lse = LSE2 ln 2 for the caller); then the row's
+// columns past its diagonal tile, which no tile of the probabilities pass
+// writes, are set to 0. VEC: T % 4 == 0, 16-byte stores.
+template <bool VEC>
+__global__ void probs_rows_kernel(const float2* __restrict__ part, float* __restrict__ lse2, float* __restrict__ lse,
+                                  float* __restrict__ probs, int64_t rows, int T, int n_t) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t r = blockIdx.x * int64_t(blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+    const int nt = int(r % T) / 128 + 1;  // tiles on or left of the diagonal
+    const float2* pr = part + r * n_t * 2;
+    float m = -INFINITY, l = 0.f;
+    for (int j = lane; j < 2 * nt; j += 32) {
+      const float2 x = pr[j];
+      if (x.x == -INFINITY) continue;
+      const float mn = fmaxf(m, x.x);
+      l = (m == -INFINITY ? 0.f : l * ex2(m - mn)) + x.y * ex2(x.x - mn);
+      m = mn;
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      const float mo = __shfl_xor_sync(FULL, m, off), lo = __shfl_xor_sync(FULL, l, off);
+      const float mn = fmaxf(m, mo);
+      l = (m == -INFINITY ? 0.f : l * ex2(m - mn)) + (mo == -INFINITY ? 0.f : lo * ex2(mo - mn));
+      m = mn;
+    }
+    if (lane == 0) {
+      const float v = m + __log2f(l);
+      lse2[r] = v;
+      lse[r] = v * kLn2;
+    }
+    float* row = probs + r * T;
+    if constexpr (VEC) {
+      for (int j = nt * 128 + 4 * lane; j < T; j += 128)
+        *reinterpret_cast<float4*>(row + j) = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      for (int j = nt * 128 + lane; j < T; j += 32) row[j] = 0.f;
+    }
+  }
+}
+
 struct Layout {
-  size_t dp, parts[4][3], total;
+  size_t dp, parts[4][3], stats, lse2, total;
 };
 enum { P_Q = 0, P_K = 1, P_V = 2, P_DO = 3 };
 
@@ -201,6 +245,12 @@ Layout layout(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, bool bf
   size_t at = 0;
   L.dp = at;
   at += round256(E * size_t(T) * T * 4);
+  // Forward: row statistics per tile and column half [E, T, n_t, 2] (max, sum)
+  // and the base-2 LSE [E, T].
+  L.stats = at;
+  at += round256(E * size_t(T) * size_t((T + 127) / 128) * 16);
+  L.lse2 = at;
+  at += round256(E * size_t(T) * 4);
   if (!bf16) {
     const size_t n[4] = {nq, nkv, nkv, nq};
     for (int t = 0; t < 4; ++t)
@@ -280,9 +330,9 @@ bool split3(const Ctx& c, const void* src, int t, int64_t n, std::string& err) {
 // out[e] (tiles j <= i) = A_e B_e^T: a (tensor ia, query heads) against b
 // (tensor ib, KV heads); bf16 storage reads the tensors themselves, fp32
 // storage their three bf16 parts.
-template <int NP, int DHP>
-bool launch_scores(const Ctx& c, const void* a_src, int ia, const void* b_src, int ib, float* out, int* status,
-                   unsigned long long timeout_ns, std::string& err) {
+template <int NP, int DHP, int MODE>
+bool launch_scores(const Ctx& c, const void* a_src, int ia, const void* b_src, int ib, float* out, float2* stats,
+                   const float* lse2, float cexp, int* status, unsigned long long timeout_ns, std::string& err) {
   using C = ScoresCfg<NP, DHP>;
   const MatParams& p = c.p;
   ScoresMaps maps{};
@@ -294,6 +344,9 @@ bool launch_scores(const Ctx& c, const void* a_src, int ia, const void* b_src, i
   }
   ScoresArgs a{};
   a.out = out;
+  a.part = stats;
+  a.lse2 = lse2;
+  a.c = cexp;
   a.status = status;
   a.timeout_ns = timeout_ns;
   a.B = int(p.B); a.Hq = int(p.Hq); a.Hkv = int(p.Hkv); a.T = int(p.T);
@@ -306,11 +359,11 @@ bool launch_scores(const Ctx& c, const void* a_src, int ia, const void* b_src, i
   const unsigned grid = unsigned(a.n_items < sms ? a.n_items : sms);
   static std::atomic<unsigned long long> set[2] = {};
   if (p.T % 4 == 0) {
-    auto k = mat_scores_kernel<NP, DHP, true>;
+    auto k = mat_scores_kernel<NP, DHP, true, MODE>;
     if (!ensure_smem(k, C::SMEM_BYTES, set[0], err)) return false;
     k<<<grid, C::NTHREADS, C::SMEM_BYTES, c.st>>>(maps, a);
   } else {
-    auto k = mat_scores_kernel<NP, DHP, false>;
+    auto k = mat_scores_kernel<NP, DHP, false, MODE>;
     if (!ensure_smem(k, C::SMEM_BYTES, set[1], err)) return false;
     k<<<grid, C::NTHREADS, C::SMEM_BYTES, c.st>>>(maps, a);
   }
@@ -351,13 +404,30 @@ bool launch_reduce(const Ctx& c, const float* x, const void* y_src, int iy, void
   return cuda_ok(cudaGetLastError(), "launch mat_reduce_kernel", err);
 }
 
-bool scores(const Ctx& c, const void* a_src, int ia, const void* b_src, int ib, float* out, std::string& err) {
+template <int MODE>
+bool scores(const Ctx& c, const void* a_src, int ia, const void* b_src, int ib, float* out, float2* stats,
+            const float* lse2, float cexp, std::string& err) {
   const MatParams& p = c.p;
   if (p.bf16)
-    return c.DHP == 64 ? launch_scores<1, 64>(c, a_src, ia, b_src, ib, out, p.status, p.timeout_ns, err)
-                       : launch_scores<1, 128>(c, a_src, ia, b_src, ib, out, p.status, p.timeout_ns, err);
-  return c.DHP == 64 ? launch_scores<3, 64>(c, a_src, ia, b_src, ib, out, p.status, p.timeout_ns, err)
-                     : launch_scores<3, 128>(c, a_src, ia, b_src, ib, out, p.status, p.timeout_ns, err);
+    return c.DHP == 64
+               ? launch_scores<1, 64, MODE>(c, a_src, ia, b_src, ib, out, stats, lse2, cexp, p.status, p.timeout_ns, err)
+               : launch_scores<1, 128, MODE>(c, a_src, ia, b_src, ib, out, stats, lse2, cexp, p.status, p.timeout_ns,
+                                             err);
+  return c.DHP == 64
+             ? launch_scores<3, 64, MODE>(c, a_src, ia, b_src, ib, out, stats, lse2, cexp, p.status, p.timeout_ns, err)
+             : launch_scores<3, 128, MODE>(c, a_src, ia, b_src, ib, out, stats, lse2, cexp, p.status, p.timeout_ns, err);
+}
+
+bool launch_probs_rows(const Ctx& c, float* lse, float* probs, std::string& err) {
+  const float2* stats = reinterpret_cast<const float2*>(c.ws + c.L.stats);
+  float* lse2 = reinterpret_cast<float*>(c.ws + c.L.lse2);
+  const int64_t rows = int64_t(c.E) * c.T;
+  const int n_t = (c.T + 127) / 128;
+  if (c.T % 4 == 0)
+    probs_rows_kernel<true><<<grid_for(rows, 8), 256, 0, c.st>>>(stats, lse2, lse, probs, rows, c.T, n_t);
+  else
+    probs_rows_kernel<false><<<grid_for(rows, 8), 256, 0, c.st>>>(stats, lse2, lse, probs, rows, c.T, n_t);
+  return cuda_ok(cudaGetLastError(), "launch probs_rows_kernel", err);
 }
 
 template <bool TRANS>
@@ -418,9 +488,17 @@ bool materialized_fwd(const MatParams& p, cudaStream_t st, std::string& err) {
       return false;
   }
   const float scale = float(1.0 / __builtin_sqrt(double(p.Dh)));
-  // S = Q K^T into the probability rows (kept tiles only), then the softmax in place.
-  if (!scores(c, p.q, P_Q, p.k, P_K, p.probs, err)) return false;
-  if (!launch_softmax(p.probs, p.lse, int64_t(c.E) * c.T, c.T, scale, st, err)) return false;
+  const float cexp = float(double(scale) * 1.4426950408889634);  // scores in base 2
+  // Two passes over S = Q K^T (kept tiles), which the tensor cores recompute
+  // instead of storing: (1) per-tile row statistics; then each row's LSE and
+  // the zero columns past its diagonal tile; (2) P = 2^(c S - LSE2) written
+  // into the kept tiles. The probabilities are written once and never read
+  // back before O = P V.
+  float2* stats = reinterpret_cast<float2*>(c.ws + c.L.stats);
+  const float* lse2 = reinterpret_cast<const float*>(c.ws + c.L.lse2);
+  if (!scores<kScoresStats>(c, p.q, P_Q, p.k, P_K, nullptr, stats, nullptr, cexp, err)) return false;
+  if (!launch_probs_rows(c, p.lse, p.probs, err)) return false;
+  if (!scores<kScoresProbs>(c, p.q, P_Q, p.k, P_K, p.probs, nullptr, lse2, cexp, err)) return false;
   // O = P V.
   return reduce<false>(c, p.probs, p.v, P_V, p.out, err);
 }
@@ -437,7 +515,7 @@ bool materialized_bwd(const MatParams& p, cudaStream_t st, std::string& err) {
   const float scale = float(1.0 / __builtin_sqrt(double(p.Dh)));
   float* dp = reinterpret_cast<float*>(c.ws + c.L.dp);
   // dP = dO V^T (kept tiles), then dS (with respect to the unscaled scores) in place.
-  if (!scores(c, p.dout, P_DO, p.v, P_V, dp, err)) return false;
+  if (!scores<kScoresRaw>(c, p.dout, P_DO, p.v, P_V, dp, nullptr, nullptr, 0.f, err)) return false;
   // dS only where the products read it: each row's causal 128-column tiles.
   if (!launch_softmax_bwd(p.probs, dp, p.dprobs, int64_t(c.E) * c.T, c.T, 128, scale, st, err)) return false;
   // dQ = dS K;  dK = dS^T Q;  dV = P^T dO  (the last two summed over each group).

@@ -257,7 +257,10 @@ RCA_API rca_status rca_attn_bwd_qkv(const void* qkv, const void* out, const floa
  *   dP = dout V^T + dprobs;  dS = probs * (dP - rowsum(probs * dP));
  *   dq = scale dS K;  dk = scale dS^T Q;  dv = probs^T dout  (dk, dv summed over
  *   the query heads of a KV head). The backward reads the probabilities the
- *   forward stored; it does not recompute them.
+ *   forward stored; it does not recompute them. The forward forms S twice on
+ *   the tensor cores instead of storing it (pass 1: row statistics, giving
+ *   lse; pass 2: probs written from S and lse), then computes out from the
+ *   stored probs.
  *
  * Layouts: q, out, dout, dq [B,T,Hq,Dh] and k, v, dk, dv [B,T,Hkv,Dh] in the
  * storage dtype (as rca_attn_fwd); probs, dprobs [B,Hq,T,T] float32 (4*B*Hq*T*T
