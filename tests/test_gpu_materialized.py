@@ -114,6 +114,36 @@ def test_multi_item_every_output(case):
         assert e <= GRAD_TOL[dt], f"{name} {nm}: {e:.3g}"
 
 
+@pytest.mark.parametrize("case", [("nan_bf16_t300", 1, 2, 1, 300, 64, "bf16"), ("nan_fp32_t130", 1, 2, 2, 130, 32, "fp32")],
+                         ids=lambda c: c[0])
+def test_forward_writes_every_output_element(case):
+    """Every element of out, probs and lse is written by the forward (the
+    kept tiles by the probabilities pass, the rest of each row by the row
+    pass): buffers filled with NaN beforehand must come back equal to the
+    oracle, with exact zeros above the diagonal. T = 300 takes the 16-byte
+    path, T = 130 the scalar one."""
+    name, B, Hq, Hkv, T, Dh, dt = case
+    q, k, v, _ = make_inputs(small(name, B, Hq, Hkv, T, Dh, dt, seed=5))
+    dev = torch.device("cuda:0")
+    qd, kd, vd = (x.to(dev) for x in (q, k, v))
+    out = torch.full_like(qd, float("nan"))
+    probs = torch.full((B, Hq, T, T), float("nan"), device=dev)
+    lse = torch.full((B, Hq, T), float("nan"), device=dev)
+    ws = torch.full((rca.rca_attn_materialized_workspace_size(B, Hq, Hkv, T, Dh, qd.dtype),), 255, dtype=torch.uint8,
+                    device=dev)
+    rca.rca_attn_materialized_fwd(qd, kd, vd, out, probs, lse, ws)
+    rca.rca_stream_status()
+    q64, k64, v64 = (to64(x) for x in (q, k, v))
+    o_ref, p_ref, l_ref = oracle.attention_probs(q64, k64, v64)
+    check_probs(name, probs, lse, p_ref, l_ref)
+    o = to64(out)
+    assert not np.isnan(o).any(), f"{name}: unwritten output rows"
+    if dt == "bf16":
+        assert np.all(np.abs(o - o_ref) <= 2.0 ** -8 * np.abs(o_ref) + 1e-5), name
+    else:
+        assert rel_fro(o, o_ref) <= GRAD_TOL["fp32"], name
+
+
 def test_zero_dprobs_equals_none():
     w = small("mat_zero_dp", 1, 2, 2, 64, 64, "bf16", seed=3)
     q, k, v, do = make_inputs(w)
