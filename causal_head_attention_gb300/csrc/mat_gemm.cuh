@@ -34,10 +34,10 @@
 // directions, see reduce_deal); roles are a TMA warp, a single-thread MMA
 // issuer, a TMEM owner, epilogue warps (TMEM lanes 32 q .. 32 q + 31: four in
 // the reduce kernel; eight in the scores kernel, two per lane quarter, each
-// with one 64-column half of the tile) and, in the reduce kernel, eight
-// converting warps that load X straight from global memory (two chunks in
-// flight per thread) and store its bf16 parts in the swizzled layout the MMA
-// reads. Two TMEM accumulators alternate between items so one item's
+// with one 64-column half of the tile) and, in the reduce kernel, sixteen
+// converting warps that load X straight from global memory (the next chunk's
+// loads in flight while the current one is stored) and store its bf16 parts
+// in the swizzled layout the MMA reads. Two TMEM accumulators alternate between items so one item's
 // epilogue overlaps the next item's products. Every wait is time-bounded.
 #pragma once
 
@@ -330,8 +330,10 @@ __global__ void __launch_bounds__(384, 1)
 // ---------------------------------------------------------------------------
 template <bool TRANS, int NPY, int DHP>
 struct ReduceCfg {
-  static constexpr int NTHREADS = 512;
-  static constexpr int NCONV = 8;                       // converting warps 8 .. 15
+  static constexpr int NCONV = 16;                      // converting warps 8 .. 8 + NCONV - 1
+  static constexpr int CONV_THREADS = 32 * NCONV;
+  static constexpr int SEG = 2048 / CONV_THREADS;      // 16-byte segments of a chunk per converting thread
+  static constexpr int NTHREADS = 256 + CONV_THREADS;
   static constexpr int DP = DHP / 64;
   static constexpr int XPART = 128 * 64 * 2;            // 128 (M) x 64 (K) bf16 = 16 KB
   static constexpr int YPANEL = 64 * 128;               // 64 rows (K) x 128 bytes
@@ -399,7 +401,7 @@ __device__ __forceinline__ int reduce_count(int c, int n_items, int G) {
 }
 
 template <bool TRANS, int NPY, int DHP>
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(ReduceCfg<TRANS, NPY, DHP>::NTHREADS, 1)
     mat_reduce_kernel(const __grid_constant__ ReduceMaps maps, const ReduceArgs a) {
   using C = ReduceCfg<TRANS, NPY, DHP>;
   extern __shared__ uint8_t smem_raw[];
@@ -518,19 +520,19 @@ __global__ void __launch_bounds__(512, 1)
     // ---------------- converting warps: X (fp32, global) -> bf16 parts (shared) ----------------
     // Per 64-position chunk, 2048 16-byte segments: rows: 128 rows x 16 segments
     // of K; columns: 64 rows (K) x 32 segments of M. Thread ct takes segments
-    // ct + 256 v, v = 0..7; the next chunk's loads are issued before this
-    // chunk's stores.
+    // ct + CONV_THREADS v, v < SEG; the next chunk's loads are issued before
+    // this chunk's stores.
     const int ct = threadIdx.x - 256;
     long long u = 0;
     bool ok = true;
-    float4 cur[8], nxt[8];
+    float4 cur[C::SEG], nxt[C::SEG];
     // Loads of chunk (item n, head r, chunk c) into regs.
-    auto load = [&](float4 (&rg)[8], int b, int hd, int t, int r, int c) {
+    auto load = [&](float4 (&rg)[C::SEG], int b, int hd, int t, int r, int c) {
       const int e = TRANS ? b * a.Hq + hd * a.group + r : b * a.Hq + hd;
       const float* xe = a.x + static_cast<size_t>(e) * a.T * a.T;
 #pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        const int sg = ct + 256 * v;
+      for (int v = 0; v < C::SEG; ++v) {
+        const int sg = ct + C::CONV_THREADS * v;
         int row, col;
         if constexpr (TRANS) {
           row = 128 * t + 64 * c + (sg >> 5);  // query position i
@@ -592,8 +594,8 @@ __global__ void __launch_bounds__(512, 1)
       }
       const uint32_t xb = sbase + s * C::STAGE;
 #pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        const int sg = ct + 256 * v;
+      for (int v = 0; v < C::SEG; ++v) {
+        const int sg = ct + C::CONV_THREADS * v;
         uint32_t off;
         if constexpr (TRANS) {
           // MN-major: row = K (query within chunk), 64 M elements per 128-byte row, M panels 8 KB apart.
@@ -616,7 +618,7 @@ __global__ void __launch_bounds__(512, 1)
       ++u;
       cc = nc;
 #pragma unroll
-      for (int v = 0; v < 8; ++v) cur[v] = nxt[v];
+      for (int v = 0; v < C::SEG; ++v) cur[v] = nxt[v];
       if (nc.valid) advance(nc);
     }
   } else if (warp >= 4) {
