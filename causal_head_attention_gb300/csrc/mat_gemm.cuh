@@ -33,8 +33,9 @@
 // reduce kernel's items differ in length and are dealt in alternating
 // directions, see reduce_deal); roles are a TMA warp, a single-thread MMA
 // issuer, a TMEM owner, epilogue warps (TMEM lanes 32 q .. 32 q + 31: four in
-// the reduce kernel; eight in the scores kernel, two per lane quarter, each
-// with one 64-column half of the tile) and, in the reduce kernel, sixteen
+// the reduce kernel; in the scores kernel four per lane quarter with bf16
+// operands, one 32-column block of the tile each, or two with fp32 operands,
+// one 64-column half each) and, in the reduce kernel, sixteen
 // converting warps that load X straight from global memory (the next chunk's
 // loads in flight while the current one is stored) and store its bf16 parts
 // in the swizzled layout the MMA reads. Two TMEM accumulators alternate between items so one item's
@@ -66,11 +67,17 @@ struct Products {
 // ---------------------------------------------------------------------------
 template <int NP, int DHP>
 struct ScoresCfg {
-  static constexpr int NTHREADS = 384;                 // warps 0-3 roles, 4-11 epilogue
+  // Epilogue warps: four per TMEM lane quarter (one 32-column block of the
+  // tile each) with bf16 operands, two (one 64-column half each) with the
+  // three-part fp32 operands, whose stages leave less room for staging.
+  static constexpr int NEPI = NP == 1 ? 16 : 8;
+  static constexpr int NGRP = NEPI / 4;                // column groups of a tile
+  static constexpr int GCOLS = 128 / NGRP;             // columns per epilogue warp
+  static constexpr int NTHREADS = 128 + 32 * NEPI;     // warps 0-3 roles, then the epilogue
   static constexpr int DP = DHP / 64;                  // 64-column panels across the head width
   static constexpr int PART = DP * kPanel64;           // one bf16 part of a 128-row tile
   static constexpr int STAGE = 2 * NP * PART;          // A parts then B parts
-  static constexpr int STAGING = 8 * 32 * 128;         // eight warps x 32 rows x 128 bytes
+  static constexpr int STAGING = NEPI * 32 * 128;      // per epilogue warp: 32 rows x 128 bytes
   static constexpr int SMEM_LIMIT = 232448;
   static constexpr int BAR_BYTES = 256;
   static constexpr int NS_FIT = (SMEM_LIMIT - 1024 - BAR_BYTES - STAGING) / STAGE;
@@ -87,7 +94,7 @@ struct ScoresCfg {
 
 struct ScoresArgs {
   float* out;         // [E, T, T]
-  float2* part;       // row statistics mode: (max, sum) of row r, tile j, column half h at [e, r, j, h]
+  float2* part;       // row statistics mode: (max, sum) of row r, tile j, column group g at [e, r, j, g]
   const float* lse2;  // probabilities mode: base-2 LSE of each row, [E, T]
   float c;            // both modes: scale * log2(e)
   int* status;
@@ -123,7 +130,7 @@ __device__ __forceinline__ void scores_item(const ScoresArgs& a, long long idx, 
 enum { kScoresRaw = 0, kScoresStats = 1, kScoresProbs = 2 };
 
 template <int NP, int DHP, bool VEC, int MODE>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(ScoresCfg<NP, DHP>::NTHREADS, 1)
     mat_scores_kernel(const __grid_constant__ ScoresMaps maps, const ScoresArgs a) {
   using C = ScoresCfg<NP, DHP>;
   extern __shared__ uint8_t smem_raw[];
@@ -142,7 +149,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(bar(C::B_ACCF + k), 1);
-      mbar_init(bar(C::B_ACCE + k), 8);  // the eight epilogue warps
+      mbar_init(bar(C::B_ACCE + k), C::NEPI);  // the epilogue warps
     }
     mbar_init(bar(C::B_FIN), 1);
     *abort_flag = 0;
@@ -223,11 +230,11 @@ __global__ void __launch_bounds__(384, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ---------------- epilogue: TMEM -> staging -> coalesced row stores ----------------
-    // Warps 4 + 4 h + q read TMEM lanes 32 q .. 32 q + 31 (tile rows) and the
-    // tile's columns 64 h .. 64 h + 63: two warps per sub-partition, so one's
-    // latency hides behind the other's work.
+    // Warps 4 + 4 g + q read TMEM lanes 32 q .. 32 q + 31 (tile rows) and the
+    // tile's column group g (GCOLS columns): several warps per sub-partition,
+    // so one's latency hides behind the others' work.
     const int q = warp & 3;
-    const int half = (warp - 4) >> 2;
+    const int grp = (warp - 4) >> 2;
     const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const uint32_t stg = sbase + C::OFF_STG + (warp - 4) * (32 * 128);
     const int rsub = lane >> 3, cq = lane & 7;  // staging read: row within a group of 4, 16-byte chunk
@@ -240,37 +247,41 @@ __global__ void __launch_bounds__(384, 1)
       float* orow = a.out + static_cast<size_t>(e) * a.T * a.T;
       const int my_row = i * 128 + 32 * q + lane;  // this thread's TMEM lane
       if constexpr (MODE == kScoresStats) {
-        // The half row in one load, this warp's share of the accumulator
-        // released at once; then its maximum (of S: c > 0) and the sum of
-        // 2^(c S - m) over the kept columns k <= lim, in four chains each. A
-        // half wholly above the diagonal gives (-inf, 0).
-        uint32_t rr[64];
-        tmem_ld64(tl + acc * 128 + 64 * half, rr);
+        // The group's columns in one load, this warp's share of the
+        // accumulator released at once; then their maximum (of S: c > 0) and
+        // the sum of 2^(c S - m) over the kept columns k <= lim, in four
+        // chains each. A group wholly above the diagonal gives (-inf, 0).
+        uint32_t rr[C::GCOLS];
+        if constexpr (C::GCOLS == 64)
+          tmem_ld64(tl + acc * 128 + C::GCOLS * grp, rr);
+        else
+          tmem_ld32(tl + acc * 128 + C::GCOLS * grp, rr);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_ACCE + acc));
-        const int lim = i == j ? my_row - (j * 128 + 64 * half) : 63;
+        const int lim = i == j ? my_row - (j * 128 + C::GCOLS * grp) : C::GCOLS - 1;
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int k = 0; k < 64; ++k)
+        for (int k = 0; k < C::GCOLS; ++k)
           if (k <= lim) mx[k & 3] = fmaxf(mx[k & 3], __uint_as_float(rr[k]));
         const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.c;
         float sm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int k = 0; k < 64; ++k)
+        for (int k = 0; k < C::GCOLS; ++k)
           if (k <= lim) sm[k & 3] += ex2(fmaf(__uint_as_float(rr[k]), a.c, -m));
         if (my_row < a.T)
-          a.part[((static_cast<size_t>(e) * a.T + my_row) * a.n_t + j) * 2 + half] =
+          a.part[((static_cast<size_t>(e) * a.T + my_row) * a.n_t + j) * C::NGRP + grp] =
               make_float2(m, (sm[0] + sm[1]) + (sm[2] + sm[3]));
         continue;
       }
       float lse2_row = 0.f;  // kScoresProbs
       if constexpr (MODE == kScoresProbs)
         if (my_row < a.T) lse2_row = a.lse2[static_cast<size_t>(e) * a.T + my_row];
-      for (int c = 2 * half; c < 2 * half + 2; ++c) {
+      constexpr int CPW = C::GCOLS / 32;  // 32-column blocks per epilogue warp
+      for (int c = CPW * grp; c < CPW * grp + CPW; ++c) {
         uint32_t r[32];
         tmem_ld32(tl + acc * 128 + 32 * c, r);
-        if (c == 2 * half + 1) {
+        if (c == CPW * grp + CPW - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(C::B_ACCE + acc));

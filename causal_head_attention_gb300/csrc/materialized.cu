@@ -190,21 +190,21 @@ size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // [dP (backward) | fp32 storage: three bf16 parts each of Q, K, V, dO]
 // Row statistics of the two-pass forward, one warp per row (e, i): the
-// (max, sum) pairs, in base 2, of the two column halves of each of the row's
-// tiles j <= i / 128 (a half wholly above the diagonal holds -inf) merged into
+// (max, sum) pairs, in base 2, of the ngrp column groups of each of the row's
+// tiles j <= i / 128 (a group wholly above the diagonal holds -inf) merged into
 // LSE2 = m + log2 l (and lse = LSE2 ln 2 for the caller); then the row's
 // columns past its diagonal tile, which no tile of the probabilities pass
 // writes, are set to 0. VEC: T % 4 == 0, 16-byte stores.
 template <bool VEC>
 __global__ void probs_rows_kernel(const float2* __restrict__ part, float* __restrict__ lse2, float* __restrict__ lse,
-                                  float* __restrict__ probs, int64_t rows, int T, int n_t) {
+                                  float* __restrict__ probs, int64_t rows, int T, int n_t, int ngrp) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
   for (int64_t r = blockIdx.x * int64_t(blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
     const int nt = int(r % T) / 128 + 1;  // tiles on or left of the diagonal
-    const float2* pr = part + r * n_t * 2;
+    const float2* pr = part + r * n_t * ngrp;
     float m = -INFINITY, l = 0.f;
-    for (int j = lane; j < 2 * nt; j += 32) {
+    for (int j = lane; j < ngrp * nt; j += 32) {
       const float2 x = pr[j];
       if (x.x == -INFINITY) continue;
       const float mn = fmaxf(m, x.x);
@@ -245,10 +245,10 @@ Layout layout(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t Dh, bool bf
   size_t at = 0;
   L.dp = at;
   at += round256(E * size_t(T) * T * 4);
-  // Forward: row statistics per tile and column half [E, T, n_t, 2] (max, sum)
-  // and the base-2 LSE [E, T].
+  // Forward: row statistics per tile and column group [E, T, n_t, <= 4] (max,
+  // sum) and the base-2 LSE [E, T].
   L.stats = at;
-  at += round256(E * size_t(T) * size_t((T + 127) / 128) * 16);
+  at += round256(E * size_t(T) * size_t((T + 127) / 128) * 4 * 8);
   L.lse2 = at;
   at += round256(E * size_t(T) * 4);
   if (!bf16) {
@@ -423,10 +423,15 @@ bool launch_probs_rows(const Ctx& c, float* lse, float* probs, std::string& err)
   float* lse2 = reinterpret_cast<float*>(c.ws + c.L.lse2);
   const int64_t rows = int64_t(c.E) * c.T;
   const int n_t = (c.T + 127) / 128;
+  // Column groups per tile of the statistics pass (the scores kernel's epilogue layout).
+  const int ngrp = c.p.bf16 ? ScoresCfg<1, 64>::NGRP : ScoresCfg<3, 64>::NGRP;
+  static_assert(ScoresCfg<1, 64>::NGRP == ScoresCfg<1, 128>::NGRP && ScoresCfg<3, 64>::NGRP == ScoresCfg<3, 128>::NGRP &&
+                    ScoresCfg<1, 64>::NGRP <= 4 && ScoresCfg<3, 64>::NGRP <= 4,
+                "column groups per tile: as the workspace sizes them");
   if (c.T % 4 == 0)
-    probs_rows_kernel<true><<<grid_for(rows, 8), 256, 0, c.st>>>(stats, lse2, lse, probs, rows, c.T, n_t);
+    probs_rows_kernel<true><<<grid_for(rows, 8), 256, 0, c.st>>>(stats, lse2, lse, probs, rows, c.T, n_t, ngrp);
   else
-    probs_rows_kernel<false><<<grid_for(rows, 8), 256, 0, c.st>>>(stats, lse2, lse, probs, rows, c.T, n_t);
+    probs_rows_kernel<false><<<grid_for(rows, 8), 256, 0, c.st>>>(stats, lse2, lse, probs, rows, c.T, n_t, ngrp);
   return cuda_ok(cudaGetLastError(), "launch probs_rows_kernel", err);
 }
 
