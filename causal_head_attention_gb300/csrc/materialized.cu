@@ -188,7 +188,6 @@ __global__ void causal_softmax_bwd_kernel(const float* __restrict__ p, float* __
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// [dP (backward) | fp32 storage: three bf16 parts each of Q, K, V, dO]
 // Row statistics of the two-pass forward, one warp per row (e, i): the
 // (max, sum) pairs, in base 2, of the ngrp column groups of each of the row's
 // tiles j <= i / 128 (a group wholly above the diagonal holds -inf) merged into
@@ -233,6 +232,8 @@ __global__ void probs_rows_kernel(const float2* __restrict__ part, float* __rest
   }
 }
 
+// Workspace: [dP (backward) | row statistics, LSE2 (forward) | fp32 storage:
+// three bf16 parts each of Q, K, V, dO]
 struct Layout {
   size_t dp, parts[4][3], stats, lse2, total;
 };
