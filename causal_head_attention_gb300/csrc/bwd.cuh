@@ -222,7 +222,8 @@ __device__ __forceinline__ void preprocess_varlen_block(const PreArgs& a, int b,
 // ----------------------------------------------------------------------------
 // dQ convert
 // ----------------------------------------------------------------------------
-// Grid-stride over float4 groups, four loads in flight per thread per pass.
+// Grid-stride over float4 groups, up to four loads in flight per thread per
+// pass (the host launches one group per thread).
 // STRIDED: the output rows (one position, all heads) are dq_row4 groups of 4
 // elements apart instead of row4 (a row of a fused QKV gradient buffer).
 template <bool F32, bool STRIDED>

@@ -741,6 +741,8 @@ rca_status varlen_convert(void* dq, const int* lens, int64_t B, int64_t Hq, int6
                           const void* ws, const WsLayout& L, cudaStream_t st) {
   const float* acc = reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws) + L.dq_off);
   const long long row4 = Hq * Dh / 4;
+  // One resident wave of blocks looping over four groups per thread (one
+  // group per thread measured slower here: most of its blocks cover padding).
   int sms = 0;
   RCA_CHECK(sm_count(&sms));
   const int64_t want = (T * row4 + 1023) / 1024, cap = std::max<int64_t>(1, int64_t(sms) * 8 / B);
@@ -810,10 +812,11 @@ rca_status do_convert(void* dq, int64_t B, int64_t Hq, int64_t T, int64_t Dh, rc
   if (dqs == 0) dqs = Hq * Dh;  // elements between consecutive positions of dq
   const float* acc = reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws) + L.dq_off);
   const long long n4 = (long long)(B * T * Hq * Dh / 4);
-  int sms = 0;
-  RCA_CHECK(sm_count(&sms));
-  long long want = (n4 + 1023) / 1024;  // four float4 groups per thread
-  const long long cap = (long long)sms * 8;
+  // One float4 group per thread, every group in flight at once: inside the
+  // training step this measured 7 us faster at B4 H16 T2048 Dh64 than one
+  // resident wave of blocks looping over four groups per thread.
+  const long long want = (n4 + 255) / 256;
+  const long long cap = (1LL << 31) - 1;
   const unsigned grid = unsigned(want < cap ? (want > 0 ? want : 1) : cap);
   const float scale = float(1.0 / std::sqrt(double(Dh)));
   const long long row4 = Hq * Dh / 4, dq_row4 = dqs / 4;
