@@ -717,21 +717,18 @@ def bench_materialized(w, dev, stream, steps, warmup, P):
     smb_ms = timed(lambda i: rca.rca_causal_softmax_bwd(s[i % 2], g[i % 2], None, scale, stream), steps)
     # The backward call runs the VJP tiled by 128 columns (dS only where its products read it).
     smbt_ms = timed(lambda i: rca.rca_causal_softmax_bwd_tiled(s[i % 2], g[i % 2], None, 128, scale, stream), steps)
-    tri = E * T * (T + 1) // 2 * 4  # bytes of the kept (lower) half of the rows
-    full = E * T * T * 4
-    sm_bytes = tri + full + E * T * 4       # read the kept entries, write whole rows and LSE
-    smb_bytes = 2 * tri + full              # read P and dP where kept, write whole rows
-    # tiled by 128: row i written up to the end of its diagonal tile
-    smbt_bytes = 2 * tri + E * sum(min(T, 128 * (i // 128 + 1)) for i in range(T)) * 4
+    mb = materialized_bytes(E, T)
+    full = mb["full"]
+    sm_bytes, smb_bytes, smbt_bytes = mb["softmax"], mb["softmax_bwd"], mb["softmax_bwd_tiled128"]
     # Forward call: the probabilities written once as whole rows and read once by
     # P V (S is formed twice on the tensor cores and never stored); the
     # [B,T,H,Dh] operands are small beside them.
-    fwd_bytes = full + tri
+    fwd_bytes = mb["fwd"]
     # Backward products over the kept triangle (dP, dQ, dK, dV), each 2 * Dh FLOPs
     # per kept score and one [T, T] triangle streamed once (dP written; dS, dS, P
     # read): the backward call minus the tiled VJP it runs, timed alone.
     prod_flops = 2.0 * w.Dh * (E * T * (T + 1) / 2) * 4
-    prod_bytes = 4 * tri
+    prod_bytes = mb["bwd_products"]
     prod_ms = bwd_ms - smbt_ms
 
     def roof(nbytes, ms):
@@ -754,6 +751,26 @@ def bench_materialized(w, dev, stream, steps, warmup, P):
         "note": "all kernels are this library's: tensor-core products over the kept triangle of tiles only, "
                 "the fused causal softmax and its VJP",
         "gpu_launches": {"per_fwd": 4 if w.dtype == "bf16" else 7, "per_bwd": 5 if w.dtype == "bf16" else 9},
+    }
+
+
+def materialized_bytes(E: int, T: int) -> dict:
+    """Algorithmic HBM bytes of the materialised path's pieces on E [T, T] fp32
+    row blocks: `tri` the kept (lower) half, `full` whole rows; the forward
+    call writes the probabilities once (whole rows) and reads them once (P V);
+    the standalone softmax reads the kept half and writes whole rows and LSE;
+    its VJP reads P and dP where kept and writes whole rows, or, tiled by 128,
+    row i up to the end of its diagonal tile; the four backward products each
+    stream one kept triangle."""
+    tri = E * T * (T + 1) // 2 * 4
+    full = E * T * T * 4
+    return {
+        "tri": tri, "full": full,
+        "fwd": full + tri,
+        "softmax": tri + full + E * T * 4,
+        "softmax_bwd": 2 * tri + full,
+        "softmax_bwd_tiled128": 2 * tri + E * sum(min(T, 128 * (i // 128 + 1)) for i in range(T)) * 4,
+        "bwd_products": 4 * tri,
     }
 
 

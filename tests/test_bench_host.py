@@ -32,6 +32,25 @@ def test_decode_bytes_by_hand():
     assert bench.decode_bytes(w32, lens) == 2 * kv + 2 * q_out + lse + table + seq_lens
 
 
+def test_materialized_bytes_by_brute_force():
+    """Each figure counted element by element on small [T, T] blocks: kept
+    entries j <= i, whole rows, and the tiled VJP's columns j < min(T, 128
+    (i // 128 + 1)), with T past one tile and ragged."""
+    for E, T in ((1, 1), (2, 5), (3, 130), (1, 300)):
+        kept = sum(i + 1 for i in range(T)) * E * 4
+        rows = E * T * T * 4
+        tiled = E * 4 * sum(len([j for j in range(T) if j < min(T, 128 * (i // 128 + 1))]) for i in range(T))
+        mb = bench.materialized_bytes(E, T)
+        assert mb["tri"] == kept and mb["full"] == rows
+        assert mb["fwd"] == rows + kept
+        assert mb["softmax"] == kept + rows + E * T * 4
+        assert mb["softmax_bwd"] == 2 * kept + rows
+        assert mb["softmax_bwd_tiled128"] == 2 * kept + tiled
+        assert mb["bwd_products"] == 4 * kept
+    # the tiled VJP writes less than whole rows once a row has a tile past its diagonal one
+    assert bench.materialized_bytes(1, 300)["softmax_bwd_tiled128"] < bench.materialized_bytes(1, 300)["softmax_bwd"]
+
+
 def test_aggregate_rate_counts_every_rank_over_the_slowest():
     assert bench.aggregate_tflops(1e12, 1, 1000.0) == pytest.approx(1.0)
     assert bench.aggregate_tflops(1e12, 4, 500.0) == pytest.approx(8.0)
